@@ -1,0 +1,224 @@
+/*
+ * mtp.h -- C ABI of the MTP self-speculative draft-and-verify step (one GPU,
+ * sm_103a).
+ *
+ * The operations come from these pages (title, section):
+ *   "MTP (Multi-Token Prediction)" (speculators user guide), "Architecture":
+ *     the MTP head normalises the verifier's hidden state and the token
+ *     embedding separately, concatenates them, projects 2H -> H, runs one
+ *     standard decoder layer (attention + MLP) and applies the shared LM head;
+ *     its output hidden state feeds the next step recursively.
+ *   "How OpenVINO MTP Speculative Decoding Works Internally", "The MTP
+ *     inputs" (hidden_states, inputs_embeds, attention metadata, position_ids,
+ *     the MTP KV cache), "Shared embeddings reduce duplication" (the head
+ *     reads the target's embedding table), "Stateful execution" (the
+ *     one-layer cache is updated in place on every invocation).
+ *   "Speculative Decoding" (OpenVINO GenAI), "Overview": greedy
+ *     verification keeps the drafts the target would have produced and
+ *     replaces the first divergent one by the target's token;
+ *     "Tree Drafting" step 4 and "Prefix Caching with Speculative Decoding":
+ *     caches advance to the accepted prefix or return to a common prefix.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers unless stated, row-major,
+ *     owned by the caller.  The library borrows them for the duration of the
+ *     asynchronous work it enqueues; it never frees them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; outputs are valid once the
+ *     stream has been synchronised.
+ *   - A host-detectable argument error returns MTP_ERR_INVALID and enqueues
+ *     nothing.  Errors found on the device (inconsistent device-side lengths,
+ *     KV capacity, a bounded wait that ran out) set a device error word, leave
+ *     the affected outputs undefined, and are reported by
+ *     mtp_get_device_error().
+ *   - dtype MTP_DTYPE_BF16: weights, KV pools, hidden/embeds and verify
+ *     logits are bf16 (uint16 bit patterns); MTP_DTYPE_F32: all float32.
+ *     Draft logits and hidden_out are always float32.
+ */
+#ifndef MTP_H_
+#define MTP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MTP_OK = 0,
+  MTP_ERR_INVALID = 1,      /* bad host argument; nothing enqueued            */
+  MTP_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed           */
+  MTP_ERR_OOM = 3,          /* workspace allocation failed                    */
+  MTP_ERR_CAPACITY = 4,     /* device: KV slot outside block table / pool     */
+  MTP_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out                 */
+  MTP_ERR_DEVICE_ARGS = 6   /* device: inconsistent lengths/offsets/pending   */
+} mtp_status;
+
+typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
+
+/* Shape of the MTP head and the limits of one context. */
+typedef struct {
+  int hidden;            /* H; multiple of 8                                  */
+  int n_q_heads;         /* query heads; multiple of n_kv_heads               */
+  int n_kv_heads;        /* key/value heads (grouped-query attention)         */
+  int head_dim;          /* 64 or 128                                         */
+  int ffn;               /* SwiGLU inner size F; multiple of 8                */
+  int vocab;             /* V (rows of the embedding table / LM head)         */
+  float eps;             /* RMSNorm epsilon                                   */
+  float rope_theta;      /* rotary base                                       */
+  int dtype;             /* mtp_dtype                                         */
+  int max_batch;         /* largest B of any call                             */
+  int max_k;             /* largest draft count K of any call (1..100)        */
+  int block_size;        /* KV tokens per paged block; must be 16             */
+  int max_pos;           /* positions + K - 1 must stay below this            */
+} mtp_config;
+
+/* Borrowed head weights (device pointers, layouts [out, in] row-major).
+ * Norm weights are [H].  w_eh is [H, 2H]: columns [0, H) act on the
+ * normalised hidden state, [H, 2H) on the normalised embedding.  w_q is
+ * [n_q*d, H], w_k and w_v [n_kv*d, H], w_o [H, n_q*d], w_gate and w_up [F, H],
+ * w_down [H, F].  embed is the shared [V, H] token-embedding table; lm_head is
+ * [V, H] and may equal embed (tied). */
+typedef struct {
+  const void *w_norm_h, *w_norm_e, *w_eh;
+  const void *w_norm_in, *w_q, *w_k, *w_v, *w_o;
+  const void *w_norm_post, *w_gate, *w_up, *w_down;
+  const void *w_norm_f, *embed, *lm_head;
+} mtp_weights;
+
+/* The single-layer MTP KV cache, paged (device pointers, borrowed).
+ *   k_pool, v_pool: [num_blocks, n_kv, block_size, head_dim] in the dtype.
+ *   block_table:    [B, max_blocks] int32; slot s of request b lives in block
+ *                   block_table[b*max_blocks + s/block_size] at row s%block_size.
+ *   seq_len:        [B] int32 committed entries per request.
+ *   pending:        [B] int32 drafted, not yet committed entries.
+ * Invariant kept by every entry point: each pool slot that no request holds
+ * (at or beyond seq_len + pending) is all-zero bits, provided the pools start
+ * zeroed or filled only below seq_len. */
+typedef struct {
+  void* k_pool;
+  void* v_pool;
+  int32_t* block_table;
+  int32_t* seq_len;
+  int32_t* pending;
+  int num_blocks;
+  int max_blocks;
+} mtp_kv;
+
+typedef struct mtp_ctx mtp_ctx;
+
+/* Create a context on `device`.  `weights` may be NULL for a context that
+ * only verifies and edits the KV cache.  Allocates the context's workspace
+ * (activations, split-KV partials, argmax keys, counters, error word) and the
+ * rotary table (angles computed in double on the host).  Returns
+ * MTP_ERR_INVALID on a bad shape, MTP_ERR_OOM / MTP_ERR_CUDA on failure; on
+ * success *out owns the workspace until mtp_destroy. */
+mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int device, mtp_ctx** out);
+
+/* K recursive MTP draft steps for B requests ("Architecture" of the MTP
+ * page; inputs as in "The MTP inputs").
+ *   hidden    [B, H]  verifier hidden state per request (dtype).
+ *   embeds    [B, H]  embedding of the token at positions[b] (dtype).
+ *   positions [B]     int32; step k (1-based) runs at positions[b] + k - 1
+ *                     and writes KV slot seq_len[b] + k - 1.
+ *   kv        the MTP cache; requires pending[b] == 0 on entry, leaves
+ *             pending[b] == K (commit or roll back before the next draft).
+ *   K         1..max_k.
+ *   chain_ids [B, K-1] int32 or NULL: when given, step k >= 2 embeds
+ *             chain_ids[b, k-2] (a given token chain, as in training)
+ *             instead of the previous draft.
+ *   draft_ids [B, K] int32 out: argmax of each step's logits, lowest id on
+ *             ties.
+ *   logits    [B, K, V] float32 out, or NULL.
+ *   hidden_out[B, H] float32 out (decoder output of step K), or NULL.
+ * Host errors: ctx without weights, B outside 1..max_batch, K outside
+ * 1..max_k, NULL required pointers.  Device errors: pending != 0, a slot
+ * beyond the block table or pool, a position beyond max_pos. */
+mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, const void* embeds,
+                     const int32_t* positions, const mtp_kv* kv, int K, const int32_t* chain_ids,
+                     int32_t* draft_ids, float* logits, float* hidden_out);
+
+/* Greedy verification ("Overview" of the speculative-decoding page).
+ * For request b with K_b = num_drafts[b] (0..max_k) drafts, target rows
+ * row_offsets[b] .. row_offsets[b] + K_b of target_logits [num_rows, V]
+ * (dtype) give r_j = argmax of row j (lowest id on ties); accepted[b] = the
+ * largest a <= K_b with drafts[b*drafts_stride + j] == r_j for all j < a;
+ * bonus[b] = r_a.  Device-checked per request: K_b <= min(max_k,
+ * drafts_stride), row_offsets[b+1] - row_offsets[b] == K_b + 1, and the rows
+ * lie inside [0, num_rows); on violation nothing of the request is read,
+ * accepted[b] = bonus[b] = -1 and the error word is set. */
+mtp_status mtp_verify(mtp_ctx* ctx, void* stream, int B, const void* target_logits, int num_rows,
+                      const int32_t* row_offsets, const int32_t* drafts, int drafts_stride,
+                      const int32_t* num_drafts, int32_t* accepted, int32_t* bonus);
+
+/* Commit ("Stateful execution"; "Tree Drafting" step 4): request b keeps
+ * its first n_keep[b] drafted slots, the other drafted slots are zeroed in
+ * place, seq_len[b] += n_keep[b], pending[b] = 0.  n_keep [B] int32 device
+ * array, 0 <= n_keep[b] <= pending[b] (device-checked; a request that fails
+ * the check is left unchanged and the error word is set). */
+mtp_status mtp_kv_commit(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv, const int32_t* n_keep);
+
+/* Commit with n_keep[b] = min(accepted[b] + extra, pending[b]) computed on
+ * the device from mtp_verify's output.  extra = 1 keeps the slot of the last
+ * confirmed input token; extra = 0 keeps only accepted drafts. */
+mtp_status mtp_kv_commit_accepted(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv,
+                                  const int32_t* accepted, int extra);
+
+/* Roll back every drafted slot: commit with n_keep = 0. */
+mtp_status mtp_kv_rollback(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv);
+
+/* Return request b to a prefix of new_len[b] entries ("Prefix Caching with
+ * Speculative Decoding"): slots new_len[b] .. seq_len[b]+pending[b]-1 are
+ * zeroed, seq_len[b] = new_len[b], pending[b] = 0.  Requires
+ * 0 <= new_len[b] <= seq_len[b] + pending[b] (device-checked). */
+mtp_status mtp_kv_truncate(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv, const int32_t* new_len);
+
+/* Synchronise the context's device, return the device error word as an
+ * mtp_status (MTP_OK if none) and clear it. */
+mtp_status mtp_get_device_error(mtp_ctx* ctx);
+
+/* Free the workspace and the context.  NULL is a no-op. */
+void mtp_destroy(mtp_ctx* ctx);
+
+/* Static string naming a status. */
+const char* mtp_status_str(mtp_status s);
+
+/* Device-to-device copy of `bytes` bytes with 16-byte vector loads/stores
+ * over a grid sized to the SM count (the bandwidth yardstick measured next
+ * to the kernels).  dst and src must be 16-byte aligned and not overlap;
+ * bytes a multiple of 16. */
+mtp_status mtp_stream_copy(void* stream, void* dst, const void* src, size_t bytes);
+
+/* Kernel timing.  Kernel ids for mtp_profile_begin. */
+typedef enum {
+  MTP_KERNEL_EH_PROJ = 0,
+  MTP_KERNEL_QKV_ROPE = 1,
+  MTP_KERNEL_ATTENTION = 2,
+  MTP_KERNEL_O_PROJ = 3,
+  MTP_KERNEL_GATE_UP = 4,
+  MTP_KERNEL_DOWN = 5,
+  MTP_KERNEL_LM_HEAD = 6,
+  MTP_KERNEL_VERIFY = 7,
+  MTP_KERNEL_KV_EDIT = 8,
+  MTP_KERNEL_COUNT = 9
+} mtp_kernel_id;
+
+/* Start recording CUDA events around every launch of kernel `kernel` (up to
+ * `capacity` launches) on the stream it is launched on.  Recording adds one
+ * event pair per launch.  Returns MTP_ERR_INVALID for a bad id or capacity. */
+mtp_status mtp_profile_begin(mtp_ctx* ctx, int kernel, int capacity);
+
+/* Stop recording; synchronise; write up to `max_out` per-launch durations in
+ * milliseconds to ms_out (host array) and their count to *n_out. */
+mtp_status mtp_profile_end(mtp_ctx* ctx, float* ms_out, int max_out, int* n_out);
+
+/* Number of kernel launches the context has issued since creation (all
+ * entry points), for launch accounting. */
+int64_t mtp_launch_count(const mtp_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTP_H_ */

@@ -1,0 +1,200 @@
+"""MTP self-speculative draft-and-verify step on one GB300 (sm_103a).
+
+A thin binding over the C ABI of ``libmtp.so`` (declared in include/mtp.h):
+the functions below carry the C names and only marshal arguments -- torch
+tensors become device pointers, torch streams become cudaStream_t handles.
+Every step of the method runs in the library's CUDA kernels; PyTorch is used
+for device memory and streams only.  There is no CPU path: if the library is
+missing, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import torch
+
+from . import _lib as L
+from ._lib import (  # noqa: F401
+    KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
+    MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
+    MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
+    MTP_KERNEL_VERIFY, MTP_OK, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
+)
+
+_clib = L.load()
+
+
+class MTPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (where, _clib.mtp_status_str(status).decode(), status))
+
+
+def _check(status: int, where: str) -> None:
+    if status != MTP_OK:
+        raise MTPError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def torch_dtype(dtype_code: int) -> torch.dtype:
+    return torch.bfloat16 if dtype_code == MTP_DTYPE_BF16 else torch.float32
+
+
+@dataclass
+class KVCache:
+    """Caller-owned paged MTP KV cache (device tensors)."""
+    k_pool: torch.Tensor        # [num_blocks, n_kv, block_size, head_dim]
+    v_pool: torch.Tensor
+    block_table: torch.Tensor   # [B, max_blocks] int32
+    seq_len: torch.Tensor       # [B] int32
+    pending: torch.Tensor       # [B] int32
+
+    def struct(self) -> MTPKV:
+        return MTPKV(_ptr(self.k_pool, name="k_pool"), _ptr(self.v_pool, name="v_pool"),
+                     _ptr(self.block_table, torch.int32, "block_table"), _ptr(self.seq_len, torch.int32, "seq_len"),
+                     _ptr(self.pending, torch.int32, "pending"), int(self.k_pool.shape[0]),
+                     int(self.block_table.shape[1]))
+
+
+class Context:
+    """Owns an mtp_ctx handle and keeps the borrowed weight tensors alive."""
+
+    def __init__(self, handle: int, cfg: MTPConfig, weights: Optional[Dict[str, torch.Tensor]]):
+        self.handle = handle
+        self.cfg = cfg
+        self.weights = weights
+
+    def close(self):
+        if self.handle:
+            _clib.mtp_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def make_config(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps=1e-6, rope_theta=1e6, dtype="bf16",
+                max_batch=1, max_k=5, block_size=16, max_pos=32768) -> MTPConfig:
+    code = MTP_DTYPE_BF16 if dtype in ("bf16", MTP_DTYPE_BF16, torch.bfloat16) else MTP_DTYPE_F32
+    return MTPConfig(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps, rope_theta, code, max_batch, max_k,
+                     block_size, max_pos)
+
+
+def mtp_init(cfg: MTPConfig, weights: Optional[Dict[str, torch.Tensor]] = None, device: Optional[int] = None
+             ) -> Context:
+    """Create a context.  ``weights`` maps the mtp_weights field names to
+    device tensors (``lm_head`` optional: tied to ``embed``); None for a
+    verify/KV-only context."""
+    if device is None:
+        device = torch.cuda.current_device()
+    wst = None
+    if weights is not None:
+        dt = torch_dtype(cfg.dtype)
+        wst = MTPWeights(*[_ptr(weights.get(n), dt, n) if weights.get(n) is not None else None
+                           for n in WEIGHT_FIELDS])
+    out = ctypes.c_void_p()
+    _check(_clib.mtp_init(ctypes.byref(cfg), ctypes.byref(wst) if wst is not None else None, int(device),
+                         ctypes.byref(out)), "mtp_init")
+    return Context(out.value, cfg, weights)
+
+
+def mtp_draft(ctx: Context, hidden: torch.Tensor, embeds: torch.Tensor, positions: torch.Tensor, kv: KVCache, K: int,
+              draft_ids: torch.Tensor, logits: Optional[torch.Tensor] = None, hidden_out: Optional[torch.Tensor] = None,
+              chain_ids: Optional[torch.Tensor] = None, stream=None) -> None:
+    dt = torch_dtype(ctx.cfg.dtype)
+    B = int(hidden.shape[0])
+    kvs = kv.struct()
+    _check(_clib.mtp_draft(ctx.handle, _stream(stream), B, _ptr(hidden, dt, "hidden"), _ptr(embeds, dt, "embeds"),
+                          _ptr(positions, torch.int32, "positions"), ctypes.byref(kvs), int(K),
+                          _ptr(chain_ids, torch.int32, "chain_ids"), _ptr(draft_ids, torch.int32, "draft_ids"),
+                          _ptr(logits, torch.float32, "logits"), _ptr(hidden_out, torch.float32, "hidden_out")),
+           "mtp_draft")
+
+
+def mtp_verify(ctx: Context, target_logits: torch.Tensor, row_offsets: torch.Tensor, drafts: torch.Tensor,
+               num_drafts: torch.Tensor, accepted: torch.Tensor, bonus: torch.Tensor, stream=None) -> None:
+    dt = torch_dtype(ctx.cfg.dtype)
+    B = int(num_drafts.shape[0])
+    _check(_clib.mtp_verify(ctx.handle, _stream(stream), B, _ptr(target_logits, dt, "target_logits"),
+                           int(target_logits.shape[0]), _ptr(row_offsets, torch.int32, "row_offsets"), _ptr(drafts, torch.int32, "drafts"),
+                           int(drafts.shape[1]), _ptr(num_drafts, torch.int32, "num_drafts"),
+                           _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus")), "mtp_verify")
+
+
+def mtp_kv_commit(ctx: Context, kv: KVCache, n_keep: torch.Tensor, stream=None) -> None:
+    kvs = kv.struct()
+    _check(_clib.mtp_kv_commit(ctx.handle, _stream(stream), int(kv.seq_len.shape[0]), ctypes.byref(kvs),
+                              _ptr(n_keep, torch.int32, "n_keep")), "mtp_kv_commit")
+
+
+def mtp_kv_commit_accepted(ctx: Context, kv: KVCache, accepted: torch.Tensor, extra: int = 1, stream=None) -> None:
+    kvs = kv.struct()
+    _check(_clib.mtp_kv_commit_accepted(ctx.handle, _stream(stream), int(kv.seq_len.shape[0]), ctypes.byref(kvs),
+                                       _ptr(accepted, torch.int32, "accepted"), int(extra)), "mtp_kv_commit_accepted")
+
+
+def mtp_kv_rollback(ctx: Context, kv: KVCache, stream=None) -> None:
+    kvs = kv.struct()
+    _check(_clib.mtp_kv_rollback(ctx.handle, _stream(stream), int(kv.seq_len.shape[0]), ctypes.byref(kvs)),
+           "mtp_kv_rollback")
+
+
+def mtp_kv_truncate(ctx: Context, kv: KVCache, new_len: torch.Tensor, stream=None) -> None:
+    kvs = kv.struct()
+    _check(_clib.mtp_kv_truncate(ctx.handle, _stream(stream), int(kv.seq_len.shape[0]), ctypes.byref(kvs),
+                                _ptr(new_len, torch.int32, "new_len")), "mtp_kv_truncate")
+
+
+def mtp_get_device_error(ctx: Context) -> int:
+    return int(_clib.mtp_get_device_error(ctx.handle))
+
+
+def mtp_destroy(ctx: Context) -> None:
+    ctx.close()
+
+
+def mtp_status_str(status: int) -> str:
+    return _clib.mtp_status_str(int(status)).decode()
+
+
+def mtp_stream_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: Optional[int] = None, stream=None) -> None:
+    n = src.numel() * src.element_size() if nbytes is None else nbytes
+    _check(_clib.mtp_stream_copy(_stream(stream), _ptr(dst, name="dst"), _ptr(src, name="src"), n),
+           "mtp_stream_copy")
+
+
+def mtp_profile_begin(ctx: Context, kernel: int, capacity: int) -> None:
+    _check(_clib.mtp_profile_begin(ctx.handle, int(kernel), int(capacity)), "mtp_profile_begin")
+
+
+def mtp_profile_end(ctx: Context, max_out: int = 1 << 16):
+    buf = (ctypes.c_float * max_out)()
+    n = ctypes.c_int(0)
+    _check(_clib.mtp_profile_end(ctx.handle, buf, max_out, ctypes.byref(n)), "mtp_profile_end")
+    return [float(buf[i]) for i in range(n.value)]
+
+
+def mtp_launch_count(ctx: Context) -> int:
+    return int(_clib.mtp_launch_count(ctx.handle))

@@ -1,0 +1,78 @@
+"""ctypes declarations of the C ABI in include/mtp.h.
+
+Loading fails loudly when libmtp.so is missing: there is no other
+implementation to fall back to."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmtp.so")
+
+c_int, c_float, c_void_p, c_size_t = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+c_int64 = ctypes.c_int64
+P_i32 = ctypes.c_void_p  # device int32 pointers are passed as plain addresses
+
+MTP_OK, MTP_ERR_INVALID, MTP_ERR_CUDA, MTP_ERR_OOM, MTP_ERR_CAPACITY, MTP_ERR_TIMEOUT, MTP_ERR_DEVICE_ARGS = range(7)
+MTP_DTYPE_F32, MTP_DTYPE_BF16 = 0, 1
+(MTP_KERNEL_EH_PROJ, MTP_KERNEL_QKV_ROPE, MTP_KERNEL_ATTENTION, MTP_KERNEL_O_PROJ, MTP_KERNEL_GATE_UP,
+ MTP_KERNEL_DOWN, MTP_KERNEL_LM_HEAD, MTP_KERNEL_VERIFY, MTP_KERNEL_KV_EDIT, MTP_KERNEL_COUNT) = range(10)
+KERNEL_NAMES = ["eh_proj", "qkv_rope", "attention", "o_proj", "gate_up", "down", "lm_head", "verify", "kv_edit"]
+
+
+class MTPConfig(ctypes.Structure):
+    _fields_ = [("hidden", c_int), ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
+                ("ffn", c_int), ("vocab", c_int), ("eps", c_float), ("rope_theta", c_float), ("dtype", c_int),
+                ("max_batch", c_int), ("max_k", c_int), ("block_size", c_int), ("max_pos", c_int)]
+
+
+WEIGHT_FIELDS = ["w_norm_h", "w_norm_e", "w_eh", "w_norm_in", "w_q", "w_k", "w_v", "w_o", "w_norm_post",
+                 "w_gate", "w_up", "w_down", "w_norm_f", "embed", "lm_head"]
+
+
+class MTPWeights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in WEIGHT_FIELDS]
+
+
+class MTPKV(ctypes.Structure):
+    _fields_ = [("k_pool", c_void_p), ("v_pool", c_void_p), ("block_table", c_void_p), ("seq_len", c_void_p),
+                ("pending", c_void_p), ("num_blocks", c_int), ("max_blocks", c_int)]
+
+
+# name -> (restype, argtypes); every symbol declared in include/mtp.h
+SIGNATURES = {
+    "mtp_init": (c_int, [ctypes.POINTER(MTPConfig), ctypes.POINTER(MTPWeights), c_int, ctypes.POINTER(c_void_p)]),
+    "mtp_draft": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P_i32, ctypes.POINTER(MTPKV), c_int,
+                          P_i32, P_i32, c_void_p, c_void_p]),
+    "mtp_verify": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, P_i32, P_i32, c_int, P_i32, P_i32, P_i32]),
+    "mtp_kv_commit": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
+    "mtp_kv_commit_accepted": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32, c_int]),
+    "mtp_kv_rollback": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV)]),
+    "mtp_kv_truncate": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
+    "mtp_get_device_error": (c_int, [c_void_p]),
+    "mtp_destroy": (None, [c_void_p]),
+    "mtp_status_str": (ctypes.c_char_p, [c_int]),
+    "mtp_stream_copy": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t]),
+    "mtp_profile_begin": (c_int, [c_void_p, c_int, c_int]),
+    "mtp_profile_end": (c_int, [c_void_p, ctypes.POINTER(c_float), c_int, ctypes.POINTER(c_int)]),
+    "mtp_launch_count": (c_int64, [c_void_p]),
+}
+
+_lib = None
+
+
+def load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libmtp.so is not built (%s); run __graft_entry__.build() or "
+                          "python -m mtp_self_speculative_gb300._build" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

@@ -1,0 +1,379 @@
+// Split-KV grouped-query decode attention over the paged single-layer MTP
+// KV cache ("MTP (Multi-Token Prediction)", "Architecture": the decoder
+// layer's attention; "How OpenVINO MTP Speculative Decoding Works
+// Internally", "Why the MTP graph is a single decoder layer": its own
+// one-layer cache).
+//
+// For request b at draft step k the query of every q head h attends to the
+// T = seq_len[b] + k entries of its kv head g = h / G (G = n_q / n_kv):
+//   o_h = softmax(q_h K_g^T / sqrt(d)) V_g.
+//
+// Grid (splits, n_kv, B); a CTA serves all G query heads of one kv head for
+// a contiguous range of 16-token blocks.  Each of its 4 warps owns every 4th
+// block of the range and stages it with one-dimensional bulk (TMA) copies --
+// a K tile and a V tile, each 16 x d contiguous in the pool -- into its own
+// ring of shared-memory stages, completed on per-stage mbarriers.  Scores:
+// each lane holds d/32 dimensions of the G queries; per-token partial dot
+// products are combined with a butterfly reduce-scatter so that lane l ends
+// with the full score of token l & 15.  Softmax is online (running max and
+// sum per head, base-2 exponentials with the scale folded into q).  Warps
+// merge in shared memory; splits merge in the last CTA to finish (arrival
+// counter), which writes o and resets the counter.
+#include "mtp_common.cuh"
+
+namespace mtp {
+
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kStages = 3;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+template <typename T>
+struct AttnArgs {
+  const float* q;        // [B, n_q * d] rotated queries
+  float* out;            // [B, n_q * d]
+  float* part;           // [B, n_q, max_splits, d + 2]
+  int* cnt;              // [B, n_kv]
+  int* err;
+  const T* k_pool;
+  const T* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  int k;                 // draft step (1-based): T = seq_len + k
+  int n_q, n_kv, max_blocks, num_blocks, bps, max_splits;
+  float qscale;          // log2(e) / sqrt(d)
+};
+
+template <typename T, int HD>
+struct KVLane;
+// Load the lane's d/32 contiguous elements of one row as floats.
+template <int HD>
+struct KVLane<uint16_t, HD> {
+  static constexpr int DPL = HD / 32;
+  __device__ static __forceinline__ void load(const uint16_t* row, int lane, float* o) {
+    if constexpr (DPL == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(row + lane * 4);
+      o[0] = bf16_lo(u.x); o[1] = bf16_hi(u.x); o[2] = bf16_lo(u.y); o[3] = bf16_hi(u.y);
+    } else {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(row + lane * 2);
+      o[0] = bf16_lo(u); o[1] = bf16_hi(u);
+    }
+  }
+};
+template <int HD>
+struct KVLane<float, HD> {
+  static constexpr int DPL = HD / 32;
+  __device__ static __forceinline__ void load(const float* row, int lane, float* o) {
+    if constexpr (DPL == 4) {
+      const float4 u = *reinterpret_cast<const float4*>(row + lane * 4);
+      o[0] = u.x; o[1] = u.y; o[2] = u.z; o[3] = u.w;
+    } else {
+      const float2 u = *reinterpret_cast<const float2*>(row + lane * 2);
+      o[0] = u.x; o[1] = u.y;
+    }
+  }
+};
+
+// Butterfly reduce-scatter of 16 per-lane partials: lane l returns the sum
+// over all 32 lanes of partial[l & 15].
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 8;
+    const float mine = hi ? v[i + 8] : v[i], other = hi ? v[i] : v[i + 8];
+    v[i] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 4;
+    const float mine = hi ? v[i + 4] : v[i], other = hi ? v[i] : v[i + 4];
+    v[i] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 2;
+    const float mine = hi ? v[i + 2] : v[i], other = hi ? v[i] : v[i + 2];
+    v[i] = mine + __shfl_xor_sync(0xffffffffu, other, 2);
+  }
+  {
+    const bool hi = lane & 1;
+    const float mine = hi ? v[1] : v[0], other = hi ? v[0] : v[1];
+    v[0] = mine + __shfl_xor_sync(0xffffffffu, other, 1);
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+template <typename T, int HD, int G>
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T> a) {
+  constexpr int DPL = HD / 32;
+  constexpr int TILE = 16 * HD;                      // elements per K (or V) tile
+  constexpr uint32_t TILE_BYTES = TILE * sizeof(T);
+  constexpr int HC = (G < 4) ? G : 4;                // heads per score pass
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  T* stage_base = reinterpret_cast<T*>(smem_raw);    // [warps][stages][2][TILE]
+  __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
+  __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
+  __shared__ int am_last;
+
+  pdl_trigger();
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < kAttnWarps * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
+  fence_mbar_init();
+  __syncthreads();
+  pdl_wait();
+
+  const int T_len = a.seq_len[b] + a.k;
+  const int nblk = (T_len + 15) >> 4;
+  const int blk0 = s * a.bps;
+  if (blk0 >= nblk || T_len <= 0) return;  // uniform across the CTA
+  const int blk1 = min(nblk, blk0 + a.bps);
+  const int nsplit = (nblk + a.bps - 1) / a.bps;
+
+  // Queries of this group, scaled for base-2 softmax: lane holds dims [lane*DPL, +DPL).
+  float qv[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j)
+      qv[h][j] = a.q[(size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + lane * DPL + j] * a.qscale;
+
+  float m[G], l[G], acc[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[h][j] = 0.0f;
+  }
+
+  T* my_stage = stage_base + (size_t)warp * kStages * 2 * TILE;
+  const size_t head_stride = (size_t)16 * HD;  // elements per (block, kv head) tile
+  auto tile_src = [&](int bi, const T* pool) -> const T* {
+    int blk = (bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    if (blk < 0 || blk >= a.num_blocks) {
+      set_error(a.err, MTP_ERR_CAPACITY);
+      blk = 0;
+    }
+    return pool + ((size_t)blk * a.n_kv + g) * head_stride;
+  };
+  auto issue = [&](int it, int bi) {
+    const int st = it % kStages;
+    T* dst = my_stage + (size_t)st * 2 * TILE;
+    mbar_expect_tx(&bars[warp][st], 2 * TILE_BYTES);
+    bulk_g2s(dst, tile_src(bi, a.k_pool), TILE_BYTES, &bars[warp][st]);
+    bulk_g2s(dst + TILE, tile_src(bi, a.v_pool), TILE_BYTES, &bars[warp][st]);
+  };
+
+  // This warp's blocks: blk0 + warp, blk0 + warp + 4, ...
+  const int first = blk0 + warp;
+  const int count = (first < blk1) ? (blk1 - first + kAttnWarps - 1) / kAttnWarps : 0;
+  if (lane == 0)
+    for (int it = 0; it < count && it < kStages; ++it) issue(it, first + it * kAttnWarps);
+  __syncwarp();
+
+  int stop_at = -1;  // iteration whose wait ran out
+  for (int it = 0; it < count; ++it) {
+    const int st = it % kStages;
+    const uint32_t parity = (uint32_t)((it / kStages) & 1);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], parity, kWaitLimit));
+    if (!ok) {
+      stop_at = it;
+      break;
+    }
+    const T* kt = my_stage + (size_t)st * 2 * TILE;
+    const T* vt = kt + TILE;
+    const int bi = first + it * kAttnWarps;
+    const int tok0 = bi * 16;
+    const int my_tok = tok0 + (lane & 15);
+    const bool valid = my_tok < T_len;
+
+    // scores s[h] for token (lane & 15)
+    float sc[G];
+#pragma unroll
+    for (int h0 = 0; h0 < G; h0 += HC) {
+      float part[HC][16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        float kvv[DPL];
+        KVLane<T, HD>::load(kt + t * HD, lane, kvv);
+#pragma unroll
+        for (int hh = 0; hh < HC; ++hh) {
+          float p = 0.0f;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) p = fmaf(qv[h0 + hh][j], kvv[j], p);
+          part[hh][t] = p;
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < HC; ++hh) sc[h0 + hh] = reduce_scatter16(part[hh], lane);
+    }
+
+    float pr[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float sv = valid ? sc[h] : -INFINITY;
+      float bmax = sv;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+      const float m_new = fmaxf(m[h], bmax);
+      const float corr = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
+      const float p = valid ? exp2f(sv - m_new) : 0.0f;
+      float psum = p;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+      l[h] = l[h] * corr + psum;
+      m[h] = m_new;
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[h][j] *= corr;
+      pr[h] = p;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      float vv[DPL];
+      KVLane<T, HD>::load(vt + t * HD, lane, vv);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float p = __shfl_sync(0xffffffffu, pr[h], t);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc[h][j] = fmaf(p, vv[j], acc[h][j]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && it + kStages < count) issue(it + kStages, first + (it + kStages) * kAttnWarps);
+    __syncwarp();
+  }
+  if (stop_at >= 0) {
+    if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+    // give the copies still in flight (iterations stop_at .. stop_at + kStages - 1)
+    // a bounded chance to land before the shared memory is reused
+    for (int it = stop_at; it < count && it < stop_at + kStages; ++it)
+      mbar_wait_bounded(&bars[warp][it % kStages], (uint32_t)((it / kStages) & 1), kWaitLimit);
+  }
+
+  // merge warps
+  float* wacc = reinterpret_cast<float*>(smem_raw);  // reuse stages: [warps][G][HD]
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) { wm[warp][h] = m[h]; wl[warp][h] = l[h]; }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) wacc[((size_t)warp * G + h) * HD + lane * DPL + j] = acc[h][j];
+  __syncthreads();
+
+  float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * (HD + 2);
+  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+    const int h = idx / HD, d = idx - h * HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w][h]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float f = (wm[w][h] == -INFINITY) ? 0.0f : exp2f(wm[w][h] - M);
+      L += wl[w][h] * f;
+      O += wacc[((size_t)w * G + h) * HD + d] * f;
+    }
+    if (nsplit == 1) {
+      a.out[(size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d] = O / L;
+    } else {
+      float* pp = part_base + ((size_t)h * a.max_splits + s) * (HD + 2);
+      if (d == 0) { pp[0] = M; pp[1] = L; }
+      pp[2 + d] = O;
+    }
+  }
+  if (nsplit == 1) return;
+
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1);
+    am_last = (prev == nsplit - 1);
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+    const int h = idx / HD, d = idx - h * HD;
+    const float* ph = part_base + (size_t)h * a.max_splits * (HD + 2);
+    float M = -INFINITY;
+    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, __ldcg(ph + (size_t)j * (HD + 2)));
+    float L = 0.0f, O = 0.0f;
+    for (int j = 0; j < nsplit; ++j) {
+      const float* pj = ph + (size_t)j * (HD + 2);
+      const float f = exp2f(__ldcg(pj) - M);
+      L += __ldcg(pj + 1) * f;
+      O += __ldcg(pj + 2 + d) * f;
+    }
+    a.out[(size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d] = O / L;
+  }
+  if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
+}
+
+template <typename T, int HD, int G>
+static cudaError_t attn_launch(mtp_ctx* ctx, cudaStream_t s, const AttnArgs<T>& a, int B, int splits) {
+  constexpr size_t stage_bytes = (size_t)kAttnWarps * kStages * 2 * 16 * HD * sizeof(T);
+  constexpr size_t merge_bytes = (size_t)kAttnWarps * G * HD * sizeof(float);
+  constexpr size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
+  auto kern = attn_kernel<T, HD, G>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_pdl(kern, dim3(splits, ctx->cfg.n_kv_heads, B), dim3(kAttnThreads), smem, s, a);
+}
+
+// Blocks per split for a batch of B requests and max_blocks capacity:
+// aim for about two CTAs per SM, never more than max_splits splits.
+static int attn_bps(const mtp_ctx* ctx, int B, int max_blocks) {
+  const long long pairs = (long long)B * ctx->cfg.n_kv_heads;
+  long long splits = (ctx->attn_target_ctas + pairs - 1) / pairs;
+  if (splits < 1) splits = 1;
+  if (splits > ctx->attn_max_splits) splits = ctx->attn_max_splits;
+  int bps = (int)((max_blocks + splits - 1) / splits);
+  if (bps < 2) bps = 2;
+  while ((max_blocks + bps - 1) / bps > ctx->attn_max_splits) ++bps;
+  return bps;
+}
+
+template <typename T>
+static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv) {
+  const mtp_config& c = ctx->cfg;
+  AttnArgs<T> a;
+  a.q = ctx->q; a.out = ctx->attn; a.part = ctx->attn_part; a.cnt = ctx->attn_cnt; a.err = ctx->err;
+  a.k_pool = (const T*)kv->k_pool; a.v_pool = (const T*)kv->v_pool;
+  a.block_table = kv->block_table; a.seq_len = kv->seq_len; a.k = k;
+  a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.max_blocks = kv->max_blocks; a.num_blocks = kv->num_blocks;
+  a.bps = attn_bps(ctx, B, kv->max_blocks);
+  const int splits = (kv->max_blocks + a.bps - 1) / a.bps;
+  a.max_splits = splits;  // partial-buffer stride of this call
+  a.qscale = 1.4426950408889634f / sqrtf((float)c.head_dim);
+  const int G = c.n_q_heads / c.n_kv_heads;
+  const int HD = c.head_dim;
+  if (HD == 128) {
+    switch (G) {
+      case 1: return attn_launch<T, 128, 1>(ctx, s, a, B, splits);
+      case 2: return attn_launch<T, 128, 2>(ctx, s, a, B, splits);
+      case 4: return attn_launch<T, 128, 4>(ctx, s, a, B, splits);
+      case 8: return attn_launch<T, 128, 8>(ctx, s, a, B, splits);
+    }
+  } else if (HD == 64) {
+    switch (G) {
+      case 1: return attn_launch<T, 64, 1>(ctx, s, a, B, splits);
+      case 2: return attn_launch<T, 64, 2>(ctx, s, a, B, splits);
+      case 4: return attn_launch<T, 64, 4>(ctx, s, a, B, splits);
+      case 8: return attn_launch<T, 64, 8>(ctx, s, a, B, splits);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv) {
+  prof_before(ctx, MTP_KERNEL_ATTENTION, s);
+  cudaError_t e = (ctx->cfg.dtype == MTP_DTYPE_BF16) ? attention_t<uint16_t>(ctx, s, B, k, kv)
+                                                     : attention_t<float>(ctx, s, B, k, kv);
+  prof_after(ctx, MTP_KERNEL_ATTENTION, s);
+  ctx->launches++;
+  return e;
+}
+
+}  // namespace mtp

@@ -1,0 +1,244 @@
+// Shared device helpers and the context layout of the MTP draft/verify
+// library.  sm_103a only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mtp.h"
+
+#ifndef __CUDA_ARCH__
+#define MTP_HOST_ONLY 1
+#endif
+
+namespace mtp {
+
+// ---------------------------------------------------------------- errors
+// Device error word values match mtp_status.
+__device__ __forceinline__ void set_error(int* err, int code) {
+  atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------- number formats
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kPerVec = 4;  // elements per 16-byte vector
+  __device__ static __forceinline__ float load1(const float* p) { return __ldg(p); }
+  __device__ static __forceinline__ void store1(float* p, float v) { *p = v; }
+};
+template <> struct Elem<uint16_t> {
+  static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ float load1(const uint16_t* p) {
+    return __uint_as_float(((uint32_t)__ldg(p)) << 16);
+  }
+  __device__ static __forceinline__ void store1(uint16_t* p, float v) { *p = f32_to_bf16_rne(v); }
+};
+
+// 16-byte streaming load that bypasses L1 (weights are read once).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Dot product of one 16-byte weight vector with the matching activations.
+template <typename T>
+__device__ __forceinline__ float dot_vec(const uint4& w, const float* x);
+
+template <>
+__device__ __forceinline__ float dot_vec<uint16_t>(const uint4& w, const float* x) {
+  const float4 a = *reinterpret_cast<const float4*>(x);
+  const float4 b = *reinterpret_cast<const float4*>(x + 4);
+  float s = bf16_lo(w.x) * a.x;
+  s = fmaf(bf16_hi(w.x), a.y, s);
+  s = fmaf(bf16_lo(w.y), a.z, s);
+  s = fmaf(bf16_hi(w.y), a.w, s);
+  s = fmaf(bf16_lo(w.z), b.x, s);
+  s = fmaf(bf16_hi(w.z), b.y, s);
+  s = fmaf(bf16_lo(w.w), b.z, s);
+  s = fmaf(bf16_hi(w.w), b.w, s);
+  return s;
+}
+
+template <>
+__device__ __forceinline__ float dot_vec<float>(const uint4& w, const float* x) {
+  const float4 a = *reinterpret_cast<const float4*>(x);
+  float s = __uint_as_float(w.x) * a.x;
+  s = fmaf(__uint_as_float(w.y), a.y, s);
+  s = fmaf(__uint_as_float(w.z), a.z, s);
+  s = fmaf(__uint_as_float(w.w), a.w, s);
+  return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Orderable key for argmax with lowest-index tie break:
+// (monotone float bits << 32) | (0xFFFFFFFF - index).  A larger key is a
+// larger value, or an equal value at a smaller index.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+  if (v == 0.0f) v = 0.0f;  // -0 and +0 compare equal
+  uint32_t b = __float_as_uint(v);
+  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) {
+  return 0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull);
+}
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = umax64(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Each kernel lets its dependent start early (the dependent only prefetches
+// weights before its own wait) and waits for its prerequisite grid before
+// touching anything the previous kernel produced or still reads.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------ bulk copy + mbarrier
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the phase did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// One-dimensional bulk (TMA) copy global -> shared, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+}  // namespace mtp
+
+// ------------------------------------------------------------ host context
+
+struct mtp_ctx {
+  mtp_config cfg;
+  mtp_weights w;
+  int has_weights;
+  int device;
+  int num_sms;
+  int q_dim, kv_dim;
+  int attn_target_ctas;
+  int attn_max_splits;
+  // workspace (one allocation)
+  void* ws;
+  size_t ws_bytes;
+  float* hid;        // [maxB, H]   recursive hidden (decoder output)
+  float* x;          // [maxB, H]   eh_proj output (residual stream)
+  float* q;          // [maxB, q_dim] rotated queries
+  float* attn;       // [maxB, q_dim] attention output
+  float* h1;         // [maxB, H]   after attention residual
+  float* act;        // [maxB, F]   silu(gate) * up
+  float* attn_part;  // split-KV partials
+  int* attn_cnt;     // [maxB, n_kv] arrival counters
+  unsigned long long* lm_keys;  // [maxB] argmax keys
+  int* lm_cnt;                  // [1]
+  unsigned long long* ver_keys; // [maxB, max_k + 1]
+  int* ver_cnt;                 // [maxB]
+  int* err;                     // [1]
+  float2* rope;                 // [max_pos, head_dim / 2] (cos, sin)
+  // timing
+  int prof_kernel;
+  int prof_cap;
+  int prof_n;
+  cudaEvent_t* prof_ev;  // 2 * prof_cap
+  long long launches;
+};
+
+namespace mtp {
+
+// Launch helper: programmatic stream serialisation on every kernel.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Kernel timing hooks (host).
+void prof_before(mtp_ctx* ctx, int kernel, cudaStream_t s);
+void prof_after(mtp_ctx* ctx, int kernel, cudaStream_t s);
+
+// Launchers implemented in the kernel translation units.
+cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
+                              const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                              const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
+cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv);
+cudaError_t launch_verify(mtp_ctx* ctx, cudaStream_t s, int B, const void* logits, int num_rows,
+                          const int32_t* row_offsets,
+                          const int32_t* drafts, int drafts_stride, const int32_t* num_drafts,
+                          int32_t* accepted, int32_t* bonus);
+cudaError_t launch_kv_edit(mtp_ctx* ctx, cudaStream_t s, int B, const mtp_kv* kv, int mode,
+                           const int32_t* arg, int extra);
+cudaError_t launch_stream_copy(cudaStream_t s, void* dst, const void* src, size_t bytes, int num_sms);
+
+enum KvEditMode { KV_COMMIT = 0, KV_COMMIT_ACCEPTED = 1, KV_ROLLBACK = 2, KV_TRUNCATE = 3 };
+
+}  // namespace mtp

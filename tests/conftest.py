@@ -8,6 +8,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionstart(session):
+    # compile libmtp.so and the input generator if they are missing or stale
+    import __graft_entry__
+    __graft_entry__.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the kernels through the C ABI)")
     config.addinivalue_line("markers", "slow: large-shape case (minutes of host work)")

@@ -1,0 +1,92 @@
+"""The C ABI library loads and exports every entry point that include/mtp.h
+declares; host-side argument checks reject bad calls before touching a
+device.  CPU only: no call here launches work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mtp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mtp_self_speculative_gb300 import _lib
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:mtp_status|void|const char\*|int64_t)\s+(mtp_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("mtp_init", "mtp_draft", "mtp_verify", "mtp_kv_commit", "mtp_kv_rollback",
+                     "mtp_destroy", "mtp_get_device_error", "mtp_status_str"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from mtp_self_speculative_gb300 import _lib
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, "binding lacks " + name
+
+
+def test_status_strings(lib):
+    assert lib.mtp_status_str(0) == b"ok"
+    assert b"invalid" in lib.mtp_status_str(1)
+    assert lib.mtp_status_str(99) == b"unknown status"
+
+
+def _cfg(**kw):
+    from mtp_self_speculative_gb300 import _lib
+    base = dict(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64, ffn=1024, vocab=4096, eps=1e-6,
+                rope_theta=1e6, dtype=0, max_batch=1, max_k=3, block_size=16, max_pos=1024)
+    base.update(kw)
+    return _lib.MTPConfig(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=96), dict(n_q_heads=6), dict(n_q_heads=48, n_kv_heads=3),
+                                 dict(block_size=32), dict(max_k=0), dict(max_k=101), dict(dtype=7),
+                                 dict(hidden=100), dict(ffn=1001), dict(vocab=0), dict(max_batch=0),
+                                 dict(eps=0.0)])
+def test_init_rejects_bad_config_without_a_device(lib, bad):
+    from mtp_self_speculative_gb300 import _lib
+    out = ctypes.c_void_p()
+    w = _lib.MTPWeights(*([1] * 15))
+    st = lib.mtp_init(ctypes.byref(_cfg(**bad)), ctypes.byref(w), 0, ctypes.byref(out))
+    assert st == _lib.MTP_ERR_INVALID
+    assert out.value is None
+
+
+def test_init_rejects_missing_weight_pointer(lib):
+    from mtp_self_speculative_gb300 import _lib
+    out = ctypes.c_void_p()
+    w = _lib.MTPWeights(*([1] * 15))
+    w.w_o = None
+    assert lib.mtp_init(ctypes.byref(_cfg()), ctypes.byref(w), 0, ctypes.byref(out)) == _lib.MTP_ERR_INVALID
+
+
+def test_calls_without_context_are_rejected(lib):
+    from mtp_self_speculative_gb300 import _lib
+    kv = _lib.MTPKV(1, 1, 1, 1, 1, 1, 1)
+    assert lib.mtp_draft(None, None, 1, 1, 1, 1, ctypes.byref(kv), 1, None, 1, None, None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_verify(None, None, 1, 1, 1, 1, 1, 1, 1, 1, 1) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_kv_commit(None, None, 1, ctypes.byref(kv), 1) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_kv_rollback(None, None, 1, ctypes.byref(kv)) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_kv_truncate(None, None, 1, ctypes.byref(kv), 1) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_get_device_error(None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_profile_begin(None, 0, 1) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_launch_count(None) == 0
+    lib.mtp_destroy(None)
+
+
+def test_stream_copy_rejects_unaligned_or_overlapping(lib):
+    from mtp_self_speculative_gb300 import _lib
+    assert lib.mtp_stream_copy(None, 16, 4096, 15) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_stream_copy(None, 17, 4096, 16) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_stream_copy(None, 4096, 4096 + 16, 64) == _lib.MTP_ERR_INVALID

@@ -1,0 +1,201 @@
+"""GPU MTP draft vs the float64 oracle, through the C ABI.
+
+Parity is checked on the same seeded inputs: both sides draft with the same
+given token chain (so every step is comparable), logits within the stated
+normwise tolerance, draft ids equal except at the oracle's near-ties, the
+appended KV entries within tolerance, every other KV slot bit-identical.  The
+free-running GPU chain is checked against the free-running oracle chain up to
+the first (legitimate) near-tie divergence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from gpu_util import (F32_LOGIT_TOL, LOGIT_TOL, check_ids, check_logits, dev, download_kv, host, kv_slots,
+                      make_context, oracle_weights, upload_kv, upload_weights)
+
+pytestmark = pytest.mark.gpu
+
+
+class Case:
+    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77):
+        self.cfg = cfg
+        self.K = K or cfg.K
+        self.w = synth.make_weights(cfg, norm=norm)
+        self.lens = synth.context_lengths(cfg) if lens is None else np.asarray(lens, dtype=np.int32)
+        self.B = len(self.lens)
+        self.kv0 = synth.make_kv(cfg, self.lens, extra_slots=self.K + 3)
+        self.di = synth.make_draft_inputs(cfg, self.w, self.lens)
+        self.chain = synth.uniform_int(cfg.seed, chain_stream, (self.B, max(self.K - 1, 1)), 0, cfg.vocab)
+        self.wdev = upload_weights(self.w)
+        self.ctx = make_context(cfg, self.wdev, max_batch=self.B, max_k=self.K,
+                                max_pos=int(self.lens.max()) + self.K + 8)
+        self.inputs = (dev(self.di.hidden), dev(self.di.embeds), dev(self.di.positions))
+
+    def gpu_draft(self, forced=True, kvd=None):
+        import mtp_self_speculative_gb300 as M
+        cfg, B, K = self.cfg, self.B, self.K
+        kvd = upload_kv(self.kv0) if kvd is None else kvd
+        ids = torch.full((B, K), -7, dtype=torch.int32, device="cuda")
+        logits = torch.empty((B, K, cfg.vocab), dtype=torch.float32, device="cuda")
+        hout = torch.empty((B, cfg.H), dtype=torch.float32, device="cuda")
+        chain = dev(self.chain[:, :K - 1].copy()) if (forced and K > 1) else None
+        M.mtp_draft(self.ctx, *self.inputs, kvd, K, ids, logits, hout, chain_ids=chain)
+        torch.cuda.synchronize()
+        assert M.mtp_get_device_error(self.ctx) == 0
+        return host(ids), host(logits), host(hout), kvd
+
+    def oracle(self, subset, forced=True, kv=None):
+        """Oracle draft on ``subset``; appends into ``kv`` (default: a copy of
+        the initial cache)."""
+        cfg = self.cfg
+        W = oracle_weights(cfg, self.w)
+        kv = self.kv0.copy() if kv is None else kv
+        view = synth.KVState(kv.k_pool, kv.v_pool, kv.block_table[subset], kv.seq_len[subset].copy(),
+                             np.zeros(len(subset), dtype=np.int32), kv.block_size)
+        chain = self.chain[subset, :self.K - 1] if (forced and self.K > 1) else None
+        res = O.draft(W, O.widen(self.di.hidden[subset], cfg.dtype), O.widen(self.di.embeds[subset], cfg.dtype),
+                      self.di.positions[subset], view, self.K, chain_ids=chain)
+        return res, view
+
+
+def check_forced(case, subset, tol, inplace=False):
+    """Forced-chain parity on the requests in ``subset``.  ``inplace`` lets
+    the oracle append into the initial cache itself (large caches; the case
+    is not used afterwards)."""
+    cfg, K = case.cfg, case.K
+    ids, logits, hout, kvd = case.gpu_draft(forced=True)
+    prefix = {b: kv_slots(case.kv0, b, 0, int(case.lens[b])) for b in subset}
+    res, view = case.oracle(subset, forced=True, kv=case.kv0 if inplace else None)
+    worst = check_logits(logits[subset], res.logits, tol)
+    exact = check_ids(ids[subset], res.logits)
+    e_h = np.max(np.abs(hout[subset] - res.hidden_out), axis=-1) / np.max(np.abs(res.hidden_out), axis=-1)
+    assert np.max(e_h) <= tol
+    got = download_kv(kvd)
+    np.testing.assert_array_equal(got.seq_len, case.lens)
+    np.testing.assert_array_equal(got.pending, K)
+    for i, b in enumerate(subset):
+        L = int(case.lens[b])
+        gk, gv = kv_slots(got, b, 0, L + K)
+        ok, ov = kv_slots(view, i, L, L + K)
+        np.testing.assert_array_equal(gk[:L], prefix[b][0])
+        np.testing.assert_array_equal(gv[:L], prefix[b][1])
+        for g_app, o_app in ((gk[L:], ok), (gv[L:], ov)):
+            a = O.widen(g_app, cfg.dtype)
+            o = O.widen(o_app, cfg.dtype)
+            err = np.max(np.abs(a - o), axis=-1) / np.maximum(np.max(np.abs(o), axis=-1), 1e-30)
+            assert np.max(err) <= tol
+        # the rest of the request's blocks stays zero
+        nblk = (L + K + cfg.block_size - 1) // cfg.block_size
+        tail = L + K
+        cap = nblk * cfg.block_size
+        if cap > tail:
+            zk, zv = kv_slots(got, b, tail, cap)
+            assert not zk.any() and not zv.any()
+    return worst, exact, ids, logits
+
+
+def check_free(case, subset, forced_ids, forced_logits, tol):
+    """Free-running chain: step 1 equals the forced run bitwise; ids follow the
+    oracle's own chain until the first near-tie."""
+    ids, logits, _, _ = case.gpu_draft(forced=False)
+    np.testing.assert_array_equal(ids[:, 0], forced_ids[:, 0])
+    np.testing.assert_array_equal(logits[:, 0], forced_logits[:, 0])
+    # a fresh copy of the initial KV for the oracle's own run
+    kv = case.kv0.copy()
+    res, _ = case.oracle(subset, forced=False, kv=kv)
+    for i, b in enumerate(subset):
+        for k in range(case.K):
+            check_logits(logits[b, k][None], res.logits[i, k][None], tol)
+            check_ids(ids[b, k][None], res.logits[i, k][None])
+            if ids[b, k] != res.ids[i, k]:
+                break            # legitimate near-tie: later steps follow different tokens
+
+
+# ------------------------------------------------------------------ small
+
+def test_tiny_f32_head_parity_and_invariants():
+    """Tiny fp32 head (H=256, 4q/2kv, d=64, F=1024, V=4096, L=128, K=3) with
+    non-unit norm weights so that a dropped norm weight shows."""
+    import mtp_self_speculative_gb300 as M
+    case = Case(synth.TINY_F32, norm="random")
+    worst, exact, ids, logits = check_forced(case, [0], F32_LOGIT_TOL)
+    check_free(case, [0], ids, logits, F32_LOGIT_TOL)
+    # determinism: a second forced run is bitwise identical
+    ids2, logits2, _, _ = case.gpu_draft(forced=True)
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_array_equal(logits2, logits)
+    # draft then full rollback leaves the cache bitwise as it was
+    _, _, _, kvd = case.gpu_draft(forced=False)
+    M.mtp_kv_rollback(case.ctx, kvd)
+    got = download_kv(kvd)
+    for f in ("k_pool", "v_pool", "seq_len", "pending"):
+        np.testing.assert_array_equal(getattr(got, f), getattr(case.kv0, f), err_msg=f)
+
+
+def test_ragged_bf16_block_edges():
+    """bf16, G=4 heads per kv head, d=128, odd vocab; contexts 0, 1, 15, 16,
+    17, 33 and 100 tokens (block boundaries, an empty cache)."""
+    cfg = synth.MTPShape("ragged_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=7, K=4,
+                         dtype="bf16", ctx_lo=0, ctx_hi=100, paged_shuffle=True, seed_index=50)
+    case = Case(cfg, norm="random", lens=[0, 1, 15, 16, 17, 33, 100])
+    _, _, ids, logits = check_forced(case, list(range(7)), LOGIT_TOL)
+    check_free(case, list(range(7)), ids, logits, LOGIT_TOL)
+
+
+def test_gqa_eight_heads_per_kv_head_f32():
+    cfg = synth.MTPShape("gqa8_f32", H=256, n_q=16, n_kv=2, head_dim=64, ffn=512, vocab=2048, batch=3, K=2,
+                         dtype="f32", ctx_lo=40, ctx_hi=300, seed_index=51)
+    case = Case(cfg, norm="random")
+    check_forced(case, [0, 1, 2], F32_LOGIT_TOL)
+
+
+def test_device_errors_leave_no_fault():
+    """pending != 0 on entry and a block table too short are reported through
+    the error word; the writes are skipped."""
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.TINY_F32
+    case = Case(cfg)
+    kv = case.kv0.copy()
+    kv.pending[:] = 1
+    kvd = upload_kv(kv)
+    ids = torch.empty((1, 3), dtype=torch.int32, device="cuda")
+    M.mtp_draft(case.ctx, *case.inputs, kvd, 3, ids)
+    assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_DEVICE_ARGS
+    kv = case.kv0.copy()
+    kv.block_table = kv.block_table[:, :8].copy()      # room for 128 slots only
+    kvd = upload_kv(kv)
+    M.mtp_draft(case.ctx, *case.inputs, kvd, 3, ids)
+    assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_CAPACITY
+    got = download_kv(kvd)
+    np.testing.assert_array_equal(got.k_pool, kv.k_pool)
+
+
+# ------------------------------------------------------------- full sizes
+
+@pytest.mark.slow
+def test_qwen3_8b_b1_full_size():
+    """Qwen3-8B-shaped head, bf16, B=1, context 4096, K=5 -- the bench's
+    workload and launch configuration."""
+    case = Case(synth.QWEN3_8B_B1)
+    worst, exact, ids, logits = check_forced(case, [0], LOGIT_TOL)
+    check_free(case, [0], ids, logits, LOGIT_TOL)
+
+
+@pytest.mark.slow
+def test_qwen3_8b_cb32_ragged_paged():
+    """Continuous batching: B=32, contexts uniform in 512..8192 in shuffled
+    16-token blocks, K=5; every request checked."""
+    case = Case(synth.QWEN3_8B_CB32)
+    check_forced(case, list(range(32)), LOGIT_TOL, inplace=True)
+
+
+@pytest.mark.slow
+def test_qwen3_32b_b128_sampled():
+    """Qwen3-32B-shaped head, B=128, context 16384 each, K=3: the whole batch
+    runs on the GPU; a seeded sample of 8 requests is checked against the
+    oracle (requests are independent given the shared weights)."""
+    case = Case(synth.QWEN3_32B_B128)
+    subset = sorted(set(synth.uniform_int(case.cfg.seed, 88, (8,), 0, 128).tolist()))
+    check_forced(case, subset, LOGIT_TOL, inplace=True)

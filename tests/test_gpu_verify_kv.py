@@ -1,0 +1,175 @@
+"""GPU verification and KV edits vs the oracle: bit-exact accepted counts,
+bonus ids, pools, lengths.  Calls go through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from gpu_util import dev, download_kv, host, make_context, upload_kv
+
+pytestmark = pytest.mark.gpu
+
+
+def _verify_gpu(ctx, vi, B):
+    import mtp_self_speculative_gb300 as M
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    bon = torch.empty(B, dtype=torch.int32, device="cuda")
+    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    return host(acc), host(bon)
+
+
+def test_verify_rollback_b64_bit_exact():
+    """64 requests, K_b uniform in 1..8, bf16 [rows, 151936] logits with a +8
+    spike per row; drafts copy the spikes for a geometric(0.8) prefix."""
+    cfg = synth.VERIFY_B64
+    vi = synth.make_verify_inputs(cfg)
+    ctx = make_context(cfg, None, max_batch=cfg.batch, max_k=vi.max_k)
+    acc, bon = _verify_gpu(ctx, vi, cfg.batch)
+    acc_o, bon_o = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "bf16")
+    np.testing.assert_array_equal(acc, acc_o)
+    np.testing.assert_array_equal(bon, bon_o)
+    # the recipe's planted prefix is what the oracle accepts (spikes dominate)
+    assert np.mean(acc_o == vi.accept_len) > 0.95
+
+
+def test_verify_tiny_f32_many_seeds():
+    """Tiny fp32 head: logits [1, 4, 4096], prefix length uniform over 0..3."""
+    cfg = synth.TINY_F32
+    ctx = make_context(cfg, None, max_batch=1, max_k=3)
+    seen = set()
+    for seed in range(40):
+        vi = synth.make_verify_inputs(cfg, num_drafts=np.array([3]), seed=1000 + seed, len_mode="uniform")
+        acc, bon = _verify_gpu(ctx, vi, 1)
+        acc_o, bon_o = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "f32")
+        np.testing.assert_array_equal(acc, acc_o)
+        np.testing.assert_array_equal(bon, bon_o)
+        seen.add(int(acc_o[0]))
+    assert seen == {0, 1, 2, 3}
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_edges_unaligned_vocab_zero_drafts_and_ties(dtype):
+    cfg = synth.MTPShape("edge", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=1001, batch=7, K=6, dtype=dtype,
+                         ctx_lo=1, ctx_hi=1, seed_index=40)
+    nd = np.array([0, 1, 6, 3, 0, 5, 2], dtype=np.int32)
+    vi = synth.make_verify_inputs(cfg, num_drafts=nd)
+    # plant exact ties in some rows: the lowest id must win
+    lg = vi.logits.copy()
+    lg[0, 17] = lg[0, 900] = lg[0, vi.planted[0]]
+    lg[3, 1000] = lg[3, vi.planted[3]]
+    vi.logits = lg
+    ctx = make_context(cfg, None, max_batch=cfg.batch, max_k=6)
+    acc, bon = _verify_gpu(ctx, vi, cfg.batch)
+    acc_o, bon_o = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, dtype)
+    np.testing.assert_array_equal(acc, acc_o)
+    np.testing.assert_array_equal(bon, bon_o)
+    # all drafts equal the argmax rows -> K_b accepted + bonus of row K_b
+    r = O.argmax_lowest(O.widen(vi.logits, dtype))
+    full = np.full_like(vi.drafts, -1)
+    for b in range(cfg.batch):
+        full[b, :nd[b]] = r[vi.row_offsets[b]:vi.row_offsets[b] + nd[b]]
+    vi.drafts = full
+    acc, bon = _verify_gpu(ctx, vi, cfg.batch)
+    np.testing.assert_array_equal(acc, nd)
+    np.testing.assert_array_equal(bon, r[vi.row_offsets[1:] - 1])
+
+
+def test_verify_inconsistent_offsets_sets_error():
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.shrink(synth.VERIFY_B64, vocab=512, batch=4)
+    vi = synth.make_verify_inputs(cfg)
+    ro = vi.row_offsets.copy()
+    ro[2] += 1                          # request 1 claims one row too many
+    ctx = make_context(cfg, None, max_batch=4, max_k=vi.max_k)
+    acc = torch.empty(4, dtype=torch.int32, device="cuda")
+    bon = torch.empty(4, dtype=torch.int32, device="cuda")
+    M.mtp_verify(ctx, dev(vi.logits), dev(ro), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+    assert M.mtp_get_device_error(ctx) == M.MTP_ERR_DEVICE_ARGS
+    assert host(acc)[1] == -1 and host(bon)[1] == -1
+    assert M.mtp_get_device_error(ctx) == 0     # cleared
+
+
+def _drafted_kv(cfg, num_drafts):
+    """KV with seq_len committed entries plus num_drafts[b] drafted ones."""
+    lens = synth.context_lengths(cfg)
+    kv = synth.make_kv(cfg, lens, extra_slots=int(num_drafts.max()) + 1, prefill_slots=lens + num_drafts)
+    kv.pending = num_drafts.astype(np.int32).copy()
+    return kv
+
+
+def test_commit_after_verify_b64_bit_exact():
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.VERIFY_B64
+    vi = synth.make_verify_inputs(cfg)
+    kv0 = _drafted_kv(cfg, vi.num_drafts)
+    kvd = upload_kv(kv0)
+    ctx = make_context(cfg, None, max_batch=cfg.batch, max_k=vi.max_k)
+    acc = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
+    bon = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
+    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+    M.mtp_kv_commit_accepted(ctx, kvd, acc, extra=1)
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    got = download_kv(kvd)
+    acc_o, _ = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "bf16")
+    kv_o = kv0.copy()
+    O.kv_commit(kv_o, np.minimum(acc_o + 1, vi.num_drafts), "bf16")
+    np.testing.assert_array_equal(got.seq_len, kv_o.seq_len)
+    np.testing.assert_array_equal(got.pending, kv_o.pending)
+    np.testing.assert_array_equal(got.k_pool, kv_o.k_pool)
+    np.testing.assert_array_equal(got.v_pool, kv_o.v_pool)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_commit_rollback_truncate_bit_exact(dtype):
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.MTPShape("kv", H=0, n_q=4, n_kv=2, head_dim=64 if dtype == "f32" else 128, ffn=0, vocab=64,
+                         batch=6, K=7, dtype=dtype, ctx_lo=0, ctx_hi=40, paged_shuffle=True, seed_index=41)
+    nd = np.array([0, 1, 7, 3, 7, 2], dtype=np.int32)
+    kv0 = _drafted_kv(cfg, nd)
+    ctx = make_context(cfg, None, max_batch=6, max_k=7)
+    n_keep = np.array([0, 1, 4, 3, 7, 0], dtype=np.int32)
+    kvd = upload_kv(kv0)
+    M.mtp_kv_commit(ctx, kvd, dev(n_keep))
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    kv_o = kv0.copy()
+    O.kv_commit(kv_o, n_keep, dtype)
+    got = download_kv(kvd)
+    for f in ("k_pool", "v_pool", "seq_len", "pending"):
+        np.testing.assert_array_equal(getattr(got, f), getattr(kv_o, f), err_msg=f)
+    # rollback: everything drafted disappears
+    kvd = upload_kv(kv0)
+    M.mtp_kv_rollback(ctx, kvd)
+    kv_o = kv0.copy()
+    O.kv_rollback(kv_o, dtype)
+    got = download_kv(kvd)
+    for f in ("k_pool", "v_pool", "seq_len", "pending"):
+        np.testing.assert_array_equal(getattr(got, f), getattr(kv_o, f), err_msg=f)
+    # truncate to a shorter common prefix
+    kvd = upload_kv(kv0)
+    new_len = np.maximum(kv0.seq_len - 5, 0).astype(np.int32)
+    M.mtp_kv_truncate(ctx, kvd, dev(new_len))
+    kv_o = kv0.copy()
+    O.kv_truncate(kv_o, new_len, dtype)
+    got = download_kv(kvd)
+    for f in ("k_pool", "v_pool", "seq_len", "pending"):
+        np.testing.assert_array_equal(getattr(got, f), getattr(kv_o, f), err_msg=f)
+    assert M.mtp_get_device_error(ctx) == 0
+
+
+def test_commit_more_than_pending_is_rejected_on_device():
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.MTPShape("kv", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=64, batch=2, K=3, dtype="bf16",
+                         ctx_lo=5, ctx_hi=5, seed_index=42)
+    nd = np.array([2, 2], dtype=np.int32)
+    kv0 = _drafted_kv(cfg, nd)
+    kvd = upload_kv(kv0)
+    ctx = make_context(cfg, None, max_batch=2, max_k=3)
+    M.mtp_kv_commit(ctx, kvd, dev(np.array([1, 3], dtype=np.int32)))
+    assert M.mtp_get_device_error(ctx) == M.MTP_ERR_DEVICE_ARGS
+    got = download_kv(kvd)
+    assert list(got.seq_len) == [6, 5] and list(got.pending) == [0, 2]   # request 1 untouched
