@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Benchmark of the MTP draft+verify step on one GB300 per process.
+
+A step is one pass of the whole hot path for one batch:
+    mtp_draft (K recursive draft steps: eh_proj, QKV+rotary+KV append,
+    split-KV attention, O-proj, SwiGLU MLP, LM head + argmax)
+    -> mtp_verify (greedy accept against target logits)
+    -> mtp_kv_commit_accepted (keep min(a+1, K) drafted slots)
+    -> mtp_kv_truncate (return the cache to its starting length so that
+       every step sees the same state).
+The target logits are built once before timing: one untimed draft gives the
+draft ids, and the target rows carry a +8 spike on those ids for a seeded
+geometric(0.8) prefix, then a mismatch -- so the verify step accepts a known
+prefix.  Inputs (1.7 GB of weights for the Qwen3-8B shape) are far larger than
+L2, so no cache flush is needed between steps.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank drives its own GPU as an independent replica (the
+path has no data-path exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM roofline"
+WORKLOADS = {c.name: c for c in synth.CONFIGS}
+DEFAULT_WORKLOAD = synth.QWEN3_8B_B1.name
+
+
+# ------------------------------------------------------------------ helpers
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (harness timing only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def blas_threads() -> int:
+    try:
+        import ctypes
+        libdir = os.path.join(os.path.dirname(np.__file__) + ".libs")
+        for so in glob.glob(os.path.join(libdir, "*openblas*.so*")):
+            lib = ctypes.CDLL(so)
+            for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                         "openblas_get_num_threads"):
+                if hasattr(lib, name):
+                    return int(getattr(lib, name)())
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def step_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True) -> dict:
+    """Algorithmic bytes of one step: every weight and KV entry read once per
+    draft step, plus the writes of logits, ids and new KV entries."""
+    e = cfg.elem_bytes
+    B = len(lens)
+    w = cfg.weight_bytes()
+    kv_row = 2 * cfg.n_kv * cfg.head_dim * e           # K and V of one slot
+    lm = cfg.vocab * cfg.H * e + cfg.H * e              # LM head rows + final norm weight
+    draft = 0
+    for k in range(1, K + 1):
+        kv_read = int(np.sum(lens + k)) * kv_row
+        draft += w + kv_read + B * kv_row + (B * cfg.vocab * 4 if with_logits else 0) + B * 4
+    verify = B * (K + 1) * cfg.vocab * e
+    commit = B * K * kv_row                               # at most K slots rewritten
+    return {"draft": draft, "verify": verify, "commit": commit, "total": draft + verify + commit,
+            "lm_head_launch": lm + B * cfg.H * 4 + (B * cfg.vocab * 4 if with_logits else 0),
+            "weights": w}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def mhz(s):
+            try:
+                return float(s.split()[0])
+            except Exception:
+                return float("nan")
+        sm = [mhz(r[1]) for r in rows]
+        smax = [mhz(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm if not math.isnan(s)]
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(s for s in smax if not math.isnan(s)) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((mhz(r[3]) for r in rows), default=None)}
+
+
+def gpu_id_for_smi(local_rank: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[local_rank] if vis else str(local_rank)
+
+
+# ------------------------------------------------------------- workload
+
+class Workload:
+    """Device-resident inputs and outputs of one draft+verify step."""
+
+    def __init__(self, cfg: synth.MTPShape, K: int):
+        import torch
+        import mtp_self_speculative_gb300 as M
+        self.cfg, self.K = cfg, K
+        self.w = synth.make_weights(cfg, norm="ones")
+        self.lens = synth.context_lengths(cfg)
+        self.B = B = len(self.lens)
+        self.kv0 = synth.make_kv(cfg, self.lens, extra_slots=K + 1)
+        self.di = synth.make_draft_inputs(cfg, self.w, self.lens)
+        tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+
+        def dev(a):
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+            return torch.from_numpy(a).cuda()
+        self.dev = dev
+        self.wdev = {k: dev(v) for k, v in self.w.items()}
+        self.ctx = M.mtp_init(M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps,
+                                            cfg.rope_theta, cfg.dtype, B, K, cfg.block_size,
+                                            int(self.lens.max()) + K + 8), self.wdev)
+        self.kv = M.KVCache(dev(self.kv0.k_pool), dev(self.kv0.v_pool), dev(self.kv0.block_table),
+                            dev(self.kv0.seq_len), dev(self.kv0.pending))
+        self.L0 = dev(self.lens.astype(np.int32))
+        self.hidden, self.embeds, self.positions = dev(self.di.hidden), dev(self.di.embeds), dev(self.di.positions)
+        self.ids = torch.empty((B, K), dtype=torch.int32, device="cuda")
+        self.logits = torch.empty((B, K, cfg.vocab), dtype=torch.float32, device="cuda")
+        self.acc = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.bonus = torch.empty(B, dtype=torch.int32, device="cuda")
+        self.tdt = tdt
+        # one untimed draft: its ids carry the target spikes
+        self.draft()
+        M.mtp_kv_rollback(self.ctx, self.kv)
+        torch.cuda.synchronize()
+        ids0 = self.ids.cpu().numpy()
+        self.ids0 = ids0
+        u = 1.0 - synth.uniform01(cfg.seed, 60, (B,))
+        n = np.minimum(synth.geometric_len(u, 0.8), K).astype(np.int32)
+        other = synth.uniform_int(cfg.seed, 61, (B, K + 1), 0, cfg.vocab - 1)
+        planted = np.empty((B, K + 1), dtype=np.int32)
+        for b in range(B):
+            for j in range(K + 1):
+                if j < n[b]:
+                    planted[b, j] = ids0[b, j]
+                else:
+                    x = int(other[b, j])
+                    planted[b, j] = x + 1 if (j < K and x >= ids0[b, j]) else x
+        vcfg = synth.shrink(cfg, batch=B, k_lo=0, k_hi=0)
+        vi = synth.make_verify_inputs(vcfg, num_drafts=np.full(B, K, dtype=np.int32), planted_ids=planted)
+        self.planted_len = n
+        self.target = dev(vi.logits)
+        self.row_offsets = dev(vi.row_offsets)
+        self.num_drafts = dev(vi.num_drafts)
+        self.vi = vi
+
+    def draft(self, logits=True):
+        import mtp_self_speculative_gb300 as M
+        M.mtp_draft(self.ctx, self.hidden, self.embeds, self.positions, self.kv, self.K, self.ids,
+                    self.logits if logits else None)
+
+    def step(self):
+        import mtp_self_speculative_gb300 as M
+        self.draft()
+        M.mtp_verify(self.ctx, self.target, self.row_offsets, self.ids, self.num_drafts, self.acc, self.bonus)
+        M.mtp_kv_commit_accepted(self.ctx, self.kv, self.acc, extra=1)
+        M.mtp_kv_truncate(self.ctx, self.kv, self.L0)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    import mtp_self_speculative_gb300 as M
+    cfg = WORKLOADS[args.workload]
+    if cfg.H == 0:
+        raise SystemExit("workload %s has no draft head; pick a draft workload" % cfg.name)
+    K = cfg.K
+    wl = Workload(cfg, K)
+    stream = torch.cuda.current_stream()
+
+    # bandwidth yardstick in the same run: 1 GiB device-to-device copy
+    nbytes = 1 << 30
+    src = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda").fill_(1)
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        M.mtp_stream_copy(dst, src)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    copies = []
+    for _ in range(10):
+        e0.record(stream)
+        M.mtp_stream_copy(dst, src)
+        e1.record(stream)
+        e1.synchronize()
+        copies.append(e0.elapsed_time(e1))
+    copy_gbs = 2 * nbytes / (min(copies) * 1e-3) / 1e9
+    del src, dst
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(wl.ctx) == 0
+
+    lm_cap = args.steps * K
+    M.mtp_profile_begin(wl.ctx, M.MTP_KERNEL_LM_HEAD, lm_cap)
+    launches0 = M.mtp_launch_count(wl.ctx)
+    sampler = ClockSampler(gpu_id_for_smi(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        wl.step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    launches = M.mtp_launch_count(wl.ctx) - launches0
+    lm_ms = M.mtp_profile_end(wl.ctx, lm_cap)
+    elapsed_ms = t0.elapsed_time(t1)
+    assert M.mtp_get_device_error(wl.ctx) == 0
+    ids_now = wl.ids.cpu().numpy()
+    deterministic = bool(np.array_equal(ids_now, wl.ids0))
+    acc = wl.acc.cpu().numpy()
+    elapsed_max = reduce_max(elapsed_ms, world)
+
+    # draft-only timing (the roofline target is the draft step)
+    M.mtp_kv_rollback(wl.ctx, wl.kv)
+    nd = max(10, args.steps // 4)
+    t0.record(stream)
+    for _ in range(nd):
+        wl.draft()
+        M.mtp_kv_rollback(wl.ctx, wl.kv)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    draft_ms = t0.elapsed_time(t1) / nd
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(wl, max(5, min(args.steps // 4, 200)))
+
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    sb = step_bytes(cfg, wl.lens, K)
+    ms_per_step = elapsed_max / args.steps
+    steps_s = world * args.steps / (elapsed_max * 1e-3)
+    emitted = int(np.sum(acc + 1))
+    lm_avg_ms = statistics.mean(lm_ms) if lm_ms else float("nan")
+    lm_gbs = sb["lm_head_launch"] / (lm_avg_ms * 1e-3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    line = {
+        "metric": METRIC,
+        "value": steps_s,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden/KV, uniform token ids)",
+        "config": {"workload": cfg.name, "hidden": cfg.H, "q_heads": cfg.n_q, "kv_heads": cfg.n_kv,
+                   "head_dim": cfg.head_dim, "ffn": cfg.ffn, "vocab": cfg.vocab, "batch": wl.B,
+                   "draft_steps_K": K, "mtp_context": [int(wl.lens.min()), int(wl.lens.max())],
+                   "tied_lm_head": True, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (%.2f GB of weights streamed per draft step)" %
+                         (sb["weights"] / 1e9)},
+        "accepted_tok_s": {"emitted": emitted * steps_s, "accepted_drafts": int(np.sum(acc)) * steps_s,
+                           "mean_emitted_per_step": emitted / wl.B},
+        "draft": {"ms_per_draft_call": draft_ms, "ms_per_draft_step": draft_ms / K,
+                  "bytes_per_draft_step": sb["draft"] / K,
+                  "hbm_frac_of_measured": sb["draft"] / (draft_ms * 1e-3) / 1e9 / peak},
+        "step_hbm": {"bytes_per_step": sb["total"],
+                     "achieved_gbs": sb["total"] / (ms_per_step * 1e-3) / 1e9,
+                     "frac_of_measured": sb["total"] / (ms_per_step * 1e-3) / 1e9 / peak},
+        "roofline": {"kernel": "lm_head_argmax", "bound": "hbm", "achieved": lm_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": lm_gbs / peak, "peak_source": peak_kind + " hbm_gbs",
+                     "traffic": args.lm_traffic, "launches_timed": len(lm_ms),
+                     "bytes_per_launch": sb["lm_head_launch"]},
+        "stream_copy_gbs": copy_gbs,
+        "gpu_launches": int(launches),
+        "deterministic_ids": deterministic,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(wl: Workload, n: int) -> dict:
+    """steps/s through the public API with pinned host inputs copied in and
+    the step's results (draft ids, accepted counts, bonus ids) read back every
+    step."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    h_hidden = wl.hidden.cpu().pin_memory()
+    h_embeds = wl.embeds.cpu().pin_memory()
+    h_pos = wl.positions.cpu().pin_memory()
+    h_target = wl.target.cpu().pin_memory()
+    h_ids = torch.empty_like(wl.ids, device="cpu").pin_memory()
+    h_acc = torch.empty_like(wl.acc, device="cpu").pin_memory()
+    h_bonus = torch.empty_like(wl.bonus, device="cpu").pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in (h_hidden, h_embeds, h_pos, h_target))
+    bo = sum(t.numel() * t.element_size() for t in (h_ids, h_acc, h_bonus))
+
+    def one():
+        wl.hidden.copy_(h_hidden, non_blocking=True)
+        wl.embeds.copy_(h_embeds, non_blocking=True)
+        wl.positions.copy_(h_pos, non_blocking=True)
+        wl.target.copy_(h_target, non_blocking=True)
+        M.mtp_draft(wl.ctx, wl.hidden, wl.embeds, wl.positions, wl.kv, wl.K, wl.ids, wl.logits)
+        M.mtp_verify(wl.ctx, wl.target, wl.row_offsets, wl.ids, wl.num_drafts, wl.acc, wl.bonus)
+        M.mtp_kv_commit_accepted(wl.ctx, wl.kv, wl.acc, extra=1)
+        M.mtp_kv_truncate(wl.ctx, wl.kv, wl.L0)
+        h_ids.copy_(wl.ids, non_blocking=True)
+        h_acc.copy_(wl.acc, non_blocking=True)
+        h_bonus.copy_(wl.bonus, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = time.perf_counter() - t
+    return {"value": n / dt, "unit": "steps/s", "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "steps": n}
+
+
+# ------------------------------------------------------- CPU / oracle legs
+
+def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1) -> dict:
+    """The float64 oracle as it stands, one full step (K draft steps, verify,
+    commit) for the same workload on the host cores."""
+    import oracle as O
+    w = synth.make_weights(cfg, norm="ones")
+    lens = synth.context_lengths(cfg)
+    kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
+    di = synth.make_draft_inputs(cfg, w, lens)
+    W = O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+    vi = synth.make_verify_inputs(synth.shrink(cfg, k_lo=0, k_hi=0), num_drafts=np.full(len(lens), cfg.K, np.int32))
+    t = time.perf_counter()
+    for _ in range(sample_steps):
+        res = O.draft(W, O.widen(di.hidden, cfg.dtype), O.widen(di.embeds, cfg.dtype), di.positions, kv, cfg.K)
+        acc, _ = O.verify(vi.logits, vi.row_offsets, res.ids, vi.num_drafts, cfg.dtype)
+        O.kv_commit(kv, np.minimum(acc + 1, cfg.K), cfg.dtype)
+        O.kv_truncate(kv, lens, cfg.dtype)
+    dt = (time.perf_counter() - t) / sample_steps
+    return {"value": 1.0 / dt, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "%d full step(s): %d draft steps + verify + commit, B=%d, float64 numpy" %
+                      (sample_steps, cfg.K, len(lens))}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed as the reference arm.  A step is sampled as one of
+    the K draft steps (the decoder layer, LM head and argmax for the whole
+    batch) plus one K-th of the verify rows; the full step is K such samples.
+    The number of samples is capped so the run stays within a few minutes."""
+    if rank != 0:
+        return
+    import oracle as O
+    cfg = WORKLOADS[args.workload]
+    w = synth.make_weights(cfg, norm="ones")
+    lens = synth.context_lengths(cfg)
+    kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
+    di = synth.make_draft_inputs(cfg, w, lens)
+    W = O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+    vi = synth.make_verify_inputs(synth.shrink(cfg, k_lo=0, k_hi=0), num_drafts=np.full(len(lens), cfg.K, np.int32))
+    hid, emb = O.widen(di.hidden, cfg.dtype), O.widen(di.embeds, cfg.dtype)
+
+    def sample():
+        res = O.draft(W, hid, emb, di.positions, kv, 1)
+        O.kv_rollback(kv, cfg.dtype)
+        O.verify(vi.logits, vi.row_offsets, np.repeat(res.ids, cfg.K, axis=1), vi.num_drafts, cfg.dtype)
+
+    budget = float(os.environ.get("MTP_REFERENCE_BUDGET_S", "150"))
+    t_start = time.perf_counter()
+    for _ in range(min(args.warmup, 1)):
+        sample()
+    times = []
+    for i in range(args.steps):
+        t = time.perf_counter()
+        sample()
+        times.append(time.perf_counter() - t)
+        if time.perf_counter() - t_start > budget:
+            break
+    # one sample is one draft step plus verify (verify is counted K times; it is
+    # under 1% of the sample), so a full step costs K samples
+    per_step = cfg.K * statistics.mean(times)
+    value = 1.0 / per_step
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": len(lens), "draft_steps_K": cfg.K},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                             "sample": "%d sampled draft step(s) of the float64 numpy oracle (decoder layer, "
+                                       "LM head, argmax, verify), scaled by K=%d to a full step%s" %
+                                       (len(times), cfg.K, "; capped by the time budget" if len(times) < args.steps
+                                        else "")},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "samples_run": len(times)}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lm-traffic", type=float, default=None,
+                    help="ncu dram bytes per LM-head launch of the current kernel, if captured")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = rank_info()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
