@@ -152,6 +152,33 @@ mtp_status mtp_verify(mtp_ctx* ctx, void* stream, int B, const void* target_logi
                       const int32_t* row_offsets, const int32_t* drafts, int drafts_stride,
                       const int32_t* num_drafts, int32_t* accepted, int32_t* bonus);
 
+/* Greedy verification without a context and without allocating.  The
+ * pages have no counterpart: this is a deployment variant of mtp_verify for
+ * callers that cannot allocate device memory where they verify -- a serving
+ * loop whose device memory is wholly owned by a fixed plan or another
+ * framework's pool, or a latency-bound loop that cannot afford the implicit
+ * device-wide synchronisation of cudaMalloc (mtp_init allocates, so such a
+ * caller cannot create a context there).  Same arguments and results as
+ * mtp_verify, with the shape passed directly: vocab, dtype (mtp_dtype) and
+ * max_k (0..100) in place of the context.
+ *   Scratch: a fixed array of 65536 argmax keys and 4096 counters (about
+ *   530 KB) that is part of the library's device image; every GPU that loads
+ *   the library holds it until the process exits.  Requires B <= 4096 and
+ *   B * (max_k + 1) <= 65536, else MTP_ERR_INVALID.
+ *   Set-up: the first call on a device looks up that array's device address
+ *   (once per device, under a lock); make that first call before any stream
+ *   capture on the device.
+ *   Sharing: every call uses the same array and clears the part it needs on
+ *   `stream` before its kernel; calls whose work overlaps on the GPU (other
+ *   streams, other host threads) race on it and must be serialised by the
+ *   caller.  Device-detected argument errors give accepted[b] = bonus[b] = -1
+ *   (there is no context error word).  Nothing is allocated: no cudaMalloc,
+ *   cudaFree or allocating library routine is called. */
+mtp_status mtp_verify_noalloc(void* stream, int B, int vocab, int dtype, int max_k, const void* target_logits,
+                              int num_rows, const int32_t* row_offsets, const int32_t* drafts,
+                              int drafts_stride, const int32_t* num_drafts, int32_t* accepted,
+                              int32_t* bonus);
+
 /* Commit ("Stateful execution"; "Tree Drafting" step 4): request b keeps
  * its first n_keep[b] drafted slots, the other drafted slots are zeroed in
  * place, seq_len[b] += n_keep[b], pending[b] = 0.  n_keep [B] int32 device

@@ -143,6 +143,23 @@ def mtp_verify(ctx: Context, target_logits: torch.Tensor, row_offsets: torch.Ten
                            _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus")), "mtp_verify")
 
 
+def mtp_verify_noalloc(target_logits: torch.Tensor, row_offsets: torch.Tensor, drafts: torch.Tensor,
+                       num_drafts: torch.Tensor, accepted: torch.Tensor, bonus: torch.Tensor, vocab: int,
+                       max_k: int, stream=None) -> None:
+    """mtp_verify without a context and without any device allocation (for
+    callers whose device memory is owned by a fixed plan or another pool, or
+    who cannot take cudaMalloc's device-wide synchronisation); the shape is
+    passed directly and the scratch is the library's fixed device array."""
+    code = MTP_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else MTP_DTYPE_F32
+    B = int(num_drafts.shape[0])
+    _check(_clib.mtp_verify_noalloc(_stream(stream), B, int(vocab), code, int(max_k),
+                                    _ptr(target_logits, name="target_logits"), int(target_logits.shape[0]),
+                                    _ptr(row_offsets, torch.int32, "row_offsets"), _ptr(drafts, torch.int32, "drafts"),
+                                    int(drafts.shape[1]), _ptr(num_drafts, torch.int32, "num_drafts"),
+                                    _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus")),
+           "mtp_verify_noalloc")
+
+
 def mtp_kv_commit(ctx: Context, kv: KVCache, n_keep: torch.Tensor, stream=None) -> None:
     kvs = kv.struct()
     _check(_clib.mtp_kv_commit(ctx.handle, _stream(stream), int(kv.seq_len.shape[0]), ctypes.byref(kvs),

@@ -46,6 +46,8 @@ SIGNATURES = {
     "mtp_draft": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P_i32, ctypes.POINTER(MTPKV), c_int,
                           P_i32, P_i32, c_void_p, c_void_p]),
     "mtp_verify": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, P_i32, P_i32, c_int, P_i32, P_i32, P_i32]),
+    "mtp_verify_noalloc": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int, P_i32, P_i32, c_int,
+                                   P_i32, P_i32, P_i32]),
     "mtp_kv_commit": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
     "mtp_kv_commit_accepted": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32, c_int]),
     "mtp_kv_rollback": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV)]),

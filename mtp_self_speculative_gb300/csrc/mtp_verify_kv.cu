@@ -15,6 +15,8 @@
 // "Prefix Caching with Speculative Decoding"): one CTA per request zeroes the
 // slots that leave the cache with 16-byte stores through the block table and
 // then updates seq_len and pending.
+#include <mutex>
+
 #include "mtp_common.cuh"
 
 namespace mtp {
@@ -279,3 +281,104 @@ cudaError_t launch_stream_copy(cudaStream_t s, void* dst, const void* src, size_
 }
 
 }  // namespace mtp
+
+// ------------------------------------------- allocation-free verification
+//
+// mtp_verify needs a context, and mtp_init allocates the context's workspace
+// with cudaMalloc.  Some callers cannot allocate device memory at the point
+// where they verify: a serving loop whose device memory is all owned by a
+// fixed plan or by another framework's pool, or a loop on a latency budget
+// where cudaMalloc's implicit device-wide synchronisation would stall every
+// other stream.  mtp_verify_noalloc runs the same verify kernel with its
+// scratch (argmax keys and arrival counters) in the array below, which is part
+// of the library's device image: it is created when the library's code is
+// loaded on a GPU and stays resident there until the process exits.
+namespace mtp {
+
+constexpr int kNoAllocMaxKeys = 65536;   // B * (max_k + 1) rows
+constexpr int kNoAllocMaxBatch = 4096;   // B
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocScratch {
+  unsigned long long keys[kNoAllocMaxKeys];
+  int cnt[kNoAllocMaxBatch];
+  int err;
+};
+
+static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+static NoAllocScratch* g_noalloc_ptr[kNoAllocMaxDevices];
+static int g_noalloc_sms[kNoAllocMaxDevices];
+static std::mutex g_noalloc_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code may not use the symbol itself as a device pointer).
+static cudaError_t noalloc_setup(int dev, NoAllocScratch** out, int* sms) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_noalloc_sms[dev] = n;
+    g_noalloc_ptr[dev] = (NoAllocScratch*)p;
+  }
+  *out = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  return cudaSuccess;
+}
+
+}  // namespace mtp
+
+extern "C" mtp_status mtp_verify_noalloc(void* stream, int B, int vocab, int dtype, int max_k,
+                                         const void* target_logits, int num_rows, const int32_t* row_offsets,
+                                         const int32_t* drafts, int drafts_stride, const int32_t* num_drafts,
+                                         int32_t* accepted, int32_t* bonus) {
+  using namespace mtp;
+  if (B < 1 || B > kNoAllocMaxBatch || max_k < 0 || max_k > 100 || (long long)B * (max_k + 1) > kNoAllocMaxKeys)
+    return MTP_ERR_INVALID;
+  if (vocab < 1 || (dtype != MTP_DTYPE_F32 && dtype != MTP_DTYPE_BF16) || num_rows < 1 || drafts_stride < 1)
+    return MTP_ERR_INVALID;
+  if (!target_logits || !row_offsets || !drafts || !num_drafts || !accepted || !bonus) return MTP_ERR_INVALID;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MTP_ERR_CUDA;
+  NoAllocScratch* sc = nullptr;
+  int sms = 0;
+  if (noalloc_setup(dev, &sc, &sms) != cudaSuccess) {
+    cudaGetLastError();
+    return MTP_ERR_CUDA;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // The array keeps whatever the previous call left: clear the part this
+  // call counts on.
+  const size_t key_bytes = (size_t)B * (max_k + 1) * sizeof(unsigned long long);
+  if (cudaMemsetAsync(sc->keys, 0, key_bytes, s) != cudaSuccess ||
+      cudaMemsetAsync(sc->cnt, 0, (size_t)B * sizeof(int), s) != cudaSuccess ||
+      cudaMemsetAsync(&sc->err, 0, sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return MTP_ERR_CUDA;
+  }
+  const int rows = B * (max_k + 1);
+  int splits = (4 * sms + rows - 1) / rows;
+  const int max_splits = (vocab + 2047) / 2048;
+  if (splits > max_splits) splits = max_splits;
+  if (splits < 1) splits = 1;
+  dim3 grid(splits, max_k + 1, B);
+  cudaError_t e;
+  if (dtype == MTP_DTYPE_BF16) {
+    VerifyArgs<uint16_t> a{(const uint16_t*)target_logits, row_offsets, drafts, drafts_stride, num_drafts, accepted,
+                           bonus, sc->keys, sc->cnt, &sc->err, vocab, max_k, splits, num_rows};
+    e = launch_pdl(verify_kernel<uint16_t>, grid, dim3(kVerifyThreads), 0, s, a);
+  } else {
+    VerifyArgs<float> a{(const float*)target_logits, row_offsets, drafts, drafts_stride, num_drafts, accepted, bonus,
+                        sc->keys, sc->cnt, &sc->err, vocab, max_k, splits, num_rows};
+    e = launch_pdl(verify_kernel<float>, grid, dim3(kVerifyThreads), 0, s, a);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MTP_ERR_CUDA;
+  }
+  return MTP_OK;
+}
