@@ -72,6 +72,10 @@ typedef struct {
   int max_k;             /* largest draft count K of any call (1..100)        */
   int block_size;        /* KV tokens per paged block; must be 16             */
   int max_pos;           /* positions + K - 1 must stay below this            */
+  int tc_min_batch;      /* batches of at least this many requests use the
+                            tensor-core (tcgen05) path when the shape allows
+                            it (bf16, head_dim 128, H % 128 == 0, F and
+                            n_q*head_dim % 64 == 0, B <= 256); 0 = 16      */
 } mtp_config;
 
 /* Borrowed head weights (device pointers, layouts [out, in] row-major).

@@ -96,10 +96,10 @@ class Context:
 
 
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps=1e-6, rope_theta=1e6, dtype="bf16",
-                max_batch=1, max_k=5, block_size=16, max_pos=32768) -> MTPConfig:
+                max_batch=1, max_k=5, block_size=16, max_pos=32768, tc_min_batch=0) -> MTPConfig:
     code = MTP_DTYPE_BF16 if dtype in ("bf16", MTP_DTYPE_BF16, torch.bfloat16) else MTP_DTYPE_F32
     return MTPConfig(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps, rope_theta, code, max_batch, max_k,
-                     block_size, max_pos)
+                     block_size, max_pos, tc_min_batch)
 
 
 def mtp_init(cfg: MTPConfig, weights: Optional[Dict[str, torch.Tensor]] = None, device: Optional[int] = None

@@ -24,7 +24,8 @@ KERNEL_NAMES = ["eh_proj", "qkv_rope", "attention", "o_proj", "gate_up", "down",
 class MTPConfig(ctypes.Structure):
     _fields_ = [("hidden", c_int), ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
                 ("ffn", c_int), ("vocab", c_int), ("eps", c_float), ("rope_theta", c_float), ("dtype", c_int),
-                ("max_batch", c_int), ("max_k", c_int), ("block_size", c_int), ("max_pos", c_int)]
+                ("max_batch", c_int), ("max_k", c_int), ("block_size", c_int), ("max_pos", c_int),
+                ("tc_min_batch", c_int)]
 
 
 WEIGHT_FIELDS = ["w_norm_h", "w_norm_e", "w_eh", "w_norm_in", "w_q", "w_k", "w_v", "w_o", "w_norm_post",

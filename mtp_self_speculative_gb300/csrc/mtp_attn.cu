@@ -32,6 +32,7 @@ template <typename T>
 struct AttnArgs {
   const float* q;        // [B, n_q * d] rotated queries
   float* out;            // [B, n_q * d]
+  uint16_t* out_bf16;    // [B, n_q * d] bf16 copy for the tensor-core O-proj, or null
   float* part;           // [B, n_q, max_splits, d + 2]
   int* cnt;              // [B, n_kv]
   int* err;
@@ -277,7 +278,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
       O += wacc[((size_t)w * G + h) * HD + d] * f;
     }
     if (nsplit == 1) {
-      a.out[(size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d] = O / L;
+      const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
+      a.out[oi] = O / L;
+      if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(O / L);
     } else {
       float* pp = part_base + ((size_t)h * a.max_splits + s) * (HD + 2);
       if (d == 0) { pp[0] = M; pp[1] = L; }
@@ -307,7 +310,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
       L += __ldcg(pj + 1) * f;
       O += __ldcg(pj + 2 + d) * f;
     }
-    a.out[(size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d] = O / L;
+    const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
+    a.out[oi] = O / L;
+    if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(O / L);
   }
   if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
 }
@@ -339,7 +344,7 @@ template <typename T>
 static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv) {
   const mtp_config& c = ctx->cfg;
   AttnArgs<T> a;
-  a.q = ctx->q; a.out = ctx->attn; a.part = ctx->attn_part; a.cnt = ctx->attn_cnt; a.err = ctx->err;
+  a.q = ctx->q; a.out = ctx->attn; a.out_bf16 = tc_supported(ctx, B) ? ctx->tc_attn : nullptr; a.part = ctx->attn_part; a.cnt = ctx->attn_cnt; a.err = ctx->err;
   a.k_pool = (const T*)kv->k_pool; a.v_pool = (const T*)kv->v_pool;
   a.block_table = kv->block_table; a.seq_len = kv->seq_len; a.k = k;
   a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.max_blocks = kv->max_blocks; a.num_blocks = kv->num_blocks;

@@ -196,6 +196,15 @@ struct mtp_ctx {
   int* ver_cnt;                 // [maxB]
   int* err;                     // [1]
   float2* rope;                 // [max_pos, head_dim / 2] (cos, sin)
+  // tensor-core path (allocated when the shape allows it)
+  void* tc_ws;
+  int tc_min_batch;
+  uint16_t* tc_xin_eh;          // [maxB, 2H] bf16 eh_proj input
+  uint16_t* tc_xn;              // [maxB, H]  bf16 normalised GEMM input
+  uint16_t* tc_attn;            // [maxB, q_dim] bf16 attention output
+  uint16_t* tc_act;             // [maxB, F]  bf16 silu(g) * u
+  float* tc_fix;                // [2 * num_sms, NTmax, 128] stream-K pieces
+  int* tc_tile_cnt;             // [max tiles]
   // timing
   int prof_kernel;
   int prof_cap;
@@ -231,6 +240,10 @@ cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K,
                               const void* embeds, const int32_t* positions, const mtp_kv* kv,
                               const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
 cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv);
+bool tc_supported(const mtp_ctx* ctx, int B);
+cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
+                                 const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                                 const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
 cudaError_t launch_verify(mtp_ctx* ctx, cudaStream_t s, int B, const void* logits, int num_rows,
                           const int32_t* row_offsets,
                           const int32_t* drafts, int drafts_stride, const int32_t* num_drafts,

@@ -1,0 +1,725 @@
+// Tensor-core (tcgen05) path of the draft step for batches of 16..256
+// requests, bf16 weights, head_dim 128.
+//
+// Every projection of "MTP (Multi-Token Prediction)", "Architecture" becomes
+// a skinny GEMM  D[128-row weight tile, N] = W_tile . X^T  with the weights
+// as the 128-row A operand and the (padded) batch as N: the weight stream is
+// read once per draft step, the activations (<= 2.6 MB) stay in L2.
+//
+// Kernel organisation (one CTA per SM, 6 warps):
+//   warp 0   TMA producer: 2-D tensor-map loads of the weight tile (128 x 64
+//            bf16, 128-byte swizzle) and the activation tile (N x 64) into a
+//            ring of shared-memory stages (full/empty mbarriers).  The weight
+//            loads of the first stages are issued before the programmatic
+//            dependency wait, so the stream starts while the previous kernel
+//            drains.
+//   warp 1   owns the TMEM allocation (2 accumulators of N fp32 columns) and
+//            issues tcgen05.mma (M=128, N, K=16) from one thread; commits
+//            free the stages and publish finished accumulators.
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM
+//            lanes 32*(w%4)..+31), fused epilogue per kind, stores.
+// Work split: the (tile, 64-wide k-block) units are divided evenly over the
+// CTAs (stream-K).  A tile cut by a CTA boundary is summed deterministically:
+// each piece is written to a fix-up slot, and the last piece to arrive adds
+// all pieces in k order before the epilogue.
+//
+// Epilogue kinds: EH_PROJ (x = D), QKV_ROPE (rotary pairs (i, i+64) of one
+// head exchanged through shared memory; q stored fp32, k/v rounded to bf16
+// into the paged cache), O_PROJ (h1 = x + D), GATE_UP (tile = 64 gate rows +
+// the matching 64 up rows; act = silu(g) * u stored bf16), DOWN (h2 = h1 + D),
+// LM_HEAD (logits; per-column argmax with warp max-reduce + ballot, CTA best
+// in shared memory, one 64-bit atomicMax per request per CTA, last CTA writes
+// the draft ids).
+//
+// RMSNorm inputs are produced by small prep kernels (one CTA per request)
+// that write bf16 GEMM operands.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "mtp_common.cuh"
+
+namespace mtp {
+
+enum TcKind { TC_EH = 0, TC_QKV = 1, TC_O = 2, TC_GU = 3, TC_DOWN = 4, TC_LM = 5 };
+
+constexpr int kTcThreads = 192;
+constexpr int kTcEpiThreads = 128;
+constexpr uint32_t kTcWaitLimit = 1u << 26;
+constexpr int kTcTileBytesA = 128 * 64 * 2;   // 16 KB
+
+struct TcMaps {
+  CUtensorMap a0, a1, a2;  // weight maps (QKV: q, k, v; GATE_UP: gate, up)
+  CUtensorMap b;           // activation map [B rows, C] bf16
+};
+
+struct TcArgs {
+  int kind;
+  int B, NT, H, q_dim, kv_dim, F, V, n_q, n_kv, bs, k, K;
+  int C, nkb, n_tiles, stages, max_pos, num_blocks, max_blocks;
+  const int32_t* positions;
+  int32_t* draft_ids;
+  float* logits;
+  float* hidden_out;
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  int32_t* pending;
+  float *hid, *x, *q, *h1;
+  uint16_t* act_bf16;
+  float* fix;              // [2 * grid][NT][128]
+  int* tile_cnt;           // [n_tiles]
+  unsigned long long* lm_keys;
+  int* lm_cnt;
+  int* err;
+  const float2* rope;
+};
+
+// ------------------------------------------------------------ primitives
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)1 << 16;               // leading offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;     // 1024 B between 8-row groups
+  d |= (uint64_t)1 << 46;               // descriptor version
+  d |= (uint64_t)2 << 61;               // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Bounded wait that also gives up once another role has given up.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t i = 0; i < kTcWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort_flag) return false;
+  }
+  return false;
+}
+
+// --------------------------------------------------------- work partition
+struct Part {
+  int u0, u1;  // this CTA's units [u0, u1)
+};
+__device__ __forceinline__ int unit_begin(long long i, long long U, long long G) { return (int)((i * U) / G); }
+__device__ __forceinline__ int cta_of_unit(long long u, long long U, long long G) {
+  return (int)(((u + 1) * G - 1) / U);
+}
+
+// ----------------------------------------------------------- epilogues
+
+struct EpiCtx {
+  int tile, m, lane, quarter;  // m = row of the tile held by this thread
+  float* xbuf;                 // [64][16] exchange buffer
+  unsigned long long* cta_best;
+};
+
+// Apply the epilogue to 16 columns [c0, c0 + 16) of this thread's row.
+__device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const float (&v)[16]) {
+  const int kind = a.kind;
+  if (kind == TC_EH || kind == TC_O || kind == TC_DOWN) {
+    const int r = e.tile * 128 + e.m;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int b = c0 + j;
+      if (b >= a.B || r >= a.H) continue;
+      const size_t o = (size_t)b * a.H + r;
+      if (kind == TC_EH) {
+        a.x[o] = v[j];
+      } else if (kind == TC_O) {
+        a.h1[o] = a.x[o] + v[j];
+      } else {
+        const float hv = a.h1[o] + v[j];
+        a.hid[o] = hv;
+        if (a.hidden_out && a.k == a.K) a.hidden_out[o] = hv;
+      }
+    }
+    return;
+  }
+  if (kind == TC_LM) {
+    const int r = e.tile * 128 + e.m;
+    const bool row_ok = r < a.V;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int b = c0 + j;
+      if (b >= a.B) continue;  // uniform across the warp
+      if (a.logits && row_ok) a.logits[((size_t)b * a.K + (a.k - 1)) * a.V + r] = v[j];
+      const uint32_t ord = row_ok ? ordered_bits(v[j]) : 0u;
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, ord);
+      const uint32_t bal = __ballot_sync(0xffffffffu, ord == mx);
+      if (e.lane == (b & 31)) {
+        const uint32_t row = (uint32_t)(e.tile * 128 + e.quarter * 32 + (__ffs(bal) - 1));
+        const unsigned long long key = ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - row);
+        atomicMax(e.cta_best + b, key);
+      }
+    }
+    return;
+  }
+  // Pair kinds: rows m and m + 64 of the tile belong together.
+  const bool upper = e.m >= 64;
+  if (upper) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) e.xbuf[(e.m - 64) * 16 + j] = v[j];
+  }
+  epi_bar();
+  if (!upper) {
+    const int i = e.m;
+    if (kind == TC_GU) {
+      const int f = e.tile * 64 + i;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int b = c0 + j;
+        if (b >= a.B || f >= a.F) continue;
+        const float g = v[j], u = e.xbuf[i * 16 + j];
+        a.act_bf16[(size_t)b * a.F + f] = f32_to_bf16_rne(g / (1.0f + __expf(-g)) * u);
+      }
+    } else {  // TC_QKV: tile = head
+      const int grp = e.tile;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int b = c0 + j;
+        if (b >= a.B) continue;
+        const float v0 = v[j], v1 = e.xbuf[i * 16 + j];
+        const int pos = a.positions[b] + a.k - 1;
+        if (pos < 0 || pos >= a.max_pos) {
+          set_error(a.err, MTP_ERR_CAPACITY);
+          continue;
+        }
+        if (grp < a.n_q) {
+          const float2 cs = a.rope[(size_t)pos * 64 + i];
+          float* qb = a.q + (size_t)b * a.q_dim + grp * 128;
+          qb[i] = v0 * cs.x - v1 * cs.y;
+          qb[i + 64] = v1 * cs.x + v0 * cs.y;
+          continue;
+        }
+        if (a.pending[b] != a.k - 1) {
+          set_error(a.err, MTP_ERR_DEVICE_ARGS);
+          continue;
+        }
+        const int slot = a.seq_len[b] + a.k - 1;
+        const int bi = slot / a.bs, off = slot - bi * a.bs;
+        const int blk = (slot >= 0 && bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+        if (blk < 0 || blk >= a.num_blocks) {
+          set_error(a.err, MTP_ERR_CAPACITY);
+          continue;
+        }
+        float o0 = v0, o1 = v1;
+        uint16_t* pool;
+        int g;
+        if (grp < a.n_q + a.n_kv) {
+          const float2 cs = a.rope[(size_t)pos * 64 + i];
+          o0 = v0 * cs.x - v1 * cs.y;
+          o1 = v1 * cs.x + v0 * cs.y;
+          pool = a.k_pool;
+          g = grp - a.n_q;
+        } else {
+          pool = a.v_pool;
+          g = grp - a.n_q - a.n_kv;
+        }
+        uint16_t* dst = pool + (((size_t)blk * a.n_kv + g) * a.bs + off) * 128;
+        dst[i] = f32_to_bf16_rne(o0);
+        dst[i + 64] = f32_to_bf16_rne(o1);
+      }
+    }
+  }
+  epi_bar();
+}
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[8], empty_bar[8], accf_bar[2], acce_bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ volatile int abort_flag;
+  __shared__ int last_flag, stop_snap;
+  __shared__ float xbuf[64 * 16];
+  __shared__ unsigned long long cta_best[256];
+
+  unsigned char* smem = (unsigned char*)(((uintptr_t)tc_smem_raw + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NT = a.NT, NS = a.stages;
+  const uint32_t bytes_b = (uint32_t)NT * 128;
+  const uint32_t stage_bytes = kTcTileBytesA + bytes_b;
+  const uint32_t tmem_cols = (2 * NT <= 32) ? 32 : (2 * NT <= 64) ? 64 : (2 * NT <= 128) ? 128 : (2 * NT <= 256) ? 256 : 512;
+
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accf_bar[0], 1);
+    mbar_init(&accf_bar[1], 1);
+    mbar_init(&acce_bar[0], 4);
+    mbar_init(&acce_bar[1], 4);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < 256; i += kTcThreads) cta_best[i] = 0ull;
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
+                 "r"(tmem_cols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  const long long G = gridDim.x, U = (long long)a.n_tiles * a.nkb;
+  const int u0 = unit_begin(blockIdx.x, U, G), u1 = unit_begin(blockIdx.x + 1, U, G);
+  const int first_tile = u0 / a.nkb;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer
+      auto a_coords = [&](int tile, const CUtensorMap*& m0, int& row) {
+        if (a.kind == TC_QKV) {
+          if (tile < a.n_q) { m0 = &maps.a0; row = tile * 128; }
+          else if (tile < a.n_q + a.n_kv) { m0 = &maps.a1; row = (tile - a.n_q) * 128; }
+          else { m0 = &maps.a2; row = (tile - a.n_q - a.n_kv) * 128; }
+        } else if (a.kind == TC_GU) {
+          m0 = &maps.a0;
+          row = tile * 64;
+        } else {
+          m0 = &maps.a0;
+          row = tile * 128;
+        }
+      };
+      auto issue_a = [&](int it_stage, int tile, int kb) {
+        unsigned char* st = smem + (size_t)it_stage * stage_bytes;
+        const CUtensorMap* m0;
+        int row;
+        a_coords(tile, m0, row);
+        if (a.kind == TC_GU) {
+          tma_load_2d(st, &maps.a0, kb * 64, row, &full_bar[it_stage]);
+          tma_load_2d(st + 8192, &maps.a1, kb * 64, row, &full_bar[it_stage]);
+        } else {
+          tma_load_2d(st, m0, kb * 64, row, &full_bar[it_stage]);
+        }
+      };
+      auto issue_b = [&](int it_stage, int kb) {
+        unsigned char* st = smem + (size_t)it_stage * stage_bytes;
+        tma_load_2d(st + kTcTileBytesA, &maps.b, kb * 64, 0, &full_bar[it_stage]);
+      };
+      const int n_it = u1 - u0;
+      const int pre = n_it < NS ? n_it : NS;
+      for (int it = 0; it < pre; ++it) {
+        const int u = u0 + it;
+        mbar_expect_tx(&full_bar[it], stage_bytes);
+        issue_a(it, u / a.nkb, u % a.nkb);
+      }
+      pdl_wait();
+      for (int it = 0; it < pre; ++it) issue_b(it, (u0 + it) % a.nkb);
+      for (int it = pre; it < n_it; ++it) {
+        const int s = it % NS;
+        if (!tc_wait(&empty_bar[s], ((it / NS) & 1) ^ 1, &abort_flag)) {
+          abort_flag = 1;
+          set_error(a.err, MTP_ERR_TIMEOUT);
+          break;
+        }
+        const int u = u0 + it;
+        mbar_expect_tx(&full_bar[s], stage_bytes);
+        issue_a(s, u / a.nkb, u % a.nkb);
+        issue_b(s, u % a.nkb);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+      int it = 0, seg = 0;
+      bool ok = true;
+      for (int u = u0; u < u1 && ok; ++seg) {
+        const int tile = u / a.nkb;
+        const int ue = min(u1, (tile + 1) * a.nkb);
+        const int buf = seg & 1;
+        if (!tc_wait(&acce_bar[buf], ((seg >> 1) & 1) ^ 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * NT);
+        for (int uu = u; uu < ue; ++uu, ++it) {
+          const int s = it % NS;
+          if (!tc_wait(&full_bar[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa_ = smem_addr(smem + (size_t)s * stage_bytes);
+          const uint32_t sb_ = sa_ + kTcTileBytesA;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma(d, sw128_desc(sa_ + kk * 32), sw128_desc(sb_ + kk * 32), idesc, (uu > u || kk > 0) ? 1u : 0u);
+          tc_commit(&empty_bar[s]);
+        }
+        if (!ok) break;
+        tc_commit(&accf_bar[buf]);
+        u = ue;
+      }
+      if (!ok) {
+        abort_flag = 1;
+        set_error(a.err, MTP_ERR_TIMEOUT);
+      }
+    }
+  } else {
+    // epilogue warps 2..5
+    pdl_wait();
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const int epi_tid = threadIdx.x - 64;
+    EpiCtx e;
+    e.m = m;
+    e.lane = lane;
+    e.quarter = quarter;
+    e.xbuf = xbuf;
+    e.cta_best = cta_best;
+    int seg = 0;
+    for (int u = u0; u < u1; ++seg) {
+      const int tile = u / a.nkb;
+      const int ue = min(u1, (tile + 1) * a.nkb);
+      const int buf = seg & 1;
+      e.tile = tile;
+      bool ok = tc_wait(&accf_bar[buf], (seg >> 1) & 1, &abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok && lane == 0) {
+        abort_flag = 1;
+        set_error(a.err, MTP_ERR_TIMEOUT);
+      }
+      // the four epilogue warps take the same decision (named barriers follow)
+      epi_bar();
+      if (epi_tid == 0) stop_snap = abort_flag;
+      epi_bar();
+      if (stop_snap) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * NT);
+      const bool whole = (u == tile * a.nkb) && (ue == (tile + 1) * a.nkb);
+      if (whole) {
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+          tc_epilogue(a, e, c0, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce_bar[buf])) : "memory");
+      } else {
+        const int slot = 2 * blockIdx.x + ((tile == first_tile) ? 0 : 1);
+        float* fs = a.fix + (size_t)slot * NT * 128;
+        for (int c0 = 0; c0 < NT; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) fs[(size_t)(c0 + j) * 128 + m] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce_bar[buf])) : "memory");
+        __threadfence();
+        epi_bar();
+        const int cta_first = cta_of_unit((long long)tile * a.nkb, U, G);
+        const int cta_last = cta_of_unit((long long)(tile + 1) * a.nkb - 1, U, G);
+        if (epi_tid == 0) {
+          const int prev = atomicAdd(a.tile_cnt + tile, 1);
+          last_flag = (prev == cta_last - cta_first);
+        }
+        epi_bar();
+        if (last_flag) {
+          __threadfence();
+          for (int c0 = 0; c0 < NT; c0 += 16) {
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+            for (int cj = cta_first; cj <= cta_last; ++cj) {
+              const int first_tile_j = unit_begin(cj, U, G) / a.nkb;
+              const int sj = 2 * cj + ((tile == first_tile_j) ? 0 : 1);
+              const float* fj = a.fix + (size_t)sj * NT * 128;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(fj + (size_t)(c0 + j) * 128 + m);
+            }
+            tc_epilogue(a, e, c0, v);
+          }
+          if (epi_tid == 0) a.tile_cnt[tile] = 0;
+        }
+        epi_bar();
+      }
+      u = ue;
+    }
+    if (a.kind == TC_LM) {
+      epi_bar();
+      for (int b = epi_tid; b < a.B; b += kTcEpiThreads)
+        if (cta_best[b]) atomicMax(a.lm_keys + b, cta_best[b]);
+      __threadfence();
+      epi_bar();
+      if (epi_tid == 0) last_flag = (atomicAdd(a.lm_cnt, 1) == (int)gridDim.x - 1);
+      epi_bar();
+      if (last_flag) {
+        __threadfence();
+        for (int b = epi_tid; b < a.B; b += kTcEpiThreads) {
+          const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
+          a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
+          a.pending[b] = a.k;
+        }
+        if (epi_tid == 0) atomicExch(a.lm_cnt, 0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols));
+  }
+}
+
+// ------------------------------------------------------------ prep kernels
+
+// xin[b] = [bf16(RMSNorm(h_b) w_h), bf16(RMSNorm(e_b) w_e)], e_b = embeds_in (k == 1)
+// or the embedding row of the previous draft / chain token.
+struct PrepEhArgs {
+  int B, H, V, k, K;
+  const uint16_t* hidden_in;
+  const uint16_t* embeds_in;
+  const float* hid;
+  const int32_t* chain_ids;
+  const int32_t* draft_ids;
+  const uint16_t* embed;
+  const uint16_t* w_h;
+  const uint16_t* w_e;
+  float eps;
+  uint16_t* out;  // [B, 2H]
+  int* err;
+};
+
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+  v = warp_sum(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = ((threadIdx.x & 31) < 8) ? red[threadIdx.x & 31] : 0.0f;
+  return warp_sum(t);
+}
+
+__device__ __forceinline__ float bf(const uint16_t* p, int i) { return __uint_as_float(((uint32_t)p[i]) << 16); }
+
+__global__ void __launch_bounds__(256) prep_eh_kernel(const PrepEhArgs a) {
+  __shared__ float red[8];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  // hidden half: step 1 reads the caller's bf16 state, later steps the fp32 recursion
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < a.H; i += 256) {
+    const float v = (a.k == 1) ? bf(a.hidden_in + (size_t)b * a.H, i) : a.hid[(size_t)b * a.H + i];
+    ss += v * v;
+  }
+  float sc = rsqrtf(block_sum256(ss, red) / (float)a.H + a.eps);
+  for (int i = threadIdx.x; i < a.H; i += 256) {
+    const float v = (a.k == 1) ? bf(a.hidden_in + (size_t)b * a.H, i) : a.hid[(size_t)b * a.H + i];
+    a.out[(size_t)b * 2 * a.H + i] = f32_to_bf16_rne(v * sc * bf(a.w_h, i));
+  }
+  // embedding half
+  const uint16_t* e;
+  if (a.k == 1) {
+    e = a.embeds_in + (size_t)b * a.H;
+  } else {
+    int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+    if (id < 0 || id >= a.V) {
+      if (threadIdx.x == 0) set_error(a.err, MTP_ERR_DEVICE_ARGS);
+      id = 0;
+    }
+    e = a.embed + (size_t)id * a.H;
+  }
+  ss = 0.0f;
+  for (int i = threadIdx.x; i < a.H; i += 256) { const float v = bf(e, i); ss += v * v; }
+  sc = rsqrtf(block_sum256(ss, red) / (float)a.H + a.eps);
+  for (int i = threadIdx.x; i < a.H; i += 256)
+    a.out[(size_t)b * 2 * a.H + a.H + i] = f32_to_bf16_rne(bf(e, i) * sc * bf(a.w_e, i));
+}
+
+// out[b] = bf16(RMSNorm(src_b) w)
+__global__ void __launch_bounds__(256) prep_norm_kernel(const float* src, const uint16_t* w, uint16_t* out, int C,
+                                                        float eps) {
+  __shared__ float red[8];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const float* s = src + (size_t)b * C;
+  float ss = 0.0f;
+  for (int i = threadIdx.x; i < C; i += 256) ss += s[i] * s[i];
+  const float sc = rsqrtf(block_sum256(ss, red) / (float)C + eps);
+  for (int i = threadIdx.x; i < C; i += 256) out[(size_t)b * C + i] = f32_to_bf16_rne(s[i] * sc * bf(w, i));
+}
+
+// -------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static bool get_encode() {
+  if (g_encode) return true;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      !fn)
+    return false;
+  g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  return true;
+}
+
+// 2-D bf16 map over [rows, cols] with box [box_rows, 64] and 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_supported(const mtp_ctx* ctx, int B) {
+  const mtp_config& c = ctx->cfg;
+  return ctx->tc_ws != nullptr && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128 && B >= ctx->tc_min_batch &&
+         B <= 256 && c.hidden % 128 == 0 && c.ffn % 64 == 0 && ctx->q_dim % 64 == 0;
+}
+
+static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int k, int K, const int32_t* positions,
+                             const mtp_kv* kv, int32_t* draft_ids, float* logits, float* hidden_out) {
+  const mtp_config& c = ctx->cfg;
+  const int NT = ((B + 15) / 16) * 16;
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  const mtp_weights& w = ctx->w;
+  int C = 0, n_tiles = 0;
+  bool ok = true;
+  switch (kind) {
+    case TC_EH:
+      C = 2 * c.hidden; n_tiles = c.hidden / 128;
+      ok = make_map(&maps.a0, w.w_eh, c.hidden, C, 128) && make_map(&maps.b, ctx->tc_xin_eh, c.max_batch, C, NT);
+      break;
+    case TC_QKV:
+      C = c.hidden; n_tiles = c.n_q_heads + 2 * c.n_kv_heads;
+      ok = make_map(&maps.a0, w.w_q, ctx->q_dim, C, 128) && make_map(&maps.a1, w.w_k, ctx->kv_dim, C, 128) &&
+           make_map(&maps.a2, w.w_v, ctx->kv_dim, C, 128) && make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
+      break;
+    case TC_O:
+      C = ctx->q_dim; n_tiles = c.hidden / 128;
+      ok = make_map(&maps.a0, w.w_o, c.hidden, C, 128) && make_map(&maps.b, ctx->tc_attn, c.max_batch, C, NT);
+      break;
+    case TC_GU:
+      C = c.hidden; n_tiles = c.ffn / 64;
+      ok = make_map(&maps.a0, w.w_gate, c.ffn, C, 64) && make_map(&maps.a1, w.w_up, c.ffn, C, 64) &&
+           make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
+      break;
+    case TC_DOWN:
+      C = c.ffn; n_tiles = c.hidden / 128;
+      ok = make_map(&maps.a0, w.w_down, c.hidden, C, 128) && make_map(&maps.b, ctx->tc_act, c.max_batch, C, NT);
+      break;
+    default:
+      C = c.hidden; n_tiles = (c.vocab + 127) / 128;
+      ok = make_map(&maps.a0, w.lm_head, c.vocab, C, 128) && make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
+      break;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kind = kind; a.B = B; a.NT = NT; a.H = c.hidden; a.q_dim = ctx->q_dim; a.kv_dim = ctx->kv_dim; a.F = c.ffn;
+  a.V = c.vocab; a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.bs = c.block_size; a.k = k; a.K = K;
+  a.C = C; a.nkb = C / 64; a.n_tiles = n_tiles; a.max_pos = c.max_pos;
+  a.num_blocks = kv->num_blocks; a.max_blocks = kv->max_blocks;
+  a.positions = positions; a.draft_ids = draft_ids; a.logits = logits; a.hidden_out = hidden_out;
+  a.k_pool = (uint16_t*)kv->k_pool; a.v_pool = (uint16_t*)kv->v_pool; a.block_table = kv->block_table;
+  a.seq_len = kv->seq_len; a.pending = kv->pending;
+  a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.h1 = ctx->h1; a.act_bf16 = ctx->tc_act;
+  a.fix = ctx->tc_fix; a.tile_cnt = ctx->tc_tile_cnt; a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
+  a.err = ctx->err; a.rope = ctx->rope;
+  const int stage_bytes = kTcTileBytesA + NT * 128;
+  const int budget = 200 * 1024;
+  int stages = budget / stage_bytes;
+  if (stages > 8) stages = 8;
+  if (stages < 2) stages = 2;
+  a.stages = stages;
+  const size_t smem = 1024 + (size_t)stages * stage_bytes;
+  int grid = ctx->num_sms;
+  const long long U = (long long)n_tiles * a.nkb;
+  if (grid > U) grid = (int)U;
+  cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int kid = (kind == TC_EH) ? MTP_KERNEL_EH_PROJ : (kind == TC_QKV) ? MTP_KERNEL_QKV_ROPE
+                  : (kind == TC_O) ? MTP_KERNEL_O_PROJ : (kind == TC_GU) ? MTP_KERNEL_GATE_UP
+                  : (kind == TC_DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
+  prof_before(ctx, kid, s);
+  cudaError_t e = launch_pdl(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), smem, s, maps, a);
+  prof_after(ctx, kid, s);
+  ctx->launches++;
+  return e;
+}
+
+static cudaError_t prep_norm(mtp_ctx* ctx, cudaStream_t s, int B, const float* src, const void* w, int C) {
+  ctx->launches++;
+  return launch_pdl(prep_norm_kernel, dim3(B), dim3(256), 0, s, src, (const uint16_t*)w, ctx->tc_xn, C,
+                    ctx->cfg.eps);
+}
+
+cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
+                                 const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                                 const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out) {
+  const mtp_config& c = ctx->cfg;
+  cudaError_t e;
+  PrepEhArgs pa;
+  pa.B = B; pa.H = c.hidden; pa.V = c.vocab; pa.k = k; pa.K = K;
+  pa.hidden_in = (const uint16_t*)hidden; pa.embeds_in = (const uint16_t*)embeds; pa.hid = ctx->hid;
+  pa.chain_ids = chain_ids; pa.draft_ids = draft_ids; pa.embed = (const uint16_t*)ctx->w.embed;
+  pa.w_h = (const uint16_t*)ctx->w.w_norm_h; pa.w_e = (const uint16_t*)ctx->w.w_norm_e; pa.eps = c.eps;
+  pa.out = ctx->tc_xin_eh; pa.err = ctx->err;
+  ctx->launches++;
+  if ((e = launch_pdl(prep_eh_kernel, dim3(B), dim3(256), 0, s, pa)) != cudaSuccess) return e;
+  if ((e = tc_launch(ctx, s, TC_EH, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
+  if ((e = prep_norm(ctx, s, B, ctx->x, ctx->w.w_norm_in, c.hidden)) != cudaSuccess) return e;
+  if ((e = tc_launch(ctx, s, TC_QKV, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
+  if ((e = launch_attention(ctx, s, B, k, kv)) != cudaSuccess) return e;
+  if ((e = tc_launch(ctx, s, TC_O, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
+  if ((e = prep_norm(ctx, s, B, ctx->h1, ctx->w.w_norm_post, c.hidden)) != cudaSuccess) return e;
+  if ((e = tc_launch(ctx, s, TC_GU, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
+  if ((e = tc_launch(ctx, s, TC_DOWN, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
+  if ((e = prep_norm(ctx, s, B, ctx->hid, ctx->w.w_norm_f, c.hidden)) != cudaSuccess) return e;
+  return tc_launch(ctx, s, TC_LM, B, k, K, positions, kv, draft_ids, logits, hidden_out);
+}
+
+}  // namespace mtp

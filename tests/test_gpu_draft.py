@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 class Case:
-    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77):
+    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77, tc_min_batch=0):
         self.cfg = cfg
         self.K = K or cfg.K
         self.w = synth.make_weights(cfg, norm=norm)
@@ -30,7 +30,7 @@ class Case:
         self.chain = synth.uniform_int(cfg.seed, chain_stream, (self.B, max(self.K - 1, 1)), 0, cfg.vocab)
         self.wdev = upload_weights(self.w)
         self.ctx = make_context(cfg, self.wdev, max_batch=self.B, max_k=self.K,
-                                max_pos=int(self.lens.max()) + self.K + 8)
+                                max_pos=int(self.lens.max()) + self.K + 8, tc_min_batch=tc_min_batch)
         self.inputs = (dev(self.di.hidden), dev(self.di.embeds), dev(self.di.positions))
 
     def gpu_draft(self, forced=True, kvd=None):
@@ -134,14 +134,30 @@ def test_tiny_f32_head_parity_and_invariants():
         np.testing.assert_array_equal(getattr(got, f), getattr(case.kv0, f), err_msg=f)
 
 
-def test_ragged_bf16_block_edges():
+@pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
+def test_ragged_bf16_block_edges(path):
     """bf16, G=4 heads per kv head, d=128, odd vocab; contexts 0, 1, 15, 16,
-    17, 33 and 100 tokens (block boundaries, an empty cache)."""
+    17, 33 and 100 tokens (block boundaries, an empty cache).  Run on both
+    the small-batch CUDA-core kernels and the tcgen05 path (forced for B=7)."""
     cfg = synth.MTPShape("ragged_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=7, K=4,
                          dtype="bf16", ctx_lo=0, ctx_hi=100, paged_shuffle=True, seed_index=50)
-    case = Case(cfg, norm="random", lens=[0, 1, 15, 16, 17, 33, 100])
+    case = Case(cfg, norm="random", lens=[0, 1, 15, 16, 17, 33, 100],
+                tc_min_batch=1 if path == "tensor_cores" else 0)
     _, _, ids, logits = check_forced(case, list(range(7)), LOGIT_TOL)
     check_free(case, list(range(7)), ids, logits, LOGIT_TOL)
+
+
+def test_tensor_core_path_batch_40_gqa8():
+    """tcgen05 path with N = 48 (40 requests padded), 8 q heads per kv head,
+    a vocabulary that ends mid-tile, and more tiles than SMs in the LM head."""
+    cfg = synth.MTPShape("tc_b40", H=768, n_q=16, n_kv=2, head_dim=128, ffn=2048, vocab=40000, batch=40, K=3,
+                         dtype="bf16", ctx_lo=1, ctx_hi=300, paged_shuffle=True, seed_index=52)
+    case = Case(cfg, norm="random")
+    _, _, ids, logits = check_forced(case, list(range(40)), LOGIT_TOL)
+    check_free(case, [0, 13, 39], ids, logits, LOGIT_TOL)
+    ids2, logits2, _, _ = case.gpu_draft(forced=True)
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_array_equal(logits2, logits)
 
 
 def test_gqa_eight_heads_per_kv_head_f32():
