@@ -104,6 +104,99 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
+// Merge the per-warp online-softmax states of this CTA, then either write the
+// output (one split) or a partial (M, L, O) and, in the last CTA of the
+// (request, kv head), combine all splits.  The combine stages each split's
+// (M, L) in shared memory, turns them into weights in parallel, and sums the
+// partial outputs with independent loads.
+template <typename T, int HD, int G>
+__device__ __forceinline__ void attn_store_out(const AttnArgs<T>& a, int b, int g, int h, int d, float v) {
+  const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
+  a.out[oi] = v;
+  if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(v);
+}
+
+constexpr int kMaxSplits = 64;
+
+template <typename T, int HD, int G>
+__device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, float (*wm)[G], float (*wl)[G], int s,
+                                   int g, int b, int nsplit) {
+  __shared__ float cm[G][kMaxSplits], cw[G][kMaxSplits];
+  __shared__ int am_last;
+  float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * (HD + 2);
+  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+    const int h = idx / HD, d = idx - h * HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w][h]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float f = (wm[w][h] == -INFINITY) ? 0.0f : exp2f(wm[w][h] - M);
+      L += wl[w][h] * f;
+      O += wacc[((size_t)w * G + h) * HD + d] * f;
+    }
+    if (nsplit == 1) {
+      attn_store_out<T, HD, G>(a, b, g, h, d, O / L);
+    } else {
+      float* pp = part_base + ((size_t)h * a.max_splits + s) * (HD + 2);
+      if (d == 0) { pp[0] = M; pp[1] = L; }
+      pp[2 + d] = O;
+    }
+  }
+  if (nsplit == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) am_last = (atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1) == nsplit - 1);
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < G * nsplit; i += kAttnThreads) {
+    const int h = i / nsplit, j = i - h * nsplit;
+    const float* pj = part_base + ((size_t)h * a.max_splits + j) * (HD + 2);
+    cm[h][j] = __ldcg(pj);
+    cw[h][j] = __ldcg(pj + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = -INFINITY;
+    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, cm[h][j]);
+    float L = 0.0f;
+    for (int j = 0; j < nsplit; ++j) L += cw[h][j] * exp2f(cm[h][j] - M);
+    const float inv = 1.0f / L;
+    for (int j = 0; j < nsplit; ++j) cw[h][j] = exp2f(cm[h][j] - M) * inv;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+    const int h = idx / HD, d = idx - h * HD;
+    const float* ph = part_base + (size_t)h * a.max_splits * (HD + 2) + 2 + d;
+    float O = 0.0f;
+#pragma unroll 8
+    for (int j = 0; j < nsplit; ++j) O = fmaf(cw[h][j], __ldcg(ph + (size_t)j * (HD + 2)), O);
+    attn_store_out<T, HD, G>(a, b, g, h, d, O);
+  }
+  if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
+}
+
+template <typename T, int HD, int G, int DPL>
+__device__ __forceinline__ void attn_finish(const AttnArgs<T>& a, unsigned char* smem_raw, float (*wm)[G],
+                                            float (*wl)[G], const float (&m)[G], const float (&l)[G],
+                                            const float (&acc)[G][DPL], int warp, int lane, int s, int g, int b,
+                                            int nsplit) {
+  float* wacc = reinterpret_cast<float*>(smem_raw);  // reuse stages: [warps][G][HD]
+  __syncthreads();
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) { wm[warp][h] = m[h]; wl[warp][h] = l[h]; }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) wacc[((size_t)warp * G + h) * HD + lane * DPL + j] = acc[h][j];
+  __syncthreads();
+  attn_finish_merged<T, HD, G>(a, wacc, wm, wl, s, g, b, nsplit);
+}
+
 template <typename T, int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T> a) {
   constexpr int DPL = HD / 32;
@@ -114,7 +207,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
   T* stage_base = reinterpret_cast<T*>(smem_raw);    // [warps][stages][2][TILE]
   __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
-  __shared__ int am_last;
 
   pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -252,69 +344,232 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
       mbar_wait_bounded(&bars[warp][it % kStages], (uint32_t)((it / kStages) & 1), kWaitLimit);
   }
 
-  // merge warps
-  float* wacc = reinterpret_cast<float*>(smem_raw);  // reuse stages: [warps][G][HD]
+  attn_finish<T, HD, G, DPL>(a, smem_raw, wm, wl, m, l, acc, warp, lane, s, g, b, nsplit);
+}
+
+// ------------------------------------------------ tensor-core attention
+//
+// bf16 cache, head_dim 128.  Same split-KV grid and per-warp block ownership
+// as above, but the arithmetic runs on mma.sync m16n8k16 (bf16 in, fp32
+// accumulate) with the G query heads of the group on the M dimension (rows
+// G..15 are zero padding):
+//   S^T[16 x 16 tokens] = Q[16 x 128] . K^T   -- 2 n-tiles x 8 k-steps
+//   O[16 x 128]        += P[16 x 16] . V      -- 16 n-tiles, k = 16 tokens
+// K and V tiles are staged by 2-D tensor-map loads with 128-byte swizzle (two
+// 64-dim halves per tile), so the ldmatrix reads of 8 token rows hit distinct
+// banks.  The S accumulators of the two token n-tiles are exactly the A
+// fragment of P, so P never leaves registers.
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return (uint32_t)f32_to_bf16_rne(lo) | ((uint32_t)f32_to_bf16_rne(hi) << 16);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Shared-memory address of 16-byte chunk c (0..15 over 128 dims) of token row
+// `row` (0..15) in a tile stored as two 2 KB swizzled halves.
+__device__ __forceinline__ uint32_t sw_chunk(uint32_t tile, int row, int c) {
+  return tile + (uint32_t)((c >> 3) * 2048 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_addr(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+template <int G>
+__global__ void __launch_bounds__(kAttnThreads, 2)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                    const AttnArgs<uint16_t> a) {
+  constexpr int HD = 128;
+  constexpr uint32_t TILE_BYTES = 16 * HD * 2;  // 4 KB per K or V tile
+  extern __shared__ __align__(1024) unsigned char smem_raw_in[];
+  unsigned char* smem_raw = (unsigned char*)(((uintptr_t)smem_raw_in + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
+  __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
+
+  pdl_trigger();
+  const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, ti = lane & 3;
+  if (threadIdx.x < kAttnWarps * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
+  fence_mbar_init();
   __syncthreads();
+  pdl_wait();
+
+  const int T_len = a.seq_len[b] + a.k;
+  const int nblk = (T_len + 15) >> 4;
+  const int blk0 = s * a.bps;
+  if (blk0 >= nblk || T_len <= 0) return;
+  const int blk1 = min(nblk, blk0 + a.bps);
+  const int nsplit = (nblk + a.bps - 1) / a.bps;
+
+  // Q fragments (A operand): row gi = head gi of the group; rows >= G and
+  // rows 8..15 are zero.  Scaled for base-2 softmax.
+  uint32_t qa[8][4];
+  {
+    const float* qh = a.q + (size_t)b * a.n_q * HD + (size_t)(g * G + gi) * HD;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      if (gi < G) {
+        qa[kk][0] = pack_bf16(qh[16 * kk + 2 * ti] * a.qscale, qh[16 * kk + 2 * ti + 1] * a.qscale);
+        qa[kk][2] = pack_bf16(qh[16 * kk + 8 + 2 * ti] * a.qscale, qh[16 * kk + 8 + 2 * ti + 1] * a.qscale);
+      } else {
+        qa[kk][0] = qa[kk][2] = 0u;
+      }
+      qa[kk][1] = qa[kk][3] = 0u;
+    }
+  }
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
+
+  unsigned char* my_stage = smem_raw + (size_t)warp * kStages * 2 * TILE_BYTES;
+  auto tile_row = [&](int bi) -> int {
+    int blk = (bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    if (blk < 0 || blk >= a.num_blocks) {
+      set_error(a.err, MTP_ERR_CAPACITY);
+      blk = 0;
+    }
+    return (blk * a.n_kv + g) * 16;
+  };
+  auto issue = [&](int it, int bi) {
+    const int st = it % kStages;
+    unsigned char* dst = my_stage + (size_t)st * 2 * TILE_BYTES;
+    const int row = tile_row(bi);
+    mbar_expect_tx(&bars[warp][st], 2 * TILE_BYTES);
+    tma_2d(dst, &kmap, 0, row, &bars[warp][st]);
+    tma_2d(dst + 2048, &kmap, 64, row, &bars[warp][st]);
+    tma_2d(dst + TILE_BYTES, &vmap, 0, row, &bars[warp][st]);
+    tma_2d(dst + TILE_BYTES + 2048, &vmap, 64, row, &bars[warp][st]);
+  };
+  const int first = blk0 + warp;
+  const int count = (first < blk1) ? (blk1 - first + kAttnWarps - 1) / kAttnWarps : 0;
   if (lane == 0)
-#pragma unroll
-    for (int h = 0; h < G; ++h) { wm[warp][h] = m[h]; wl[warp][h] = l[h]; }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) wacc[((size_t)warp * G + h) * HD + lane * DPL + j] = acc[h][j];
-  __syncthreads();
+    for (int it = 0; it < count && it < kStages; ++it) issue(it, first + it * kAttnWarps);
+  __syncwarp();
 
-  float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * (HD + 2);
-  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
-    const int h = idx / HD, d = idx - h * HD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w][h]);
-    float L = 0.0f, O = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float f = (wm[w][h] == -INFINITY) ? 0.0f : exp2f(wm[w][h] - M);
-      L += wl[w][h] * f;
-      O += wacc[((size_t)w * G + h) * HD + d] * f;
+  int stop_at = -1;
+  for (int it = 0; it < count; ++it) {
+    const int st = it % kStages;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], (uint32_t)((it / kStages) & 1),
+                                                              kWaitLimit));
+    if (!ok) {
+      stop_at = it;
+      break;
     }
-    if (nsplit == 1) {
-      const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
-      a.out[oi] = O / L;
-      if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(O / L);
-    } else {
-      float* pp = part_base + ((size_t)h * a.max_splits + s) * (HD + 2);
-      if (d == 0) { pp[0] = M; pp[1] = L; }
-      pp[2 + d] = O;
-    }
-  }
-  if (nsplit == 1) return;
+    const uint32_t kt = smem_addr(my_stage + (size_t)st * 2 * TILE_BYTES);
+    const uint32_t vt = kt + TILE_BYTES;
+    const int tok0 = (first + it * kAttnWarps) * 16;
 
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int prev = atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1);
-    am_last = (prev == nsplit - 1);
-  }
-  __syncthreads();
-  if (!am_last) return;
-  __threadfence();
-  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
-    const int h = idx / HD, d = idx - h * HD;
-    const float* ph = part_base + (size_t)h * a.max_splits * (HD + 2);
-    float M = -INFINITY;
-    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, __ldcg(ph + (size_t)j * (HD + 2)));
-    float L = 0.0f, O = 0.0f;
-    for (int j = 0; j < nsplit; ++j) {
-      const float* pj = ph + (size_t)j * (HD + 2);
-      const float f = exp2f(__ldcg(pj) - M);
-      L += __ldcg(pj + 1) * f;
-      O += __ldcg(pj + 2 + d) * f;
+    // S^T = Q K^T: n-tile j covers tokens 8j..8j+7
+    float sc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < 8; kk += 2) {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int c = 2 * (kk + (mi >> 1)) + (mi & 1);
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(sw_chunk(kt, 8 * j + ri, c), r0, r1, r2, r3);
+        mma_bf16(sc[j], qa[kk], r0, r1);
+        mma_bf16(sc[j], qa[kk + 1], r2, r3);
+      }
     }
-    const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
-    a.out[oi] = O / L;
-    if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(O / L);
+    // online softmax on row gi (tokens 2ti, 2ti+1 of each n-tile); rows 8..15 are padding
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = tok0 + 8 * j + 2 * ti + e;
+        if (tok >= T_len) sc[j][e] = -INFINITY;
+        mx = fmaxf(mx, sc[j][e]);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new);
+    float p[2][2], rs = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        p[j][e] = (sc[j][e] == -INFINITY) ? 0.0f : exp2f(sc[j][e] - m_new);
+        rs += p[j][e];
+      }
+    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+    l_run = l_run * corr + rs;
+    m_run = m_new;
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      o[n][0] *= corr;
+      o[n][1] *= corr;
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(p[0][0], p[0][1]);
+    pa[1] = 0u;
+    pa[2] = pack_bf16(p[1][0], p[1][1]);
+    pa[3] = 0u;
+    // O += P V: n-tile n covers dims 8n..8n+7
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const int mi = lane >> 3, ri = lane & 7;
+      const int tok = 8 * (mi & 1) + ri;
+      uint32_t r0, r1, r2, r3;
+      ldsm_x4_t(sw_chunk(vt, tok, c + (mi >> 1)), r0, r1, r2, r3);
+      mma_bf16(o[c], pa, r0, r1);
+      mma_bf16(o[c + 1], pa, r2, r3);
+    }
+    __syncwarp();
+    if (lane == 0 && it + kStages < count) issue(it + kStages, first + (it + kStages) * kAttnWarps);
+    __syncwarp();
   }
-  if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
+  if (stop_at >= 0) {
+    if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+    for (int it = stop_at; it < count && it < stop_at + kStages; ++it)
+      mbar_wait_bounded(&bars[warp][it % kStages], (uint32_t)((it / kStages) & 1), kWaitLimit);
+  }
+
+  // per-warp state -> shared memory, then the common merge/combine
+  float* wacc = reinterpret_cast<float*>(smem_raw);  // [warps][G][HD]
+  __syncthreads();
+  if (gi < G && ti == 0) {
+    wm[warp][gi] = m_run;
+    wl[warp][gi] = l_run;
+  }
+  if (gi < G) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      wacc[((size_t)warp * G + gi) * HD + 8 * n + 2 * ti] = o[n][0];
+      wacc[((size_t)warp * G + gi) * HD + 8 * n + 2 * ti + 1] = o[n][1];
+    }
+  }
+  __syncthreads();
+  attn_finish_merged<uint16_t, HD, G>(a, wacc, wm, wl, s, g, b, nsplit);
 }
 
 template <typename T, int HD, int G>
@@ -329,13 +584,13 @@ static cudaError_t attn_launch(mtp_ctx* ctx, cudaStream_t s, const AttnArgs<T>& 
 
 // Blocks per split for a batch of B requests and max_blocks capacity:
 // aim for about two CTAs per SM, never more than max_splits splits.
-static int attn_bps(const mtp_ctx* ctx, int B, int max_blocks) {
+static int attn_bps(const mtp_ctx* ctx, int B, int max_blocks, int min_bps) {
   const long long pairs = (long long)B * ctx->cfg.n_kv_heads;
   long long splits = (ctx->attn_target_ctas + pairs - 1) / pairs;
   if (splits < 1) splits = 1;
   if (splits > ctx->attn_max_splits) splits = ctx->attn_max_splits;
   int bps = (int)((max_blocks + splits - 1) / splits);
-  if (bps < 2) bps = 2;
+  if (bps < min_bps) bps = min_bps;
   while ((max_blocks + bps - 1) / bps > ctx->attn_max_splits) ++bps;
   return bps;
 }
@@ -348,12 +603,35 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
   a.k_pool = (const T*)kv->k_pool; a.v_pool = (const T*)kv->v_pool;
   a.block_table = kv->block_table; a.seq_len = kv->seq_len; a.k = k;
   a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.max_blocks = kv->max_blocks; a.num_blocks = kv->num_blocks;
-  a.bps = attn_bps(ctx, B, kv->max_blocks);
+  const int G = c.n_q_heads / c.n_kv_heads;
+  const int HD = c.head_dim;
+  const bool use_mma = sizeof(T) == 2 && HD == 128;
+  // the tensor-core kernel keeps at least 4 blocks per warp to amortise its
+  // set-up and the split combine
+  a.bps = attn_bps(ctx, B, kv->max_blocks, use_mma ? 16 : 2);
   const int splits = (kv->max_blocks + a.bps - 1) / a.bps;
   a.max_splits = splits;  // partial-buffer stride of this call
   a.qscale = 1.4426950408889634f / sqrtf((float)c.head_dim);
-  const int G = c.n_q_heads / c.n_kv_heads;
-  const int HD = c.head_dim;
+  if (use_mma) {
+    CUtensorMap km, vm;
+    const uint64_t rows = (uint64_t)kv->num_blocks * c.n_kv_heads * 16;
+    if (!make_map(&km, kv->k_pool, rows, 128, 16) || !make_map(&vm, kv->v_pool, rows, 128, 16))
+      return cudaErrorInvalidValue;
+    const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
+    const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096;
+    dim3 grid(splits, c.n_kv_heads, B);
+    switch (G) {
+      case 1: cudaFuncSetAttribute(attn_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+              return launch_pdl(attn_mma_kernel<1>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
+      case 2: cudaFuncSetAttribute(attn_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+              return launch_pdl(attn_mma_kernel<2>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
+      case 4: cudaFuncSetAttribute(attn_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+              return launch_pdl(attn_mma_kernel<4>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
+      case 8: cudaFuncSetAttribute(attn_mma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+              return launch_pdl(attn_mma_kernel<8>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (HD == 128) {
     switch (G) {
       case 1: return attn_launch<T, 128, 1>(ctx, s, a, B, splits);

@@ -2,6 +2,7 @@
 // library.  sm_103a only.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -241,6 +242,9 @@ cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K,
                               const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
 cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv);
 bool tc_supported(const mtp_ctx* ctx, int B);
+// 2-D bf16 tensor map over [rows, cols] (row-major) with a [box_rows, 64]
+// box and 128-byte swizzle; false if the driver rejects it.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
 cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
                                  const void* embeds, const int32_t* positions, const mtp_kv* kv,
                                  const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);

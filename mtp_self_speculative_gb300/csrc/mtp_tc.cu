@@ -603,7 +603,7 @@ static bool get_encode() {
 }
 
 // 2-D bf16 map over [rows, cols] with box [box_rows, 64] and 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   if (!get_encode()) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
