@@ -111,6 +111,54 @@ def step_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool 
             "weights": w}
 
 
+def kernel_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True) -> dict:
+    """Algorithmic bytes of one launch of each kernel (draft kernels: one
+    draft step, attention averaged over k = 1..K)."""
+    e = cfg.elem_bytes
+    B = len(lens)
+    H, F, V, qd, kvd = cfg.H, cfg.ffn, cfg.vocab, cfg.q_dim, cfg.kv_dim
+    kv_row = 2 * kvd * e
+    mean_ctx = float(np.sum(lens)) + B * (K + 1) / 2.0
+    return {
+        "eh_proj": H * 2 * H * e + 2 * H * e + B * 2 * H * e + B * H * 4,
+        "qkv_rope": (qd + 2 * kvd) * H * e + H * e + B * H * 4 + B * (qd * 4 + kv_row),
+        "attention": mean_ctx * kv_row + B * qd * 8,
+        "o_proj": H * qd * e + B * (qd + 2 * H) * 4,
+        "gate_up": 2 * F * H * e + H * e + B * (H * 4 + F * 4),
+        "down": H * F * e + B * (F * 4 + 2 * H * 4),
+        "lm_head": V * H * e + H * e + B * H * 4 + (B * V * 4 if with_logits else 0),
+        "verify": B * (K + 1) * V * e,
+    }
+
+
+def kernel_breakdown(wl, steps: int) -> dict:
+    """Mean live duration of each kernel (CUDA events around its launches,
+    one kernel id at a time) and its bandwidth against its algorithmic
+    bytes.  Events break the programmatic overlap at the timed kernel's
+    boundaries, so these are per-kernel, not additive, figures."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    kb = kernel_bytes(wl.cfg, wl.lens, wl.K)
+    peak = float(measured_peaks()[0]["hbm_gbs"])
+    out = {}
+    for kid, name in enumerate(M.KERNEL_NAMES):
+        per_step = wl.K if kid <= M.MTP_KERNEL_LM_HEAD else (2 if kid == M.MTP_KERNEL_KV_EDIT else 1)
+        M.mtp_profile_begin(wl.ctx, kid, steps * per_step)
+        for _ in range(steps):
+            wl.step()
+        torch.cuda.synchronize()
+        ms = M.mtp_profile_end(wl.ctx, steps * per_step)
+        if not ms:
+            continue
+        us = 1e3 * statistics.mean(ms)
+        entry = {"us": round(us, 2), "launches": len(ms)}
+        if name in kb:
+            gbs = kb[name] / (us * 1e-6) / 1e9
+            entry.update({"bytes": int(kb[name]), "gbs": round(gbs, 1), "frac": round(gbs / peak, 3)})
+        out[name] = entry
+    return out
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -319,6 +367,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     draft_ms = t0.elapsed_time(t1) / nd
 
+    kernels = kernel_breakdown(wl, 20)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -365,6 +415,7 @@ def run_ours(args, rank, world, local_rank):
                      "unit": "GB/s", "frac": lm_gbs / peak, "peak_source": peak_kind + " hbm_gbs",
                      "traffic": args.lm_traffic, "launches_timed": len(lm_ms),
                      "bytes_per_launch": sb["lm_head_launch"]},
+        "kernels": kernels,
         "stream_copy_gbs": copy_gbs,
         "gpu_launches": int(launches),
         "deterministic_ids": deterministic,
