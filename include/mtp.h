@@ -75,7 +75,7 @@ typedef struct {
   int tc_min_batch;      /* batches of at least this many requests use the
                             tensor-core (tcgen05) path when the shape allows
                             it (bf16, head_dim 128, H % 128 == 0, F and
-                            n_q*head_dim % 64 == 0, B <= 256); 0 = 16      */
+                            n_q*head_dim % 64 == 0, B <= 256); 0 = 5       */
 } mtp_config;
 
 /* Borrowed head weights (device pointers, layouts [out, in] row-major).

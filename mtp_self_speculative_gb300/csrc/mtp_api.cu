@@ -153,7 +153,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     return MTP_ERR_CUDA;
   }
   // tensor-core path workspace
-  ctx->tc_min_batch = c.tc_min_batch > 0 ? c.tc_min_batch : 16;
+  ctx->tc_min_batch = c.tc_min_batch > 0 ? c.tc_min_batch : 5;
   if (with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128 && c.hidden % 128 == 0 && c.ffn % 64 == 0 &&
       ctx->q_dim % 64 == 0 && c.max_batch >= ctx->tc_min_batch) {
     const size_t mb = (size_t)c.max_batch;

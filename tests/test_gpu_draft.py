@@ -138,13 +138,25 @@ def test_tiny_f32_head_parity_and_invariants():
 def test_ragged_bf16_block_edges(path):
     """bf16, G=4 heads per kv head, d=128, odd vocab; contexts 0, 1, 15, 16,
     17, 33 and 100 tokens (block boundaries, an empty cache).  Run on both
-    the small-batch CUDA-core kernels and the tcgen05 path (forced for B=7)."""
+    the register-streaming CUDA-core kernels (B=7 in two groups of at most 4)
+    and the tcgen05 path."""
     cfg = synth.MTPShape("ragged_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=7, K=4,
                          dtype="bf16", ctx_lo=0, ctx_hi=100, paged_shuffle=True, seed_index=50)
     case = Case(cfg, norm="random", lens=[0, 1, 15, 16, 17, 33, 100],
-                tc_min_batch=1 if path == "tensor_cores" else 0)
+                tc_min_batch=1 if path == "tensor_cores" else 1 << 20)
     _, _, ids, logits = check_forced(case, list(range(7)), LOGIT_TOL)
     check_free(case, list(range(7)), ids, logits, LOGIT_TOL)
+
+
+@pytest.mark.parametrize("lens", [[33], [0, 17], [5, 16, 40]])
+def test_small_batch_bf16_tma_streamed(lens):
+    """bf16 batches of 1..3: the TMA-streamed CUDA-core kernels (1, 2 and 4
+    batch rows per pass)."""
+    cfg = synth.MTPShape("small_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=len(lens), K=3,
+                         dtype="bf16", ctx_lo=0, ctx_hi=64, paged_shuffle=True, seed_index=53)
+    case = Case(cfg, norm="random", lens=lens)
+    _, _, ids, logits = check_forced(case, list(range(len(lens))), LOGIT_TOL)
+    check_free(case, list(range(len(lens))), ids, logits, LOGIT_TOL)
 
 
 def test_tensor_core_path_batch_40_gqa8():
