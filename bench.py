@@ -331,8 +331,6 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     assert M.mtp_get_device_error(wl.ctx) == 0
 
-    lm_cap = args.steps * K
-    M.mtp_profile_begin(wl.ctx, M.MTP_KERNEL_LM_HEAD, lm_cap)
     launches0 = M.mtp_launch_count(wl.ctx)
     sampler = ClockSampler(gpu_id_for_smi(local_rank)) if rank == 0 else None
     if sampler:
@@ -348,8 +346,17 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     clocks = sampler.stop() if sampler else None
     launches = M.mtp_launch_count(wl.ctx) - launches0
-    lm_ms = M.mtp_profile_end(wl.ctx, lm_cap)
     elapsed_ms = t0.elapsed_time(t1)
+    # Roofline kernel: CUDA events around every LM-head launch, recorded by
+    # the library on its stream, over a second pass of the same steps (event
+    # records between kernels cancel the programmatic overlap, so they stay
+    # out of the timed region above).
+    lm_steps = min(args.steps, 400)
+    M.mtp_profile_begin(wl.ctx, M.MTP_KERNEL_LM_HEAD, lm_steps * K)
+    for _ in range(lm_steps):
+        wl.step()
+    torch.cuda.synchronize()
+    lm_ms = M.mtp_profile_end(wl.ctx, lm_steps * K)
     assert M.mtp_get_device_error(wl.ctx) == 0
     ids_now = wl.ids.cpu().numpy()
     deterministic = bool(np.array_equal(ids_now, wl.ids0))

@@ -83,6 +83,11 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     if (!ctx->w.lm_head) ctx->w.lm_head = ctx->w.embed;
   }
   ctx->prof_kernel = -1;
+  // Which small-batch projection kinds use the bulk-copy streamed kernel
+  // (bit = kind: eh, qkv, o, gate_up, down, lm_head); MTP_GEMV_STREAM
+  // overrides the default for tuning.
+  ctx->gemv_stream_mask = 0x3F;
+  if (const char* env = getenv("MTP_GEMV_STREAM")) ctx->gemv_stream_mask = (int)strtol(env, nullptr, 0);
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
     free(ctx);
@@ -313,6 +318,11 @@ mtp_status mtp_profile_begin(mtp_ctx* ctx, int kernel, int capacity) {
 mtp_status mtp_profile_end(mtp_ctx* ctx, float* ms_out, int max_out, int* n_out) {
   if (!ctx || !n_out || (max_out > 0 && !ms_out)) return MTP_ERR_INVALID;
   ctx->prof_kernel = -1;
+  // Which small-batch projection kinds use the bulk-copy streamed kernel
+  // (bit = kind: eh, qkv, o, gate_up, down, lm_head); MTP_GEMV_STREAM
+  // overrides the default for tuning.
+  ctx->gemv_stream_mask = 0x3F;
+  if (const char* env = getenv("MTP_GEMV_STREAM")) ctx->gemv_stream_mask = (int)strtol(env, nullptr, 0);
   const int n = ctx->prof_n;
   *n_out = 0;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;

@@ -212,6 +212,9 @@ struct mtp_ctx {
   int prof_n;
   cudaEvent_t* prof_ev;  // 2 * prof_cap
   long long launches;
+  // small-batch projections: bit k set = kernel kind k streams its weights
+  // through shared memory with bulk copies (else register streaming)
+  int gemv_stream_mask;
 };
 
 namespace mtp {

@@ -375,6 +375,229 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
   }
 }
 
+// ------------------------------------------------- TMA-streamed variant
+//
+// Same work split and epilogues as gemv_kernel, for batches of at most 4:
+// one CTA per SM; warp 0 is a producer that streams this CTA's row pairs
+// into a ring of shared-memory stages with one-dimensional bulk (TMA) copies
+// (one copy per contiguous pair, two for rotary or gate/up pairs), completing
+// on per-stage mbarriers; it starts before the dependency wait, so the ring
+// (about 200 KB per SM) fills while the previous kernel drains.  Warps 1..8
+// stage the normalised input, then consume pairs round-robin from shared
+// memory and release each stage as soon as its values are in registers.
+// The stage count is a multiple of the number of consuming warps, and pair
+// it goes to stage it % stages and warp it % consumers (see below).
+
+constexpr int kTmaConsumers = 8;
+constexpr int kTmaThreads = 32 * (kTmaConsumers + 1);
+constexpr int kMaxTmaStages = 16;
+constexpr uint32_t kGemvWaitLimit = 1u << 24;
+
+__device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ float cons_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int cw = (threadIdx.x >> 5) - 1, l = threadIdx.x & 31;
+  cons_bar();
+  if (l == 0) red[cw] = v;
+  cons_bar();
+  return warp_sum((l < kTmaConsumers) ? red[l] : 0.0f);
+}
+
+template <typename T, typename S>
+__device__ __forceinline__ void cons_stage_row(float* dst, const S* src, int n, const T* w, float eps, float* red) {
+  const int ct = threadIdx.x - 32;
+  float ss = 0.0f;
+  for (int i = ct; i < n; i += 256) {
+    float v;
+    if constexpr (sizeof(S) == 4) v = src[i];
+    else v = Elem<T>::load1(reinterpret_cast<const T*>(src) + i);
+    dst[i] = v;
+    ss = fmaf(v, v, ss);
+  }
+  if (w == nullptr) return;
+  const float scale = rsqrtf(cons_sum(ss, red) / (float)n + eps);
+  for (int i = ct; i < n; i += 256) dst[i] = dst[i] * scale * Elem<T>::load1(w + i);
+}
+
+template <typename T, int KIND>
+__device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
+  for (int b = 0; b < nb; ++b) {
+    float* dst = xs + (size_t)b * C;
+    if constexpr (KIND == EH_PROJ) {
+      if (a.k == 1) {
+        cons_stage_row<T, T>(dst, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h, a.eps, red);
+        cons_stage_row<T, T>(dst + a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e, a.eps, red);
+      } else {
+        cons_stage_row<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_h, a.eps, red);
+        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
+                             : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+        if (id < 0 || id >= a.V) {
+          if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
+          id = 0;
+        }
+        cons_stage_row<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e, a.eps, red);
+      }
+    } else if constexpr (KIND == QKV_ROPE) {
+      cons_stage_row<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in, a.eps, red);
+    } else if constexpr (KIND == O_PROJ) {
+      cons_stage_row<T, float>(dst, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr, a.eps, red);
+    } else if constexpr (KIND == GATE_UP) {
+      cons_stage_row<T, float>(dst, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post, a.eps, red);
+    } else if constexpr (KIND == DOWN) {
+      cons_stage_row<T, float>(dst, a.act + (size_t)b * a.F, a.F, (const T*)nullptr, a.eps, red);
+    } else {
+      cons_stage_row<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_f, a.eps, red);
+    }
+  }
+  cons_bar();
+}
+
+template <typename T, int KIND, int NB>
+__global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs<T> a, int stages, int consumers) {
+  extern __shared__ __align__(128) unsigned char gsm[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxTmaStages], empty_bar[kMaxTmaStages];
+  __shared__ float red[kTmaConsumers];
+  __shared__ unsigned long long cta_best[kTmaConsumers][NB];
+  __shared__ int am_last;
+
+  pdl_trigger();
+  const int C = gemv_cols(a, KIND);
+  const int P = gemv_pairs(a, KIND);
+  const int G = gridDim.x;
+  const int p_begin = (int)(((long long)blockIdx.x * P) / G);
+  const int p_end = (int)(((long long)(blockIdx.x + 1) * P) / G);
+  const int n = p_end - p_begin;
+  const uint32_t row_bytes = (uint32_t)C * sizeof(T);
+  const uint32_t stage_stride = (2 * row_bytes + 127) & ~127u;
+  float* xs = reinterpret_cast<float*>(gsm + (size_t)stages * stage_stride);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int VPE = Elem<T>::kPerVec;
+  const int nvec = C / VPE;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int it = 0; it < n; ++it) {
+        const int s = it % stages;
+        if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)(((it / stages) & 1) ^ 1), kGemvWaitLimit)) {
+          set_error(a.err, MTP_ERR_TIMEOUT);
+          break;
+        }
+        int r0, r1;
+        const T *w0, *w1;
+        pair_rows<T, KIND>(a, p_begin + it, C, r0, r1, w0, w1);
+        unsigned char* st = gsm + (size_t)s * stage_stride;
+        if (w1 == w0 + C) {
+          mbar_expect_tx(&full_bar[s], 2 * row_bytes);
+          bulk_g2s(st, w0, 2 * row_bytes, &full_bar[s]);
+        } else if (w1) {
+          mbar_expect_tx(&full_bar[s], 2 * row_bytes);
+          bulk_g2s(st, w0, row_bytes, &full_bar[s]);
+          bulk_g2s(st + row_bytes, w1, row_bytes, &full_bar[s]);
+        } else {
+          mbar_expect_tx(&full_bar[s], row_bytes);
+          bulk_g2s(st, w0, row_bytes, &full_bar[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // consumers
+  pdl_wait();
+  const int nb = a.B;  // launched only for B <= NB
+  cons_stage_inputs<T, KIND>(a, xs, C, nb, red);
+  const int cw = warp - 1;
+  // Full-barrier waits are by phase parity, so a warp may wait on a stage
+  // only after the stage's previous fill has landed.  `stages` is a multiple
+  // of the number of consuming warps A: pair it uses stage it % stages and
+  // warp it % A, so consecutive uses of a stage belong to the same warp,
+  // which consumed (hence saw land) the previous fill itself.
+  const int active = consumers;
+  unsigned long long best[NB];
+#pragma unroll
+  for (int j = 0; j < NB; ++j) best[j] = 0ull;
+  for (int it = cw; cw < active && it < n; it += active) {
+    const int s = it % stages;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], (uint32_t)((it / stages) & 1), kGemvWaitLimit))) {
+      if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+      break;
+    }
+    int r0, r1;
+    const T *w0, *w1;
+    pair_rows<T, KIND>(a, p_begin + it, C, r0, r1, w0, w1);
+    const T* s0 = reinterpret_cast<const T*>(gsm + (size_t)s * stage_stride);
+    const T* s1 = s0 + C;
+    const bool two = (w1 != nullptr);
+    float acc0[NB], acc1[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) acc0[j] = acc1[j] = 0.0f;
+#pragma unroll 4
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 wa = *reinterpret_cast<const uint4*>(s0 + (size_t)v * VPE);
+      const uint4 wb = two ? *reinterpret_cast<const uint4*>(s1 + (size_t)v * VPE) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        if (j < nb) {
+          const float* xp = xs + (size_t)j * C + (size_t)v * VPE;
+          acc0[j] += dot_vec<T>(wa, xp);
+          acc1[j] += dot_vec<T>(wb, xp);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[s])) : "memory");
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      acc0[j] = warp_sum(acc0[j]);
+      acc1[j] = warp_sum(acc1[j]);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        if (j < nb) epilogue<T, KIND>(a, j, r0, r1, acc0[j], acc1[j], best[j]);
+    }
+  }
+
+  if constexpr (KIND == LM_HEAD) {
+    if (lane == 0)
+#pragma unroll
+      for (int j = 0; j < NB; ++j) cta_best[cw][j] = best[j];
+    cons_bar();
+    const int ct = threadIdx.x - 32;
+    if (ct < nb) {
+      unsigned long long m = 0ull;
+      for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][ct]);
+      if (m) atomicMax(a.lm_keys + ct, m);
+      __threadfence();
+    }
+    cons_bar();
+    if (ct == 0) {
+      __threadfence();
+      am_last = (atomicAdd(a.lm_cnt, 1) == (int)gridDim.x - 1);
+    }
+    cons_bar();
+    if (am_last) {
+      __threadfence();
+      for (int b = ct; b < a.B; b += 256) {
+        const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
+        a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
+        a.pending[b] = a.k;
+      }
+      if (ct == 0) atomicExch(a.lm_cnt, 0);
+    }
+  }
+}
+
 template <typename T, int KIND>
 static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& a) {
   const int C = (KIND == EH_PROJ) ? 2 * a.H : (KIND == O_PROJ) ? a.q_dim : (KIND == DOWN) ? a.F : a.H;
@@ -393,6 +616,45 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
                   : (KIND == DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
   cudaError_t e;
   prof_before(ctx, kid, s);
+  // TMA-streamed variant for B <= 4
+  {
+    const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;
+    const size_t stage_stride = ((size_t)2 * C * sizeof(T) + 127) & ~(size_t)127;
+    const size_t xs_bytes = (size_t)nbt * C * sizeof(float);
+    const size_t budget = 220 * 1024;
+    int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;
+    if (max_stages > kMaxTmaStages) max_stages = kMaxTmaStages;
+    // stages = consumers * k: pick the consumer count (4..8) that keeps the most stages
+    int consumers = 0, stages = 0;
+    for (int cw = kTmaConsumers; cw >= 1; --cw) {
+      const int st = cw * (max_stages / cw);
+      if (st > stages || (st == stages && st > 0 && cw > consumers && cw <= max_stages)) {
+        stages = st;
+        consumers = cw;
+      }
+      if (cw <= 4 && stages > 0) break;
+    }
+    if (((ctx->gemv_stream_mask >> KIND) & 1) && a.B <= 4 && stages >= 2 && consumers >= 2) {
+      const size_t smem_t = stages * stage_stride + xs_bytes;
+      const int gridt = min(ctx->num_sms, P);
+      if (nbt == 1) {
+        auto kern = gemv_tma_kernel<T, KIND, 1>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
+      } else if (nbt == 2) {
+        auto kern = gemv_tma_kernel<T, KIND, 2>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
+      } else {
+        auto kern = gemv_tma_kernel<T, KIND, 4>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
+      }
+      prof_after(ctx, kid, s);
+      ctx->launches++;
+      return e;
+    }
+  }
   if (nb == 4) {
     auto kern = gemv_kernel<T, KIND, 4>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
