@@ -162,9 +162,6 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   if (with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128 && c.hidden % 128 == 0 && c.ffn % 64 == 0 &&
       ctx->q_dim % 64 == 0 && c.max_batch >= ctx->tc_min_batch) {
     const size_t mb = (size_t)c.max_batch;
-    const int nt_max = ((c.max_batch < 256 ? c.max_batch : 256) + 15) / 16 * 16;
-    const size_t tiles = std::max<size_t>({(size_t)(c.vocab + 127) / 128, (size_t)c.ffn / 64,
-                                          (size_t)c.hidden / 128, (size_t)(c.n_q_heads + 2 * c.n_kv_heads)});
     size_t o2 = 0;
     auto take2 = [&](size_t bytes) {
       const size_t o = o2;
@@ -173,7 +170,6 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     };
     const size_t t_eh = take2(mb * 2 * c.hidden * 2), t_xn = take2(mb * c.hidden * 2);
     const size_t t_at = take2(mb * ctx->q_dim * 2), t_act = take2(mb * c.ffn * 2);
-    const size_t t_fix = take2((size_t)2 * sms * nt_max * 128 * 4), t_cnt = take2(tiles * 4);
     if (cudaMalloc(&ctx->tc_ws, o2) != cudaSuccess || cudaMemset(ctx->tc_ws, 0, o2) != cudaSuccess) {
       cudaGetLastError();
       if (ctx->tc_ws) cudaFree(ctx->tc_ws);
@@ -186,8 +182,6 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     ctx->tc_xn = (uint16_t*)(tb + t_xn);
     ctx->tc_attn = (uint16_t*)(tb + t_at);
     ctx->tc_act = (uint16_t*)(tb + t_act);
-    ctx->tc_fix = (float*)(tb + t_fix);
-    ctx->tc_tile_cnt = (int*)(tb + t_cnt);
   }
   *out = ctx;
   return MTP_OK;

@@ -204,8 +204,6 @@ struct mtp_ctx {
   uint16_t* tc_xn;              // [maxB, H]  bf16 normalised GEMM input
   uint16_t* tc_attn;            // [maxB, q_dim] bf16 attention output
   uint16_t* tc_act;             // [maxB, F]  bf16 silu(g) * u
-  float* tc_fix;                // [2 * num_sms, NTmax, 128] stream-K pieces
-  int* tc_tile_cnt;             // [max tiles]
   // timing
   int prof_kernel;
   int prof_cap;

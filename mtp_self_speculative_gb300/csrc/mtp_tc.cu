@@ -18,10 +18,17 @@
 //            free the stages and publish finished accumulators.
 //   warps 2-5 epilogue: tcgen05.ld of the accumulator rows (warp w reads TMEM
 //            lanes 32*(w%4)..+31), fused epilogue per kind, stores.
-// Work split: the (tile, 64-wide k-block) units are divided evenly over the
-// CTAs (stream-K).  A tile cut by a CTA boundary is summed deterministically:
-// each piece is written to a fix-up slot, and the last piece to arrive adds
-// all pieces in k order before the epilogue.
+// Work split (no global fix-up, deterministic):
+//   * kinds with at least as many 128-row tiles as CTAs (LM head, large
+//     FFNs) take whole tiles, a balanced contiguous range per CTA, with two
+//     TMEM accumulators so the epilogue of one tile overlaps the next tile's
+//     MMAs;
+//   * kinds with fewer tiles than CTAs are split along K over a thread-block
+//     cluster of S <= 8 CTAs per tile: each CTA accumulates its K-slice in
+//     TMEM, parks the partial tile in its (drained) stage memory, and after a
+//     cluster barrier CTA rank r sums column slice r over the S partials in
+//     rank order through distributed shared memory and applies the epilogue.
+// Two CTAs per SM whenever the ring and TMEM allow it.
 //
 // Epilogue kinds: EH_PROJ (x = D), QKV_ROPE (rotary pairs (i, i+64) of one
 // head exchanged through shared memory; q stored fp32, k/v rounded to bf16
@@ -35,6 +42,8 @@
 // that write bf16 GEMM operands.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include "mtp_common.cuh"
 
@@ -56,6 +65,7 @@ struct TcArgs {
   int kind;
   int B, NT, H, q_dim, kv_dim, F, V, n_q, n_kv, bs, k, K;
   int C, nkb, n_tiles, stages, max_pos, num_blocks, max_blocks;
+  int ksplit;              // 1: whole tiles per CTA; S > 1: cluster of S CTAs per tile
   const int32_t* positions;
   int32_t* draft_ids;
   float* logits;
@@ -67,8 +77,6 @@ struct TcArgs {
   int32_t* pending;
   float *hid, *x, *q, *h1;
   uint16_t* act_bf16;
-  float* fix;              // [2 * grid][NT][128]
-  int* tile_cnt;           // [n_tiles]
   unsigned long long* lm_keys;
   int* lm_cnt;
   int* err;
@@ -136,22 +144,100 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
-// --------------------------------------------------------- work partition
-struct Part {
-  int u0, u1;  // this CTA's units [u0, u1)
-};
-__device__ __forceinline__ int unit_begin(long long i, long long U, long long G) { return (int)((i * U) / G); }
-__device__ __forceinline__ int cta_of_unit(long long u, long long U, long long G) {
-  return (int)(((u + 1) * G - 1) / U);
-}
 
 // ----------------------------------------------------------- epilogues
+
+
+// Per-request metadata of the QKV epilogue, cached in shared memory once per
+// CTA: rotary position (-1: out of range) and the element offset of the new
+// KV slot in the pools at kv head 0 (-1: invalid slot or pending mismatch).
+struct QkvMeta {
+  int pos[256];
+  long long kv[256];
+};
+
+__device__ void qkv_meta_fill(const TcArgs& a, QkvMeta* meta, int tid, int nthreads) {
+  for (int b = tid; b < a.B; b += nthreads) {
+    int pos = a.positions[b] + a.k - 1;
+    if (pos < 0 || pos >= a.max_pos) {
+      set_error(a.err, MTP_ERR_CAPACITY);
+      pos = -1;
+    }
+    meta->pos[b] = pos;
+    long long kvoff = -1;
+    if (a.pending[b] != a.k - 1) {
+      set_error(a.err, MTP_ERR_DEVICE_ARGS);
+    } else {
+      const int slot = a.seq_len[b] + a.k - 1;
+      const int bi = slot / a.bs, off = slot - bi * a.bs;
+      const int blk = (slot >= 0 && bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+      if (blk < 0 || blk >= a.num_blocks) set_error(a.err, MTP_ERR_CAPACITY);
+      else kvoff = ((long long)blk * a.n_kv * a.bs + off) * 128;
+    }
+    meta->kv[b] = kvoff;
+  }
+}
 
 struct EpiCtx {
   int tile, m, lane, quarter;  // m = row of the tile held by this thread
   float* xbuf;                 // [64][16] exchange buffer
   unsigned long long* cta_best;
+  const QkvMeta* meta;
 };
+
+// Pair kinds, one output pair: rows i and i + 64 of the tile for batch row b.
+__device__ __forceinline__ void tc_pair_store(const TcArgs& a, const QkvMeta* meta, int tile, int i, int b, float v0,
+                                              float v1) {
+  if (a.kind == TC_GU) {
+    const int f = tile * 64 + i;
+    if (f < a.F) a.act_bf16[(size_t)b * a.F + f] = f32_to_bf16_rne(v0 / (1.0f + __expf(-v0)) * v1);
+    return;
+  }
+  // TC_QKV: tile = head
+  const int grp = tile;
+  const int pos = meta->pos[b];
+  if (pos < 0) return;
+  if (grp < a.n_q) {
+    const float2 cs = a.rope[(size_t)pos * 64 + i];
+    float* qb = a.q + (size_t)b * a.q_dim + grp * 128;
+    qb[i] = v0 * cs.x - v1 * cs.y;
+    qb[i + 64] = v1 * cs.x + v0 * cs.y;
+    return;
+  }
+  const long long kvoff = meta->kv[b];
+  if (kvoff < 0) return;
+  float o0 = v0, o1 = v1;
+  uint16_t* pool;
+  int g;
+  if (grp < a.n_q + a.n_kv) {
+    const float2 cs = a.rope[(size_t)pos * 64 + i];
+    o0 = v0 * cs.x - v1 * cs.y;
+    o1 = v1 * cs.x + v0 * cs.y;
+    pool = a.k_pool;
+    g = grp - a.n_q;
+  } else {
+    pool = a.v_pool;
+    g = grp - a.n_q - a.n_kv;
+  }
+  uint16_t* dst = pool + kvoff + (size_t)g * a.bs * 128;
+  dst[i] = f32_to_bf16_rne(o0);
+  dst[i + 64] = f32_to_bf16_rne(o1);
+}
+
+// Plain kinds, one output: row r of the layer output for batch row b.
+__device__ __forceinline__ void tc_plain_store(const TcArgs& a, int r, int b, float v) {
+  if (r >= a.H) return;
+  const size_t o = (size_t)b * a.H + r;
+  if (a.kind == TC_EH) {
+    a.x[o] = v;
+  } else if (a.kind == TC_O) {
+    a.h1[o] = a.x[o] + v;
+  } else {
+    const float hv = a.h1[o] + v;
+    a.hid[o] = hv;
+    if (a.hidden_out && a.k == a.K) a.hidden_out[o] = hv;
+  }
+}
 
 // Apply the epilogue to 16 columns [c0, c0 + 16) of this thread's row.
 __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const float (&v)[16]) {
@@ -159,20 +245,8 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
   if (kind == TC_EH || kind == TC_O || kind == TC_DOWN) {
     const int r = e.tile * 128 + e.m;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int b = c0 + j;
-      if (b >= a.B || r >= a.H) continue;
-      const size_t o = (size_t)b * a.H + r;
-      if (kind == TC_EH) {
-        a.x[o] = v[j];
-      } else if (kind == TC_O) {
-        a.h1[o] = a.x[o] + v[j];
-      } else {
-        const float hv = a.h1[o] + v[j];
-        a.hid[o] = hv;
-        if (a.hidden_out && a.k == a.K) a.hidden_out[o] = hv;
-      }
-    }
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < a.B) tc_plain_store(a, r, c0 + j, v[j]);
     return;
   }
   if (kind == TC_LM) {
@@ -202,69 +276,53 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
   }
   epi_bar();
   if (!upper) {
-    const int i = e.m;
-    if (kind == TC_GU) {
-      const int f = e.tile * 64 + i;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int b = c0 + j;
-        if (b >= a.B || f >= a.F) continue;
-        const float g = v[j], u = e.xbuf[i * 16 + j];
-        a.act_bf16[(size_t)b * a.F + f] = f32_to_bf16_rne(g / (1.0f + __expf(-g)) * u);
-      }
-    } else {  // TC_QKV: tile = head
-      const int grp = e.tile;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int b = c0 + j;
-        if (b >= a.B) continue;
-        const float v0 = v[j], v1 = e.xbuf[i * 16 + j];
-        const int pos = a.positions[b] + a.k - 1;
-        if (pos < 0 || pos >= a.max_pos) {
-          set_error(a.err, MTP_ERR_CAPACITY);
-          continue;
-        }
-        if (grp < a.n_q) {
-          const float2 cs = a.rope[(size_t)pos * 64 + i];
-          float* qb = a.q + (size_t)b * a.q_dim + grp * 128;
-          qb[i] = v0 * cs.x - v1 * cs.y;
-          qb[i + 64] = v1 * cs.x + v0 * cs.y;
-          continue;
-        }
-        if (a.pending[b] != a.k - 1) {
-          set_error(a.err, MTP_ERR_DEVICE_ARGS);
-          continue;
-        }
-        const int slot = a.seq_len[b] + a.k - 1;
-        const int bi = slot / a.bs, off = slot - bi * a.bs;
-        const int blk = (slot >= 0 && bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
-        if (blk < 0 || blk >= a.num_blocks) {
-          set_error(a.err, MTP_ERR_CAPACITY);
-          continue;
-        }
-        float o0 = v0, o1 = v1;
-        uint16_t* pool;
-        int g;
-        if (grp < a.n_q + a.n_kv) {
-          const float2 cs = a.rope[(size_t)pos * 64 + i];
-          o0 = v0 * cs.x - v1 * cs.y;
-          o1 = v1 * cs.x + v0 * cs.y;
-          pool = a.k_pool;
-          g = grp - a.n_q;
-        } else {
-          pool = a.v_pool;
-          g = grp - a.n_q - a.n_kv;
-        }
-        uint16_t* dst = pool + (((size_t)blk * a.n_kv + g) * a.bs + off) * 128;
-        dst[i] = f32_to_bf16_rne(o0);
-        dst[i + 64] = f32_to_bf16_rne(o1);
-      }
-    }
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < a.B) tc_pair_store(a, e.meta, e.tile, e.m, c0 + j, v[j], e.xbuf[e.m * 16 + j]);
   }
   epi_bar();
 }
 
+__device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- kernel
+
+// Work of one CTA: a list of segments (tile, k-blocks [k0, k1)).
+//   ksplit == 1: whole tiles, a balanced contiguous range per CTA.
+//   ksplit == S: CTA blockIdx.x is rank r of the cluster for tile
+//                blockIdx.x / S and owns k-blocks [r*nkb/S, (r+1)*nkb/S).
+struct SegList {
+  int t0, count, k0, k1;  // ksplit == 1: tiles t0..t0+count-1 with [0, nkb)
+};
+__device__ __forceinline__ SegList seg_list(const TcArgs& a) {
+  SegList L;
+  if (a.ksplit == 1) {
+    const long long G = gridDim.x;
+    L.t0 = (int)(((long long)blockIdx.x * a.n_tiles) / G);
+    L.count = (int)(((long long)(blockIdx.x + 1) * a.n_tiles) / G) - L.t0;
+    L.k0 = 0;
+    L.k1 = a.nkb;
+  } else {
+    const int r = blockIdx.x % a.ksplit;
+    L.t0 = blockIdx.x / a.ksplit;
+    L.count = 1;
+    L.k0 = (int)(((long long)r * a.nkb) / a.ksplit);
+    L.k1 = (int)(((long long)(r + 1) * a.nkb) / a.ksplit);
+  }
+  return L;
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
@@ -274,19 +332,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   __shared__ int last_flag, stop_snap;
   __shared__ float xbuf[64 * 16];
   __shared__ unsigned long long cta_best[256];
+  __shared__ QkvMeta qkv_meta;
 
   unsigned char* smem = (unsigned char*)(((uintptr_t)tc_smem_raw + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = a.NT, NS = a.stages;
   const uint32_t bytes_b = (uint32_t)NT * 128;
   const uint32_t stage_bytes = kTcTileBytesA + bytes_b;
-  const uint32_t tmem_cols = (2 * NT <= 32) ? 32 : (2 * NT <= 64) ? 64 : (2 * NT <= 128) ? 128 : (2 * NT <= 256) ? 256 : 512;
+  const int nacc = (a.ksplit == 1) ? 2 : 1;
+  const uint32_t need = (uint32_t)(nacc * NT);
+  const uint32_t tmem_cols = need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
 
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], 1);
     }
     mbar_init(&accf_bar[0], 1);
     mbar_init(&accf_bar[1], 1);
@@ -305,92 +366,72 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
-
-  const long long G = gridDim.x, U = (long long)a.n_tiles * a.nkb;
-  const int u0 = unit_begin(blockIdx.x, U, G), u1 = unit_begin(blockIdx.x + 1, U, G);
-  const int first_tile = u0 / a.nkb;
+  const SegList L = seg_list(a);
+  const int per_seg = L.k1 - L.k0;
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer
-      auto a_coords = [&](int tile, const CUtensorMap*& m0, int& row) {
-        if (a.kind == TC_QKV) {
-          if (tile < a.n_q) { m0 = &maps.a0; row = tile * 128; }
-          else if (tile < a.n_q + a.n_kv) { m0 = &maps.a1; row = (tile - a.n_q) * 128; }
-          else { m0 = &maps.a2; row = (tile - a.n_q - a.n_kv) * 128; }
-        } else if (a.kind == TC_GU) {
-          m0 = &maps.a0;
-          row = tile * 64;
-        } else {
-          m0 = &maps.a0;
-          row = tile * 128;
-        }
-      };
-      auto issue_a = [&](int it_stage, int tile, int kb) {
-        unsigned char* st = smem + (size_t)it_stage * stage_bytes;
-        const CUtensorMap* m0;
-        int row;
-        a_coords(tile, m0, row);
+      // producer: segments in order, their k-blocks in order
+      auto issue_a = [&](int st, int tile, int kb) {
+        unsigned char* dst = smem + (size_t)st * stage_bytes;
         if (a.kind == TC_GU) {
-          tma_load_2d(st, &maps.a0, kb * 64, row, &full_bar[it_stage]);
-          tma_load_2d(st + 8192, &maps.a1, kb * 64, row, &full_bar[it_stage]);
+          tma_load_2d(dst, &maps.a0, kb * 64, tile * 64, &full_bar[st]);
+          tma_load_2d(dst + 8192, &maps.a1, kb * 64, tile * 64, &full_bar[st]);
+        } else if (a.kind == TC_QKV) {
+          if (tile < a.n_q) tma_load_2d(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st]);
+          else if (tile < a.n_q + a.n_kv) tma_load_2d(dst, &maps.a1, kb * 64, (tile - a.n_q) * 128, &full_bar[st]);
+          else tma_load_2d(dst, &maps.a2, kb * 64, (tile - a.n_q - a.n_kv) * 128, &full_bar[st]);
         } else {
-          tma_load_2d(st, m0, kb * 64, row, &full_bar[it_stage]);
+          tma_load_2d(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st]);
         }
       };
-      auto issue_b = [&](int it_stage, int kb) {
-        unsigned char* st = smem + (size_t)it_stage * stage_bytes;
-        tma_load_2d(st + kTcTileBytesA, &maps.b, kb * 64, 0, &full_bar[it_stage]);
+      auto issue_b = [&](int st, int kb) {
+        tma_load_2d(smem + (size_t)st * stage_bytes + kTcTileBytesA, &maps.b, kb * 64, 0, &full_bar[st]);
       };
-      const int n_it = u1 - u0;
+      const int n_it = L.count * per_seg;
       const int pre = n_it < NS ? n_it : NS;
       for (int it = 0; it < pre; ++it) {
-        const int u = u0 + it;
         mbar_expect_tx(&full_bar[it], stage_bytes);
-        issue_a(it, u / a.nkb, u % a.nkb);
+        issue_a(it, L.t0 + it / per_seg, L.k0 + it % per_seg);
       }
       pdl_wait();
-      for (int it = 0; it < pre; ++it) issue_b(it, (u0 + it) % a.nkb);
+      for (int it = 0; it < pre; ++it) issue_b(it, L.k0 + it % per_seg);
       for (int it = pre; it < n_it; ++it) {
-        const int s = it % NS;
-        if (!tc_wait(&empty_bar[s], ((it / NS) & 1) ^ 1, &abort_flag)) {
+        const int st = it % NS;
+        if (!tc_wait(&empty_bar[st], ((it / NS) & 1) ^ 1, &abort_flag)) {
           abort_flag = 1;
           set_error(a.err, MTP_ERR_TIMEOUT);
           break;
         }
-        const int u = u0 + it;
-        mbar_expect_tx(&full_bar[s], stage_bytes);
-        issue_a(s, u / a.nkb, u % a.nkb);
-        issue_b(s, u % a.nkb);
+        mbar_expect_tx(&full_bar[st], stage_bytes);
+        issue_a(st, L.t0 + it / per_seg, L.k0 + it % per_seg);
+        issue_b(st, L.k0 + it % per_seg);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer
       const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-      int it = 0, seg = 0;
+      int it = 0;
       bool ok = true;
-      for (int u = u0; u < u1 && ok; ++seg) {
-        const int tile = u / a.nkb;
-        const int ue = min(u1, (tile + 1) * a.nkb);
+      for (int seg = 0; seg < L.count && ok; ++seg) {
         const int buf = seg & 1;
         if (!tc_wait(&acce_bar[buf], ((seg >> 1) & 1) ^ 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * NT);
-        for (int uu = u; uu < ue; ++uu, ++it) {
-          const int s = it % NS;
-          if (!tc_wait(&full_bar[s], (it / NS) & 1, &abort_flag)) { ok = false; break; }
+        for (int kk_ = 0; kk_ < per_seg; ++kk_, ++it) {
+          const int st = it % NS;
+          if (!tc_wait(&full_bar[st], (it / NS) & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa_ = smem_addr(smem + (size_t)s * stage_bytes);
+          const uint32_t sa_ = smem_addr(smem + (size_t)st * stage_bytes);
           const uint32_t sb_ = sa_ + kTcTileBytesA;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma(d, sw128_desc(sa_ + kk * 32), sw128_desc(sb_ + kk * 32), idesc, (uu > u || kk > 0) ? 1u : 0u);
-          tc_commit(&empty_bar[s]);
+            tc_mma(d, sw128_desc(sa_ + kk * 32), sw128_desc(sb_ + kk * 32), idesc, (kk_ > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty_bar[st]);
         }
         if (!ok) break;
         tc_commit(&accf_bar[buf]);
-        u = ue;
       }
       if (!ok) {
         abort_flag = 1;
@@ -409,12 +450,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     e.quarter = quarter;
     e.xbuf = xbuf;
     e.cta_best = cta_best;
-    int seg = 0;
-    for (int u = u0; u < u1; ++seg) {
-      const int tile = u / a.nkb;
-      const int ue = min(u1, (tile + 1) * a.nkb);
+    e.meta = &qkv_meta;
+    if (a.kind == TC_QKV) {
+      qkv_meta_fill(a, &qkv_meta, epi_tid, kTcEpiThreads);
+      epi_bar();
+    }
+    for (int seg = 0; seg < L.count; ++seg) {
       const int buf = seg & 1;
-      e.tile = tile;
+      e.tile = L.t0 + seg;
       bool ok = tc_wait(&accf_bar[buf], (seg >> 1) & 1, &abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) {
@@ -428,57 +471,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       if (stop_snap) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * NT);
-      const bool whole = (u == tile * a.nkb) && (ue == (tile + 1) * a.nkb);
-      if (whole) {
+      if (a.ksplit == 1) {
         for (int c0 = 0; c0 < NT; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + c0, v);
           tc_epilogue(a, e, c0, v);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce_bar[buf])) : "memory");
       } else {
-        const int slot = 2 * blockIdx.x + ((tile == first_tile) ? 0 : 1);
-        float* fs = a.fix + (size_t)slot * NT * 128;
+        // partial tile -> shared memory (the stages are drained): part[c][row]
+        float* part = reinterpret_cast<float*>(smem);
         for (int c0 = 0; c0 < NT; c0 += 16) {
           float v[16];
           tmem_ld16(tbase + c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) fs[(size_t)(c0 + j) * 128 + m] = v[j];
+          for (int j = 0; j < 16; ++j) part[(c0 + j) * 128 + m] = v[j];
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce_bar[buf])) : "memory");
-        __threadfence();
-        epi_bar();
-        const int cta_first = cta_of_unit((long long)tile * a.nkb, U, G);
-        const int cta_last = cta_of_unit((long long)(tile + 1) * a.nkb - 1, U, G);
-        if (epi_tid == 0) {
-          const int prev = atomicAdd(a.tile_cnt + tile, 1);
-          last_flag = (prev == cta_last - cta_first);
-        }
-        epi_bar();
-        if (last_flag) {
-          __threadfence();
-          for (int c0 = 0; c0 < NT; c0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
-            for (int cj = cta_first; cj <= cta_last; ++cj) {
-              const int first_tile_j = unit_begin(cj, U, G) / a.nkb;
-              const int sj = 2 * cj + ((tile == first_tile_j) ? 0 : 1);
-              const float* fj = a.fix + (size_t)sj * NT * 128;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(fj + (size_t)(c0 + j) * 128 + m);
-            }
-            tc_epilogue(a, e, c0, v);
-          }
-          if (epi_tid == 0) a.tile_cnt[tile] = 0;
-        }
-        epi_bar();
       }
-      u = ue;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&acce_bar[buf])) : "memory");
     }
     if (a.kind == TC_LM) {
       epi_bar();
@@ -498,6 +509,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         if (epi_tid == 0) atomicExch(a.lm_cnt, 0);
       }
     }
+  }
+
+  if (a.ksplit > 1) {
+    // Cluster reduction: every CTA of the cluster holds one k-slice partial of
+    // the same tile in shared memory; rank r sums the column slice
+    // [r*NT/S, (r+1)*NT/S) over ranks 0..S-1 in order (deterministic) through
+    // distributed shared memory and applies the epilogue to it.
+    __syncwarp();
+    cluster_sync_all();
+    if (warp >= 2 && !abort_flag) {
+      const int S = a.ksplit;
+      const int r = blockIdx.x % S;
+      const int tile = blockIdx.x / S;
+      const int c_lo = (r * NT) / S, c_hi = ((r + 1) * NT) / S;
+      const int rows = (a.kind == TC_QKV || a.kind == TC_GU) ? 64 : 128;
+      const uint32_t part_local = smem_addr(smem);
+      uint32_t base[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) base[j] = (j < S) ? mapa(part_local, (uint32_t)j) : 0u;
+      const int items = (c_hi - c_lo) * rows;
+      for (int idx = threadIdx.x - 64; idx < items; idx += kTcEpiThreads) {
+        const int c = c_lo + idx / rows, mm = idx % rows;
+        if (c >= a.B) continue;
+        float v0 = 0.0f, v1 = 0.0f;
+        const uint32_t off0 = (uint32_t)((c * 128 + mm) * 4), off1 = off0 + 64 * 4;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < S) {
+            v0 += ld_dsmem(base[j] + off0);
+            if (rows == 64) v1 += ld_dsmem(base[j] + off1);
+          }
+        if (rows == 64) tc_pair_store(a, &qkv_meta, tile, mm, c, v0, v1);
+        else tc_plain_store(a, tile * 128 + mm, c, v0);
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();
   }
 
   tc_fence_before();
@@ -668,24 +716,78 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   a.k_pool = (uint16_t*)kv->k_pool; a.v_pool = (uint16_t*)kv->v_pool; a.block_table = kv->block_table;
   a.seq_len = kv->seq_len; a.pending = kv->pending;
   a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.h1 = ctx->h1; a.act_bf16 = ctx->tc_act;
-  a.fix = ctx->tc_fix; a.tile_cnt = ctx->tc_tile_cnt; a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
+  a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
   a.err = ctx->err; a.rope = ctx->rope;
   const int stage_bytes = kTcTileBytesA + NT * 128;
-  const int budget = 200 * 1024;
+  // two CTAs per SM when a ring of >= 3 stages fits in ~100 KB and both CTAs'
+  // accumulators fit in TMEM (512 columns)
+  const bool two_per_sm = 3 * stage_bytes <= 100 * 1024 && 2 * (2 * NT) <= 512;
+  const int budget = two_per_sm ? 100 * 1024 : 200 * 1024;
   int stages = budget / stage_bytes;
   if (stages > 8) stages = 8;
   if (stages < 2) stages = 2;
   a.stages = stages;
+  const int slots = (two_per_sm ? 2 : 1) * ctx->num_sms;
   const size_t smem = 1024 + (size_t)stages * stage_bytes;
-  int grid = ctx->num_sms;
-  const long long U = (long long)n_tiles * a.nkb;
-  if (grid > U) grid = (int)U;
   cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int S = 1;
+  if (kind != TC_LM && n_tiles < slots && (size_t)stages * stage_bytes >= (size_t)NT * 128 * 4) {
+    // the LM head keeps whole tiles (argmax epilogue).  Largest cluster size
+    // S <= 8 whose clusters all fit on the GPU at once (one wave).
+    int s_max = slots / n_tiles;
+    if (s_max > 8) s_max = 8;
+    if (s_max > a.nkb / 2) s_max = a.nkb / 2;
+    for (int cand = s_max; cand >= 2; --cand) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(n_tiles * cand);
+      q.blockDim = dim3(kTcThreads);
+      q.dynamicSmemBytes = smem;
+      q.stream = s;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = (unsigned)cand;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)tc_gemm_kernel, &q) != cudaSuccess) {
+        cudaGetLastError();
+        continue;
+      }
+      if (clusters >= n_tiles) {
+        S = cand;
+        break;
+      }
+    }
+  }
+  a.ksplit = S;
+  const int grid = (S > 1) ? n_tiles * S : (n_tiles < slots ? n_tiles : slots);
+  if (getenv("MTP_TC_TRACE")) {
+    static int seen[8] = {0};
+    if (!seen[kind]++)
+      fprintf(stderr, "tc kind %d: B %d NT %d tiles %d nkb %d stages %d two_per_sm %d cluster %d grid %d\n", kind, B,
+              NT, n_tiles, a.nkb, stages, (int)two_per_sm, S, grid);
+  }
   const int kid = (kind == TC_EH) ? MTP_KERNEL_EH_PROJ : (kind == TC_QKV) ? MTP_KERNEL_QKV_ROPE
                   : (kind == TC_O) ? MTP_KERNEL_O_PROJ : (kind == TC_GU) ? MTP_KERNEL_GATE_UP
                   : (kind == TC_DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
   prof_before(ctx, kid, s);
-  cudaError_t e = launch_pdl(tc_gemm_kernel, dim3(grid), dim3(kTcThreads), smem, s, maps, a);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kTcThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = (S > 1) ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, tc_gemm_kernel, maps, a);
   prof_after(ctx, kid, s);
   ctx->launches++;
   return e;
