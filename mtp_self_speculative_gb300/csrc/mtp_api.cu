@@ -7,6 +7,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "mtp_common.cuh"
@@ -24,6 +27,19 @@ void prof_after(mtp_ctx* ctx, int kernel, cudaStream_t s) {
 }
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[std::make_pair(func, dev)];
+  if (bytes <= have) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
 
 }  // namespace mtp
 
@@ -196,6 +212,8 @@ void mtp_destroy(mtp_ctx* ctx) {
   }
   cudaFree(ctx->ws);
   if (ctx->tc_ws) cudaFree(ctx->tc_ws);
+  free(ctx->tc_plan_cache);
+  free(ctx->attn_map_cache);
   free(ctx);
 }
 

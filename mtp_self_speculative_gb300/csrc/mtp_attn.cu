@@ -19,6 +19,9 @@
 // sum per head, base-2 exponentials with the scale folded into q).  Warps
 // merge in shared memory; splits merge in the last CTA to finish (arrival
 // counter), which writes o and resets the counter.
+#include <stdlib.h>
+#include <string.h>
+
 #include "mtp_common.cuh"
 
 namespace mtp {
@@ -578,7 +581,7 @@ static cudaError_t attn_launch(mtp_ctx* ctx, cudaStream_t s, const AttnArgs<T>& 
   constexpr size_t merge_bytes = (size_t)kAttnWarps * G * HD * sizeof(float);
   constexpr size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
   auto kern = attn_kernel<T, HD, G>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  ensure_smem((const void*)kern, smem);
   return launch_pdl(kern, dim3(splits, ctx->cfg.n_kv_heads, B), dim3(kAttnThreads), smem, s, a);
 }
 
@@ -594,6 +597,13 @@ static int attn_bps(const mtp_ctx* ctx, int B, int max_blocks, int min_bps) {
   while ((max_blocks + bps - 1) / bps > ctx->attn_max_splits) ++bps;
   return bps;
 }
+
+struct AttnMapCache {
+  CUtensorMap km, vm;
+  const void* k_pool;
+  const void* v_pool;
+  int num_blocks;
+};
 
 template <typename T>
 static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv) {
@@ -613,21 +623,36 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
   a.max_splits = splits;  // partial-buffer stride of this call
   a.qscale = 1.4426950408889634f / sqrtf((float)c.head_dim);
   if (use_mma) {
-    CUtensorMap km, vm;
-    const uint64_t rows = (uint64_t)kv->num_blocks * c.n_kv_heads * 16;
-    if (!make_map(&km, kv->k_pool, rows, 128, 16) || !make_map(&vm, kv->v_pool, rows, 128, 16))
-      return cudaErrorInvalidValue;
+    // tensor maps of the pools, re-encoded only when the pools change
+    if (!ctx->attn_map_cache) {
+      ctx->attn_map_cache = aligned_alloc(64, sizeof(AttnMapCache));
+      if (!ctx->attn_map_cache) return cudaErrorMemoryAllocation;
+      memset(ctx->attn_map_cache, 0, sizeof(AttnMapCache));
+    }
+    AttnMapCache* mc = (AttnMapCache*)ctx->attn_map_cache;
+    if (mc->k_pool != kv->k_pool || mc->v_pool != kv->v_pool || mc->num_blocks != kv->num_blocks) {
+      const uint64_t rows = (uint64_t)kv->num_blocks * c.n_kv_heads * 16;
+      if (!make_map(&mc->km, kv->k_pool, rows, 128, 16) || !make_map(&mc->vm, kv->v_pool, rows, 128, 16)) {
+        mc->k_pool = mc->v_pool = nullptr;
+        return cudaErrorInvalidValue;
+      }
+      mc->k_pool = kv->k_pool;
+      mc->v_pool = kv->v_pool;
+      mc->num_blocks = kv->num_blocks;
+    }
+    const CUtensorMap& km = mc->km;
+    const CUtensorMap& vm = mc->vm;
     const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
     const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096;
     dim3 grid(splits, c.n_kv_heads, B);
     switch (G) {
-      case 1: cudaFuncSetAttribute(attn_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      case 1: ensure_smem((const void*)attn_mma_kernel<1>, smem);
               return launch_pdl(attn_mma_kernel<1>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 2: cudaFuncSetAttribute(attn_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      case 2: ensure_smem((const void*)attn_mma_kernel<2>, smem);
               return launch_pdl(attn_mma_kernel<2>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 4: cudaFuncSetAttribute(attn_mma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      case 4: ensure_smem((const void*)attn_mma_kernel<4>, smem);
               return launch_pdl(attn_mma_kernel<4>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 8: cudaFuncSetAttribute(attn_mma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      case 8: ensure_smem((const void*)attn_mma_kernel<8>, smem);
               return launch_pdl(attn_mma_kernel<8>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
     }
     return cudaErrorInvalidValue;

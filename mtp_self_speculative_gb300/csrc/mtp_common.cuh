@@ -210,6 +210,9 @@ struct mtp_ctx {
   int prof_n;
   cudaEvent_t* prof_ev;  // 2 * prof_cap
   long long launches;
+  // host-side caches (tensor maps need 64-byte aligned storage)
+  void* tc_plan_cache;          // TcPlan[6][17], lazily allocated
+  void* attn_map_cache;         // AttnMapCache, lazily allocated
   // small-batch projections: bit k set = kernel kind k streams its weights
   // through shared memory with bulk copies (else register streaming)
   int gemv_stream_mask;
@@ -232,6 +235,10 @@ cudaError_t launch_pdl(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStre
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device);
+// later calls with the same or a smaller size are free.
+cudaError_t ensure_smem(const void* func, size_t bytes);
 
 // Kernel timing hooks (host).
 void prof_before(mtp_ctx* ctx, int kernel, cudaStream_t s);

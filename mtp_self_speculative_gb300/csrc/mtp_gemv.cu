@@ -639,15 +639,15 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
       const int gridt = min(ctx->num_sms, P);
       if (nbt == 1) {
         auto kern = gemv_tma_kernel<T, KIND, 1>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       } else if (nbt == 2) {
         auto kern = gemv_tma_kernel<T, KIND, 2>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       } else {
         auto kern = gemv_tma_kernel<T, KIND, 4>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_t);
+        ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       }
       prof_after(ctx, kid, s);
@@ -657,15 +657,15 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
   }
   if (nb == 4) {
     auto kern = gemv_kernel<T, KIND, 4>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   } else if (nb == 2) {
     auto kern = gemv_kernel<T, KIND, 2>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   } else {
     auto kern = gemv_kernel<T, KIND, 1>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   }
   prof_after(ctx, kid, s);

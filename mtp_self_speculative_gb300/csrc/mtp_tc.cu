@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 #include <stdio.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "mtp_common.cuh"
 
@@ -668,13 +669,28 @@ bool tc_supported(const mtp_ctx* ctx, int B) {
          B <= 256 && c.hidden % 128 == 0 && c.ffn % 64 == 0 && ctx->q_dim % 64 == 0;
 }
 
-static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int k, int K, const int32_t* positions,
-                             const mtp_kv* kv, int32_t* draft_ids, float* logits, float* hidden_out) {
-  const mtp_config& c = ctx->cfg;
-  const int NT = ((B + 15) / 16) * 16;
+// Launch plan of one GEMM kind at one padded batch width NT: tensor maps,
+// ring depth, cluster size, grid.  Computed once per context and cached (the
+// maps depend only on the weights and the context's activation buffers).
+struct TcPlan {
   TcMaps maps;
-  memset(&maps, 0, sizeof(maps));
+  int valid, stages, S, grid, n_tiles, C;
+  size_t smem;
+};
+constexpr int kTcPlanSlots = 17;  // NT / 16 for NT <= 256
+
+static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
+  if (!ctx->tc_plan_cache) {
+    const size_t bytes = sizeof(TcPlan) * 6 * kTcPlanSlots;
+    ctx->tc_plan_cache = aligned_alloc(64, (bytes + 63) / 64 * 64);
+    if (!ctx->tc_plan_cache) return nullptr;
+    memset(ctx->tc_plan_cache, 0, bytes);
+  }
+  TcPlan* p = &((TcPlan*)ctx->tc_plan_cache)[kind * kTcPlanSlots + NT / 16];
+  if (p->valid) return p;
+  const mtp_config& c = ctx->cfg;
   const mtp_weights& w = ctx->w;
+  TcMaps& maps = p->maps;
   int C = 0, n_tiles = 0;
   bool ok = true;
   switch (kind) {
@@ -705,19 +721,8 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
       ok = make_map(&maps.a0, w.lm_head, c.vocab, C, 128) && make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
       break;
   }
-  if (!ok) return cudaErrorInvalidValue;
-  TcArgs a;
-  memset(&a, 0, sizeof(a));
-  a.kind = kind; a.B = B; a.NT = NT; a.H = c.hidden; a.q_dim = ctx->q_dim; a.kv_dim = ctx->kv_dim; a.F = c.ffn;
-  a.V = c.vocab; a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.bs = c.block_size; a.k = k; a.K = K;
-  a.C = C; a.nkb = C / 64; a.n_tiles = n_tiles; a.max_pos = c.max_pos;
-  a.num_blocks = kv->num_blocks; a.max_blocks = kv->max_blocks;
-  a.positions = positions; a.draft_ids = draft_ids; a.logits = logits; a.hidden_out = hidden_out;
-  a.k_pool = (uint16_t*)kv->k_pool; a.v_pool = (uint16_t*)kv->v_pool; a.block_table = kv->block_table;
-  a.seq_len = kv->seq_len; a.pending = kv->pending;
-  a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.h1 = ctx->h1; a.act_bf16 = ctx->tc_act;
-  a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
-  a.err = ctx->err; a.rope = ctx->rope;
+  if (!ok) return nullptr;
+  const int nkb = C / 64;
   const int stage_bytes = kTcTileBytesA + NT * 128;
   // two CTAs per SM when a ring of >= 3 stages fits in ~100 KB and both CTAs'
   // accumulators fit in TMEM (512 columns)
@@ -726,17 +731,16 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   int stages = budget / stage_bytes;
   if (stages > 8) stages = 8;
   if (stages < 2) stages = 2;
-  a.stages = stages;
   const int slots = (two_per_sm ? 2 : 1) * ctx->num_sms;
   const size_t smem = 1024 + (size_t)stages * stage_bytes;
-  cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ensure_smem((const void*)tc_gemm_kernel, smem) != cudaSuccess) return nullptr;
   int S = 1;
   if (kind != TC_LM && n_tiles < slots && (size_t)stages * stage_bytes >= (size_t)NT * 128 * 4) {
     // the LM head keeps whole tiles (argmax epilogue).  Largest cluster size
     // S <= 8 whose clusters all fit on the GPU at once (one wave).
     int s_max = slots / n_tiles;
     if (s_max > 8) s_max = 8;
-    if (s_max > a.nkb / 2) s_max = a.nkb / 2;
+    if (s_max > nkb / 2) s_max = nkb / 2;
     for (int cand = s_max; cand >= 2; --cand) {
       cudaLaunchConfig_t q = {};
       q.gridDim = dim3(n_tiles * cand);
@@ -761,33 +765,58 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
       }
     }
   }
-  a.ksplit = S;
-  const int grid = (S > 1) ? n_tiles * S : (n_tiles < slots ? n_tiles : slots);
-  if (getenv("MTP_TC_TRACE")) {
-    static int seen[8] = {0};
-    if (!seen[kind]++)
-      fprintf(stderr, "tc kind %d: B %d NT %d tiles %d nkb %d stages %d two_per_sm %d cluster %d grid %d\n", kind, B,
-              NT, n_tiles, a.nkb, stages, (int)two_per_sm, S, grid);
-  }
+  p->stages = stages;
+  p->S = S;
+  p->grid = (S > 1) ? n_tiles * S : (n_tiles < slots ? n_tiles : slots);
+  p->n_tiles = n_tiles;
+  p->C = C;
+  p->smem = smem;
+  p->valid = 1;
+  if (getenv("MTP_TC_TRACE"))
+    fprintf(stderr, "tc kind %d: NT %d tiles %d nkb %d stages %d two_per_sm %d cluster %d grid %d\n", kind, NT,
+            n_tiles, nkb, stages, (int)two_per_sm, S, p->grid);
+  return p;
+}
+
+static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int k, int K, const int32_t* positions,
+                             const mtp_kv* kv, int32_t* draft_ids, float* logits, float* hidden_out) {
+  const mtp_config& c = ctx->cfg;
+  const int NT = ((B + 15) / 16) * 16;
+  const TcPlan* pl = tc_plan(ctx, s, kind, NT);
+  if (!pl) return cudaErrorInvalidValue;
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kind = kind; a.B = B; a.NT = NT; a.H = c.hidden; a.q_dim = ctx->q_dim; a.kv_dim = ctx->kv_dim; a.F = c.ffn;
+  a.V = c.vocab; a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.bs = c.block_size; a.k = k; a.K = K;
+  a.C = pl->C; a.nkb = pl->C / 64; a.n_tiles = pl->n_tiles; a.max_pos = c.max_pos;
+  a.num_blocks = kv->num_blocks; a.max_blocks = kv->max_blocks;
+  a.positions = positions; a.draft_ids = draft_ids; a.logits = logits; a.hidden_out = hidden_out;
+  a.k_pool = (uint16_t*)kv->k_pool; a.v_pool = (uint16_t*)kv->v_pool; a.block_table = kv->block_table;
+  a.seq_len = kv->seq_len; a.pending = kv->pending;
+  a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.h1 = ctx->h1; a.act_bf16 = ctx->tc_act;
+  a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
+  a.err = ctx->err; a.rope = ctx->rope;
+  a.stages = pl->stages;
+  a.ksplit = pl->S;
   const int kid = (kind == TC_EH) ? MTP_KERNEL_EH_PROJ : (kind == TC_QKV) ? MTP_KERNEL_QKV_ROPE
                   : (kind == TC_O) ? MTP_KERNEL_O_PROJ : (kind == TC_GU) ? MTP_KERNEL_GATE_UP
                   : (kind == TC_DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
   prof_before(ctx, kid, s);
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(grid);
+  lc.gridDim = dim3(pl->grid);
   lc.blockDim = dim3(kTcThreads);
-  lc.dynamicSmemBytes = smem;
+  lc.dynamicSmemBytes = pl->smem;
   lc.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)S;
+  attr[1].val.clusterDim.x = (unsigned)pl->S;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = (S > 1) ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&lc, tc_gemm_kernel, maps, a);
+  lc.numAttrs = (pl->S > 1) ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, tc_gemm_kernel, pl->maps, a);
   prof_after(ctx, kid, s);
   ctx->launches++;
   return e;
