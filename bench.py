@@ -40,6 +40,9 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM roofline"
+# dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch from an ncu capture of the
+# current kernel (profiles/lm_head_argmax_qwen3_8b_mtp_b1.md); other workloads report null.
+LM_TRAFFIC = {"qwen3_8b_mtp_b1": 1244752000 + 3860992}
 WORKLOADS = {c.name: c for c in synth.CONFIGS}
 DEFAULT_WORKLOAD = synth.QWEN3_8B_B1.name
 
@@ -420,7 +423,8 @@ def run_ours(args, rank, world, local_rank):
                      "frac_of_measured": sb["total"] / (ms_per_step * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": "lm_head_argmax", "bound": "hbm", "achieved": lm_gbs, "peak": peak,
                      "unit": "GB/s", "frac": lm_gbs / peak, "peak_source": peak_kind + " hbm_gbs",
-                     "traffic": args.lm_traffic, "launches_timed": len(lm_ms),
+                     "traffic": args.lm_traffic if args.lm_traffic is not None else LM_TRAFFIC.get(cfg.name),
+                     "launches_timed": len(lm_ms),
                      "bytes_per_launch": sb["lm_head_launch"]},
         "kernels": kernels,
         "stream_copy_gbs": copy_gbs,
@@ -561,11 +565,16 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ctx", type=int, default=None,
+                    help="override the committed MTP context length (smaller cases for profiling)")
     ap.add_argument("--lm-traffic", type=float, default=None,
                     help="ncu dram bytes per LM-head launch of the current kernel, if captured")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
+    if args.ctx is not None:
+        import dataclasses
+        WORKLOADS[args.workload] = dataclasses.replace(WORKLOADS[args.workload], ctx_lo=args.ctx, ctx_hi=args.ctx)
     rank, world, local_rank = rank_info()
     if world > 1:
         import torch
