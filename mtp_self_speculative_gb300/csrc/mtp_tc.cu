@@ -576,33 +576,70 @@ struct PrepEhArgs {
   int* err;
 };
 
-__device__ __forceinline__ float block_sum256(float v, float* red) {
+
+
+// Single pass: each thread keeps its (up to kPrepPer) elements in registers
+// between the sum of squares and the scaled bf16 store.  512 threads, 4
+// contiguous elements per thread per slot (16-byte fp32 / 8-byte bf16 I/O).
+constexpr int kPrepThreads = 512;
+constexpr int kPrepPer = 8;  // slots of 4 elements: rows up to 512 * 4 * 8 = 16384 wide
+
+__device__ __forceinline__ float prep_sum(float v, float* red) {
   v = warp_sum(v);
   __syncthreads();
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  float t = ((threadIdx.x & 31) < 8) ? red[threadIdx.x & 31] : 0.0f;
+  float t = ((threadIdx.x & 31) < (kPrepThreads / 32)) ? red[threadIdx.x & 31] : 0.0f;
   return warp_sum(t);
 }
 
-__device__ __forceinline__ float bf(const uint16_t* p, int i) { return __uint_as_float(((uint32_t)p[i]) << 16); }
+__device__ __forceinline__ void store_bf16x4(uint16_t* dst, float a0, float a1, float a2, float a3) {
+  uint2 u;
+  u.x = (uint32_t)f32_to_bf16_rne(a0) | ((uint32_t)f32_to_bf16_rne(a1) << 16);
+  u.y = (uint32_t)f32_to_bf16_rne(a2) | ((uint32_t)f32_to_bf16_rne(a3) << 16);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
 
-__global__ void __launch_bounds__(256) prep_eh_kernel(const PrepEhArgs a) {
-  __shared__ float red[8];
+// Normalise one row of n (multiple of 4) elements given as fp32 (src32) or
+// bf16 (src16) and write bf16(x * rsqrt(mean x^2 + eps) * w) to dst.
+__device__ __forceinline__ void prep_row(const float* src32, const uint16_t* src16, const uint16_t* w, uint16_t* dst,
+                                         int n, float eps, float* red) {
+  float4 v[kPrepPer];
+  float ss = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPrepPer; ++j) {
+    const int i = (threadIdx.x + j * kPrepThreads) * 4;
+    if (i < n) {
+      if (src32) {
+        v[j] = *reinterpret_cast<const float4*>(src32 + i);
+      } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(src16 + i);
+        v[j] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+      }
+      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
+  }
+  const float sc = rsqrtf(prep_sum(ss, red) / (float)n + eps);
+#pragma unroll
+  for (int j = 0; j < kPrepPer; ++j) {
+    const int i = (threadIdx.x + j * kPrepThreads) * 4;
+    if (i < n) {
+      const uint2 wu = *reinterpret_cast<const uint2*>(w + i);
+      store_bf16x4(dst + i, v[j].x * sc * bf16_lo(wu.x), v[j].y * sc * bf16_hi(wu.x), v[j].z * sc * bf16_lo(wu.y),
+                   v[j].w * sc * bf16_hi(wu.y));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_eh_kernel(const PrepEhArgs a) {
+  __shared__ float red[kPrepThreads / 32];
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x;
+  uint16_t* out = a.out + (size_t)b * 2 * a.H;
   // hidden half: step 1 reads the caller's bf16 state, later steps the fp32 recursion
-  float ss = 0.0f;
-  for (int i = threadIdx.x; i < a.H; i += 256) {
-    const float v = (a.k == 1) ? bf(a.hidden_in + (size_t)b * a.H, i) : a.hid[(size_t)b * a.H + i];
-    ss += v * v;
-  }
-  float sc = rsqrtf(block_sum256(ss, red) / (float)a.H + a.eps);
-  for (int i = threadIdx.x; i < a.H; i += 256) {
-    const float v = (a.k == 1) ? bf(a.hidden_in + (size_t)b * a.H, i) : a.hid[(size_t)b * a.H + i];
-    a.out[(size_t)b * 2 * a.H + i] = f32_to_bf16_rne(v * sc * bf(a.w_h, i));
-  }
+  if (a.k == 1) prep_row(nullptr, a.hidden_in + (size_t)b * a.H, a.w_h, out, a.H, a.eps, red);
+  else prep_row(a.hid + (size_t)b * a.H, nullptr, a.w_h, out, a.H, a.eps, red);
   // embedding half
   const uint16_t* e;
   if (a.k == 1) {
@@ -615,25 +652,17 @@ __global__ void __launch_bounds__(256) prep_eh_kernel(const PrepEhArgs a) {
     }
     e = a.embed + (size_t)id * a.H;
   }
-  ss = 0.0f;
-  for (int i = threadIdx.x; i < a.H; i += 256) { const float v = bf(e, i); ss += v * v; }
-  sc = rsqrtf(block_sum256(ss, red) / (float)a.H + a.eps);
-  for (int i = threadIdx.x; i < a.H; i += 256)
-    a.out[(size_t)b * 2 * a.H + a.H + i] = f32_to_bf16_rne(bf(e, i) * sc * bf(a.w_e, i));
+  prep_row(nullptr, e, a.w_e, out + a.H, a.H, a.eps, red);
 }
 
 // out[b] = bf16(RMSNorm(src_b) w)
-__global__ void __launch_bounds__(256) prep_norm_kernel(const float* src, const uint16_t* w, uint16_t* out, int C,
-                                                        float eps) {
-  __shared__ float red[8];
+__global__ void __launch_bounds__(kPrepThreads) prep_norm_kernel(const float* src, const uint16_t* w, uint16_t* out,
+                                                                 int C, float eps) {
+  __shared__ float red[kPrepThreads / 32];
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x;
-  const float* s = src + (size_t)b * C;
-  float ss = 0.0f;
-  for (int i = threadIdx.x; i < C; i += 256) ss += s[i] * s[i];
-  const float sc = rsqrtf(block_sum256(ss, red) / (float)C + eps);
-  for (int i = threadIdx.x; i < C; i += 256) out[(size_t)b * C + i] = f32_to_bf16_rne(s[i] * sc * bf(w, i));
+  prep_row(src + (size_t)b * C, nullptr, w, out + (size_t)b * C, C, eps, red);
 }
 
 // -------------------------------------------------------------- host side
@@ -666,7 +695,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 bool tc_supported(const mtp_ctx* ctx, int B) {
   const mtp_config& c = ctx->cfg;
   return ctx->tc_ws != nullptr && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128 && B >= ctx->tc_min_batch &&
-         B <= 256 && c.hidden % 128 == 0 && c.ffn % 64 == 0 && ctx->q_dim % 64 == 0;
+         B <= 256 && c.hidden % 128 == 0 && c.hidden <= 16384 && c.ffn % 64 == 0 && ctx->q_dim % 64 == 0;
 }
 
 // Launch plan of one GEMM kind at one padded batch width NT: tensor maps,
@@ -824,7 +853,7 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
 
 static cudaError_t prep_norm(mtp_ctx* ctx, cudaStream_t s, int B, const float* src, const void* w, int C) {
   ctx->launches++;
-  return launch_pdl(prep_norm_kernel, dim3(B), dim3(256), 0, s, src, (const uint16_t*)w, ctx->tc_xn, C,
+  return launch_pdl(prep_norm_kernel, dim3(B), dim3(kPrepThreads), 0, s, src, (const uint16_t*)w, ctx->tc_xn, C,
                     ctx->cfg.eps);
 }
 
@@ -840,7 +869,7 @@ cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int
   pa.w_h = (const uint16_t*)ctx->w.w_norm_h; pa.w_e = (const uint16_t*)ctx->w.w_norm_e; pa.eps = c.eps;
   pa.out = ctx->tc_xin_eh; pa.err = ctx->err;
   ctx->launches++;
-  if ((e = launch_pdl(prep_eh_kernel, dim3(B), dim3(256), 0, s, pa)) != cudaSuccess) return e;
+  if ((e = launch_pdl(prep_eh_kernel, dim3(B), dim3(kPrepThreads), 0, s, pa)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_EH, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
   if ((e = prep_norm(ctx, s, B, ctx->x, ctx->w.w_norm_in, c.hidden)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_QKV, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
