@@ -761,20 +761,25 @@ static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
   if (stages > 8) stages = 8;
   if (stages < 2) stages = 2;
   const int slots = (two_per_sm ? 2 : 1) * ctx->num_sms;
-  const size_t smem = 1024 + (size_t)stages * stage_bytes;
-  if (ensure_smem((const void*)tc_gemm_kernel, smem) != cudaSuccess) return nullptr;
+  // Clusters are placed one CTA per SM, so a split-K launch gets the whole
+  // SM's shared memory for its ring.
+  int cl_stages = (200 * 1024) / stage_bytes;
+  if (cl_stages > 8) cl_stages = 8;
+  const size_t cl_smem = 1024 + (size_t)cl_stages * stage_bytes;
+  size_t smem = 1024 + (size_t)stages * stage_bytes;
+  if (ensure_smem((const void*)tc_gemm_kernel, cl_smem > smem ? cl_smem : smem) != cudaSuccess) return nullptr;
   int S = 1;
-  if (kind != TC_LM && n_tiles < slots && (size_t)stages * stage_bytes >= (size_t)NT * 128 * 4) {
+  if (kind != TC_LM && n_tiles < slots && (size_t)cl_stages * stage_bytes >= (size_t)NT * 128 * 4) {
     // the LM head keeps whole tiles (argmax epilogue).  Largest cluster size
     // S <= 8 whose clusters all fit on the GPU at once (one wave).
-    int s_max = slots / n_tiles;
+    int s_max = ctx->num_sms / n_tiles;
     if (s_max > 8) s_max = 8;
     if (s_max > nkb / 2) s_max = nkb / 2;
     for (int cand = s_max; cand >= 2; --cand) {
       cudaLaunchConfig_t q = {};
       q.gridDim = dim3(n_tiles * cand);
       q.blockDim = dim3(kTcThreads);
-      q.dynamicSmemBytes = smem;
+      q.dynamicSmemBytes = cl_smem;
       q.stream = s;
       cudaLaunchAttribute qa[1];
       qa[0].id = cudaLaunchAttributeClusterDimension;
@@ -793,6 +798,12 @@ static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
         break;
       }
     }
+  }
+  // split-K clusters, and whole-tile launches with at most one CTA per SM,
+  // get the whole SM's shared memory for a deeper ring
+  if (S > 1 || n_tiles <= ctx->num_sms) {
+    stages = cl_stages;
+    smem = cl_smem;
   }
   p->stages = stages;
   p->S = S;
