@@ -76,6 +76,10 @@ typedef struct {
                             tensor-core (tcgen05) path when the shape allows
                             it (bf16, head_dim 128, H % 128 == 0, F and
                             n_q*head_dim % 64 == 0, B <= 256); 0 = 5       */
+  int persistent_max_batch; /* batches of 1 .. this many requests run all K
+                            draft steps in one persistent cooperative kernel
+                            (bf16, head_dim 128); 0 = 4, negative = never;
+                            capped at 4 and at max_batch                    */
 } mtp_config;
 
 /* Borrowed head weights (device pointers, layouts [out, in] row-major).
@@ -137,8 +141,15 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
  *   logits    [B, K, V] float32 out, or NULL.
  *   hidden_out[B, H] float32 out (decoder output of step K), or NULL.
  * Host errors: ctx without weights, B outside 1..max_batch, K outside
- * 1..max_k, NULL required pointers.  Device errors: pending != 0, a slot
- * beyond the block table or pool, a position beyond max_pos. */
+ * 1..max_k, NULL required pointers.  Device errors (MTP_ERR_DEVICE_ARGS,
+ * MTP_ERR_CAPACITY; read with mtp_get_device_error): pending != 0 on entry
+ * -- that request's cache and pending are then left untouched at every step
+ * --, a slot beyond the block table or pool, a position beyond max_pos (that
+ * write is skipped).  Batches of 1..persistent_max_batch run in one
+ * cooperative launch that holds every SM of the device; its waits give up
+ * after 2 s with MTP_ERR_TIMEOUT, and the context then refuses further
+ * persistent drafts (they return at once with the same error) until
+ * mtp_get_device_error has read it. */
 mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, const void* embeds,
                      const int32_t* positions, const mtp_kv* kv, int K, const int32_t* chain_ids,
                      int32_t* draft_ids, float* logits, float* hidden_out);
@@ -232,7 +243,8 @@ typedef enum {
   MTP_KERNEL_LM_HEAD = 6,
   MTP_KERNEL_VERIFY = 7,
   MTP_KERNEL_KV_EDIT = 8,
-  MTP_KERNEL_COUNT = 9
+  MTP_KERNEL_DRAFT_PERSISTENT = 9, /* all K steps of one small-batch draft call */
+  MTP_KERNEL_COUNT = 10
 } mtp_kernel_id;
 
 /* Start recording CUDA events around every launch of kernel `kernel` (up to

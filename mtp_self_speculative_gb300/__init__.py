@@ -20,7 +20,7 @@ from ._lib import (  # noqa: F401
     KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
     MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
     MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
-    MTP_KERNEL_VERIFY, MTP_OK, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
+    MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
 )
 
 _clib = L.load()
@@ -96,10 +96,11 @@ class Context:
 
 
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps=1e-6, rope_theta=1e6, dtype="bf16",
-                max_batch=1, max_k=5, block_size=16, max_pos=32768, tc_min_batch=0) -> MTPConfig:
+                max_batch=1, max_k=5, block_size=16, max_pos=32768, tc_min_batch=0,
+                persistent_max_batch=0) -> MTPConfig:
     code = MTP_DTYPE_BF16 if dtype in ("bf16", MTP_DTYPE_BF16, torch.bfloat16) else MTP_DTYPE_F32
     return MTPConfig(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps, rope_theta, code, max_batch, max_k,
-                     block_size, max_pos, tc_min_batch)
+                     block_size, max_pos, tc_min_batch, persistent_max_batch)
 
 
 def mtp_init(cfg: MTPConfig, weights: Optional[Dict[str, torch.Tensor]] = None, device: Optional[int] = None

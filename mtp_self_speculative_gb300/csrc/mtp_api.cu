@@ -134,6 +134,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   const size_t o_lmk = take(maxB * 8), o_lmc = take(4);
   const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(maxB * 4);
   const size_t o_err = take(4);
+  const size_t o_bad = take(maxB * 4);
   const size_t o_rope = take(rope_n * sizeof(float2));
   ctx->ws_bytes = off;
   if (cudaMalloc(&ctx->ws, off) != cudaSuccess) {
@@ -155,6 +156,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->ver_keys = (unsigned long long*)(base + o_vk);
   ctx->ver_cnt = (int*)(base + o_vc);
   ctx->err = (int*)(base + o_err);
+  ctx->req_bad = (int*)(base + o_bad);
   ctx->rope = (float2*)(base + o_rope);
   cudaError_t e = cudaMemset(ctx->ws, 0, off);
   if (e == cudaSuccess && rope_n) {
@@ -199,6 +201,38 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     ctx->tc_attn = (uint16_t*)(tb + t_at);
     ctx->tc_act = (uint16_t*)(tb + t_act);
   }
+  // persistent draft kernel workspace: attention records, counters, argmax
+  // keys and the grid-barrier words
+  ctx->p_max_batch = c.persistent_max_batch < 0 ? 0 : (c.persistent_max_batch == 0 ? 4 : c.persistent_max_batch);
+  if (ctx->p_max_batch > 4) ctx->p_max_batch = 4;
+  if (ctx->p_max_batch > c.max_batch) ctx->p_max_batch = c.max_batch;
+  if (!(with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128)) ctx->p_max_batch = 0;
+  if (ctx->p_max_batch > 0) {
+    const size_t pb = (size_t)ctx->p_max_batch;
+    size_t o3 = 0;
+    auto take3 = [&](size_t bytes) {
+      const size_t o = o3;
+      o3 = align_up(o3 + bytes, 256);
+      return o;
+    };
+    const size_t p_rec = take3(pb * c.n_q_heads * (size_t)sms * 132 * 4);
+    const size_t p_cnt = take3(pb * c.n_kv_heads * 4);
+    const size_t p_keys = take3((size_t)c.max_k * pb * 8);
+    const size_t p_bar = take3(384);
+    if (cudaMalloc(&ctx->p_ws, o3) != cudaSuccess || cudaMemset(ctx->p_ws, 0, o3) != cudaSuccess) {
+      cudaGetLastError();
+      if (ctx->p_ws) cudaFree(ctx->p_ws);
+      if (ctx->tc_ws) cudaFree(ctx->tc_ws);
+      cudaFree(ctx->ws);
+      free(ctx);
+      return MTP_ERR_OOM;
+    }
+    char* pbase = (char*)ctx->p_ws;
+    ctx->p_rec = (float*)(pbase + p_rec);
+    ctx->p_seg_cnt = (int*)(pbase + p_cnt);
+    ctx->p_keys = (unsigned long long*)(pbase + p_keys);
+    ctx->p_gbar = (unsigned long long*)(pbase + p_bar);
+  }
   *out = ctx;
   return MTP_OK;
 }
@@ -212,6 +246,7 @@ void mtp_destroy(mtp_ctx* ctx) {
   }
   cudaFree(ctx->ws);
   if (ctx->tc_ws) cudaFree(ctx->tc_ws);
+  if (ctx->p_ws) cudaFree(ctx->p_ws);
   free(ctx->tc_plan_cache);
   free(ctx->attn_map_cache);
   free(ctx);
@@ -238,6 +273,9 @@ mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, cons
   if (!hidden || !embeds || !positions || !draft_ids || !kv_ok(kv)) return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (persistent_supported(ctx, B))
+    return after_launch(launch_draft_persistent(ctx, s, B, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
+                                                logits, hidden_out));
   const bool tc = tc_supported(ctx, B);
   for (int k = 1; k <= K; ++k) {
     cudaError_t e = tc ? launch_draft_step_tc(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
@@ -293,6 +331,9 @@ mtp_status mtp_get_device_error(mtp_ctx* ctx) {
   int word = 0;
   if (cudaMemcpy(&word, ctx->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return MTP_ERR_CUDA;
   if (word && cudaMemset(ctx->err, 0, 4) != cudaSuccess) return MTP_ERR_CUDA;
+  // a persistent draft call that gave up leaves its grid-barrier words
+  // (arrivals, abort flag) inconsistent: start them afresh
+  if (word == MTP_ERR_TIMEOUT && ctx->p_gbar && cudaMemset(ctx->p_gbar, 0, 384) != cudaSuccess) return MTP_ERR_CUDA;
   return (mtp_status)word;
 }
 

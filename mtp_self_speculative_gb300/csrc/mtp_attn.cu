@@ -23,6 +23,7 @@
 #include <string.h>
 
 #include "mtp_common.cuh"
+#include "mtp_attn_mma.cuh"
 
 namespace mtp {
 
@@ -353,52 +354,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
 // ------------------------------------------------ tensor-core attention
 //
 // bf16 cache, head_dim 128.  Same split-KV grid and per-warp block ownership
-// as above, but the arithmetic runs on mma.sync m16n8k16 (bf16 in, fp32
-// accumulate) with the G query heads of the group on the M dimension (rows
-// G..15 are zero padding):
-//   S^T[16 x 16 tokens] = Q[16 x 128] . K^T   -- 2 n-tiles x 8 k-steps
-//   O[16 x 128]        += P[16 x 16] . V      -- 16 n-tiles, k = 16 tokens
-// K and V tiles are staged by 2-D tensor-map loads with 128-byte swizzle (two
-// 64-dim halves per tile), so the ldmatrix reads of 8 token rows hit distinct
-// banks.  The S accumulators of the two token n-tiles are exactly the A
-// fragment of P, so P never leaves registers.
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return (uint32_t)f32_to_bf16_rne(lo) | ((uint32_t)f32_to_bf16_rne(hi) << 16);
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// Shared-memory address of 16-byte chunk c (0..15 over 128 dims) of token row
-// `row` (0..15) in a tile stored as two 2 KB swizzled halves.
-__device__ __forceinline__ uint32_t sw_chunk(uint32_t tile, int row, int c) {
-  return tile + (uint32_t)((c >> 3) * 2048 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_addr(dst)),
-      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
+// as above; each block's arithmetic is attn_tile_mma (mma.sync m16n8k16 with
+// the group's query heads on M, P kept in registers) on K/V tiles staged by
+// swizzled 2-D tensor-map loads.
 
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads, 2)
@@ -427,22 +385,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int blk1 = min(nblk, blk0 + a.bps);
   const int nsplit = (nblk + a.bps - 1) / a.bps;
 
-  // Q fragments (A operand): row gi = head gi of the group; rows >= G and
-  // rows 8..15 are zero.  Scaled for base-2 softmax.
   uint32_t qa[8][4];
-  {
-    const float* qh = a.q + (size_t)b * a.n_q * HD + (size_t)(g * G + gi) * HD;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      if (gi < G) {
-        qa[kk][0] = pack_bf16(qh[16 * kk + 2 * ti] * a.qscale, qh[16 * kk + 2 * ti + 1] * a.qscale);
-        qa[kk][2] = pack_bf16(qh[16 * kk + 8 + 2 * ti] * a.qscale, qh[16 * kk + 8 + 2 * ti + 1] * a.qscale);
-      } else {
-        qa[kk][0] = qa[kk][2] = 0u;
-      }
-      qa[kk][1] = qa[kk][3] = 0u;
-    }
-  }
+  load_q_frags(qa, a.q + (size_t)b * a.n_q * HD + (size_t)(g * G) * HD, a.qscale, lane, G);
   float o[16][4];
 #pragma unroll
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
@@ -459,14 +403,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   };
   auto issue = [&](int it, int bi) {
     const int st = it % kStages;
-    unsigned char* dst = my_stage + (size_t)st * 2 * TILE_BYTES;
-    const int row = tile_row(bi);
-    mbar_expect_tx(&bars[warp][st], 2 * TILE_BYTES);
-    tma_2d(dst, &kmap, 0, row, &bars[warp][st]);
-    tma_2d(dst + 2048, &kmap, 64, row, &bars[warp][st]);
-    tma_2d(dst + TILE_BYTES, &vmap, 0, row, &bars[warp][st]);
-    tma_2d(dst + TILE_BYTES + 2048, &vmap, 64, row, &bars[warp][st]);
+    tma_kv_tile(my_stage + (size_t)st * 2 * TILE_BYTES, &kmap, &vmap, tile_row(bi), &bars[warp][st]);
   };
+
   const int first = blk0 + warp;
   const int count = (first < blk1) ? (blk1 - first + kAttnWarps - 1) / kAttnWarps : 0;
   if (lane == 0)
@@ -486,67 +425,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     const uint32_t vt = kt + TILE_BYTES;
     const int tok0 = (first + it * kAttnWarps) * 16;
 
-    // S^T = Q K^T: n-tile j covers tokens 8j..8j+7
-    float sc[2][4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 8; kk += 2) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int c = 2 * (kk + (mi >> 1)) + (mi & 1);
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(sw_chunk(kt, 8 * j + ri, c), r0, r1, r2, r3);
-        mma_bf16(sc[j], qa[kk], r0, r1);
-        mma_bf16(sc[j], qa[kk + 1], r2, r3);
-      }
-    }
-    // online softmax on row gi (tokens 2ti, 2ti+1 of each n-tile); rows 8..15 are padding
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int tok = tok0 + 8 * j + 2 * ti + e;
-        if (tok >= T_len) sc[j][e] = -INFINITY;
-        mx = fmaxf(mx, sc[j][e]);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float corr = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - m_new);
-    float p[2][2], rs = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        p[j][e] = (sc[j][e] == -INFINITY) ? 0.0f : exp2f(sc[j][e] - m_new);
-        rs += p[j][e];
-      }
-    rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-    rs += __shfl_xor_sync(0xffffffffu, rs, 2);
-    l_run = l_run * corr + rs;
-    m_run = m_new;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= corr;
-      o[n][1] *= corr;
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16(p[0][0], p[0][1]);
-    pa[1] = 0u;
-    pa[2] = pack_bf16(p[1][0], p[1][1]);
-    pa[3] = 0u;
-    // O += P V: n-tile n covers dims 8n..8n+7
-#pragma unroll
-    for (int c = 0; c < 16; c += 2) {
-      const int mi = lane >> 3, ri = lane & 7;
-      const int tok = 8 * (mi & 1) + ri;
-      uint32_t r0, r1, r2, r3;
-      ldsm_x4_t(sw_chunk(vt, tok, c + (mi >> 1)), r0, r1, r2, r3);
-      mma_bf16(o[c], pa, r0, r1);
-      mma_bf16(o[c + 1], pa, r2, r3);
-    }
+    attn_tile_mma(kt, vt, qa, o, m_run, l_run, tok0, T_len, lane);
     __syncwarp();
     if (lane == 0 && it + kStages < count) issue(it + kStages, first + (it + kStages) * kAttnWarps);
     __syncwarp();
@@ -605,6 +484,29 @@ struct AttnMapCache {
   int num_blocks;
 };
 
+bool attn_tensor_maps(mtp_ctx* ctx, const mtp_kv* kv, const CUtensorMap** km, const CUtensorMap** vm) {
+  // re-encoded only when the pools change
+  if (!ctx->attn_map_cache) {
+    ctx->attn_map_cache = aligned_alloc(64, sizeof(AttnMapCache));
+    if (!ctx->attn_map_cache) return false;
+    memset(ctx->attn_map_cache, 0, sizeof(AttnMapCache));
+  }
+  AttnMapCache* mc = (AttnMapCache*)ctx->attn_map_cache;
+  if (mc->k_pool != kv->k_pool || mc->v_pool != kv->v_pool || mc->num_blocks != kv->num_blocks) {
+    const uint64_t rows = (uint64_t)kv->num_blocks * ctx->cfg.n_kv_heads * 16;
+    if (!make_map(&mc->km, kv->k_pool, rows, 128, 16) || !make_map(&mc->vm, kv->v_pool, rows, 128, 16)) {
+      mc->k_pool = mc->v_pool = nullptr;
+      return false;
+    }
+    mc->k_pool = kv->k_pool;
+    mc->v_pool = kv->v_pool;
+    mc->num_blocks = kv->num_blocks;
+  }
+  *km = &mc->km;
+  *vm = &mc->vm;
+  return true;
+}
+
 template <typename T>
 static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv) {
   const mtp_config& c = ctx->cfg;
@@ -623,25 +525,10 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
   a.max_splits = splits;  // partial-buffer stride of this call
   a.qscale = 1.4426950408889634f / sqrtf((float)c.head_dim);
   if (use_mma) {
-    // tensor maps of the pools, re-encoded only when the pools change
-    if (!ctx->attn_map_cache) {
-      ctx->attn_map_cache = aligned_alloc(64, sizeof(AttnMapCache));
-      if (!ctx->attn_map_cache) return cudaErrorMemoryAllocation;
-      memset(ctx->attn_map_cache, 0, sizeof(AttnMapCache));
-    }
-    AttnMapCache* mc = (AttnMapCache*)ctx->attn_map_cache;
-    if (mc->k_pool != kv->k_pool || mc->v_pool != kv->v_pool || mc->num_blocks != kv->num_blocks) {
-      const uint64_t rows = (uint64_t)kv->num_blocks * c.n_kv_heads * 16;
-      if (!make_map(&mc->km, kv->k_pool, rows, 128, 16) || !make_map(&mc->vm, kv->v_pool, rows, 128, 16)) {
-        mc->k_pool = mc->v_pool = nullptr;
-        return cudaErrorInvalidValue;
-      }
-      mc->k_pool = kv->k_pool;
-      mc->v_pool = kv->v_pool;
-      mc->num_blocks = kv->num_blocks;
-    }
-    const CUtensorMap& km = mc->km;
-    const CUtensorMap& vm = mc->vm;
+    const CUtensorMap *kmp, *vmp;
+    if (!attn_tensor_maps(ctx, kv, &kmp, &vmp)) return cudaErrorInvalidValue;
+    const CUtensorMap& km = *kmp;
+    const CUtensorMap& vm = *vmp;
     const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
     const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096;
     dim3 grid(splits, c.n_kv_heads, B);

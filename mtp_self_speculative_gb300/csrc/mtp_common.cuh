@@ -167,6 +167,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// L2 policy for data read exactly once (streamed weights): evict first, so
+// that the stream does not push out small data that is read again (norm
+// weights, activations, the KV cache, block tables).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 }  // namespace mtp
 
 // ------------------------------------------------------------ host context
@@ -196,6 +214,7 @@ struct mtp_ctx {
   unsigned long long* ver_keys; // [maxB, max_k + 1]
   int* ver_cnt;                 // [maxB]
   int* err;                     // [1]
+  int* req_bad;                 // [maxB] 1: pending was not 0 when the draft call began
   float2* rope;                 // [max_pos, head_dim / 2] (cos, sin)
   // tensor-core path (allocated when the shape allows it)
   void* tc_ws;
@@ -216,6 +235,16 @@ struct mtp_ctx {
   // small-batch projections: bit k set = kernel kind k streams its weights
   // through shared memory with bulk copies (else register streaming)
   int gemv_stream_mask;
+  // persistent draft kernel (batches 1..p_max_batch; 0 = off)
+  int p_max_batch;
+  void* p_ws;
+  float* p_rec;                  // [p_max_batch * n_kv, num_sms, G, 132] attention records
+  int* p_seg_cnt;                // [p_max_batch * n_kv]
+  unsigned long long* p_keys;    // [max_k, p_max_batch]
+  unsigned long long* p_gbar;    // grid barrier: arrivals, completed barriers, abort flag (128 B apart)
+  int p_nslots[3];               // launch plan per batch width 1, 2, 4 (0 = not yet made)
+  int p_warps[3];
+  size_t p_smem[3];
 };
 
 namespace mtp {
@@ -250,6 +279,14 @@ cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K,
                               const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
 cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv);
 bool tc_supported(const mtp_ctx* ctx, int B);
+bool persistent_supported(const mtp_ctx* ctx, int B);
+cudaError_t launch_draft_persistent(mtp_ctx* ctx, cudaStream_t s, int B, int K, const void* hidden,
+                                    const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                                    const int32_t* chain_ids, int32_t* draft_ids, float* logits,
+                                    float* hidden_out);
+// Swizzled [16 x 64] tensor maps over the K and V pools (head_dim 128),
+// cached in the context; false if they cannot be encoded.
+bool attn_tensor_maps(mtp_ctx* ctx, const mtp_kv* kv, const CUtensorMap** km, const CUtensorMap** vm);
 // 2-D bf16 tensor map over [rows, cols] (row-major) with a [box_rows, 64]
 // box and 128-byte swizzle; false if the driver rejects it.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);

@@ -53,6 +53,7 @@ struct StepArgs {
   unsigned long long* lm_keys;
   int* lm_cnt;
   int* err;
+  int* req_bad;
   const float2* rope;
 };
 
@@ -227,7 +228,7 @@ __device__ __forceinline__ void epilogue(const StepArgs<T>& a, int b, int r0, in
       qb[r1] = v1 * cs.x + v0 * cs.y;
       return;
     }
-    if (a.pending[b] != a.k - 1) {
+    if (__ldcg(a.req_bad + b) || a.pending[b] != a.k - 1) {
       set_error(a.err, MTP_ERR_DEVICE_ARGS);
       return;
     }
@@ -286,6 +287,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
     }
   }
   pdl_wait();
+  if (KIND == EH_PROJ && a.k == 1 && blockIdx.x == 0)
+    for (int b = threadIdx.x; b < a.B; b += kThreads) a.req_bad[b] = (a.pending[b] != 0);
 
   for (int b0 = 0; b0 < a.B; b0 += NB) {
     const int nb = min(NB, a.B - b0);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
       for (int b = threadIdx.x; b < a.B; b += kThreads) {
         const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
         a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-        a.pending[b] = a.k;
+        if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
       }
       if (threadIdx.x == 0) atomicExch(a.lm_cnt, 0);
     }
@@ -514,6 +517,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 
   // consumers
   pdl_wait();
+  if (KIND == EH_PROJ && a.k == 1 && blockIdx.x == 0)
+    for (int b = threadIdx.x - 32; b < a.B; b += 32 * kTmaConsumers) a.req_bad[b] = (a.pending[b] != 0);
   const int nb = a.B;  // launched only for B <= NB
   cons_stage_inputs<T, KIND>(a, xs, C, nb, red);
   const int cw = warp - 1;
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
       for (int b = ct; b < a.B; b += 256) {
         const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
         a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-        a.pending[b] = a.k;
+        if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
       }
       if (ct == 0) atomicExch(a.lm_cnt, 0);
     }
@@ -694,6 +699,7 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
   a.seq_len = kv->seq_len; a.pending = kv->pending;
   a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.attn = ctx->attn; a.h1 = ctx->h1; a.act = ctx->act;
   a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt; a.err = ctx->err; a.rope = ctx->rope;
+  a.req_bad = ctx->req_bad;
 
   cudaError_t e;
   if ((e = launch_kind<T, EH_PROJ>(ctx, s, a)) != cudaSuccess) return e;

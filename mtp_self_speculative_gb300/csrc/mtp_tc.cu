@@ -81,6 +81,7 @@ struct TcArgs {
   unsigned long long* lm_keys;
   int* lm_cnt;
   int* err;
+  int* req_bad;
   const float2* rope;
 };
 
@@ -166,7 +167,7 @@ __device__ void qkv_meta_fill(const TcArgs& a, QkvMeta* meta, int tid, int nthre
     }
     meta->pos[b] = pos;
     long long kvoff = -1;
-    if (a.pending[b] != a.k - 1) {
+    if (__ldcg(a.req_bad + b) || a.pending[b] != a.k - 1) {
       set_error(a.err, MTP_ERR_DEVICE_ARGS);
     } else {
       const int slot = a.seq_len[b] + a.k - 1;
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         for (int b = epi_tid; b < a.B; b += kTcEpiThreads) {
           const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
           a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-          a.pending[b] = a.k;
+          if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
         }
         if (epi_tid == 0) atomicExch(a.lm_cnt, 0);
       }
@@ -574,6 +575,8 @@ struct PrepEhArgs {
   float eps;
   uint16_t* out;  // [B, 2H]
   int* err;
+  const int32_t* pending;
+  int* req_bad;   // written at step 1: pending was not 0 on entry
 };
 
 
@@ -636,6 +639,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_eh_kernel(const PrepEhArgs 
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x;
+  if (a.k == 1 && threadIdx.x == 0) a.req_bad[b] = (a.pending[b] != 0);
   uint16_t* out = a.out + (size_t)b * 2 * a.H;
   // hidden half: step 1 reads the caller's bf16 state, later steps the fp32 recursion
   if (a.k == 1) prep_row(nullptr, a.hidden_in + (size_t)b * a.H, a.w_h, out, a.H, a.eps, red);
@@ -835,7 +839,7 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   a.seq_len = kv->seq_len; a.pending = kv->pending;
   a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.h1 = ctx->h1; a.act_bf16 = ctx->tc_act;
   a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt;
-  a.err = ctx->err; a.rope = ctx->rope;
+  a.err = ctx->err; a.rope = ctx->rope; a.req_bad = ctx->req_bad;
   a.stages = pl->stages;
   a.ksplit = pl->S;
   const int kid = (kind == TC_EH) ? MTP_KERNEL_EH_PROJ : (kind == TC_QKV) ? MTP_KERNEL_QKV_ROPE
@@ -878,7 +882,7 @@ cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int
   pa.hidden_in = (const uint16_t*)hidden; pa.embeds_in = (const uint16_t*)embeds; pa.hid = ctx->hid;
   pa.chain_ids = chain_ids; pa.draft_ids = draft_ids; pa.embed = (const uint16_t*)ctx->w.embed;
   pa.w_h = (const uint16_t*)ctx->w.w_norm_h; pa.w_e = (const uint16_t*)ctx->w.w_norm_e; pa.eps = c.eps;
-  pa.out = ctx->tc_xin_eh; pa.err = ctx->err;
+  pa.out = ctx->tc_xin_eh; pa.err = ctx->err; pa.pending = kv->pending; pa.req_bad = ctx->req_bad;
   ctx->launches++;
   if ((e = launch_pdl(prep_eh_kernel, dim3(B), dim3(kPrepThreads), 0, s, pa)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_EH, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;

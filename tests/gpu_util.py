@@ -42,11 +42,12 @@ def download_kv(kvd) -> synth.KVState:
                          host(kvd.pending))
 
 
-def make_context(cfg: synth.MTPShape, wdev=None, max_batch=None, max_k=None, max_pos=None, tc_min_batch=0):
+def make_context(cfg: synth.MTPShape, wdev=None, max_batch=None, max_k=None, max_pos=None, tc_min_batch=0,
+                 persistent_max_batch=0):
     import mtp_self_speculative_gb300 as M
     c = M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps, cfg.rope_theta,
                       cfg.dtype, max_batch or cfg.batch, max_k or cfg.K, cfg.block_size,
-                      max_pos or (cfg.ctx_hi + 64), tc_min_batch)
+                      max_pos or (cfg.ctx_hi + 64), tc_min_batch, persistent_max_batch)
     return M.mtp_init(c, wdev)
 
 

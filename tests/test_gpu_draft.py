@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 class Case:
-    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77, tc_min_batch=0):
+    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77, tc_min_batch=0, persistent_max_batch=0):
         self.cfg = cfg
         self.K = K or cfg.K
         self.w = synth.make_weights(cfg, norm=norm)
@@ -30,7 +30,8 @@ class Case:
         self.chain = synth.uniform_int(cfg.seed, chain_stream, (self.B, max(self.K - 1, 1)), 0, cfg.vocab)
         self.wdev = upload_weights(self.w)
         self.ctx = make_context(cfg, self.wdev, max_batch=self.B, max_k=self.K,
-                                max_pos=int(self.lens.max()) + self.K + 8, tc_min_batch=tc_min_batch)
+                                max_pos=int(self.lens.max()) + self.K + 8, tc_min_batch=tc_min_batch,
+                                persistent_max_batch=persistent_max_batch)
         self.inputs = (dev(self.di.hidden), dev(self.di.embeds), dev(self.di.positions))
 
     def gpu_draft(self, forced=True, kvd=None):
@@ -148,15 +149,32 @@ def test_ragged_bf16_block_edges(path):
     check_free(case, list(range(7)), ids, logits, LOGIT_TOL)
 
 
-@pytest.mark.parametrize("lens", [[33], [0, 17], [5, 16, 40]])
-def test_small_batch_bf16_tma_streamed(lens):
-    """bf16 batches of 1..3: the TMA-streamed CUDA-core kernels (1, 2 and 4
-    batch rows per pass)."""
+@pytest.mark.parametrize("path", ["streamed", "persistent"])
+@pytest.mark.parametrize("lens", [[33], [0, 17], [5, 16, 40], [1, 30, 2, 64]])
+def test_small_batch_bf16(lens, path):
+    """bf16 batches of 1..4 on both small-batch paths: the per-step
+    TMA-streamed CUDA-core kernels (1, 2 and 4 batch rows per pass) and the
+    persistent kernel that runs all K steps in one cooperative launch."""
     cfg = synth.MTPShape("small_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=len(lens), K=3,
                          dtype="bf16", ctx_lo=0, ctx_hi=64, paged_shuffle=True, seed_index=53)
-    case = Case(cfg, norm="random", lens=lens)
+    case = Case(cfg, norm="random", lens=lens, persistent_max_batch=-1 if path == "streamed" else 4)
     _, _, ids, logits = check_forced(case, list(range(len(lens))), LOGIT_TOL)
     check_free(case, list(range(len(lens))), ids, logits, LOGIT_TOL)
+    ids2, logits2, _, _ = case.gpu_draft(forced=True)
+    np.testing.assert_array_equal(ids2, ids)
+    np.testing.assert_array_equal(logits2, logits)
+
+
+@pytest.mark.parametrize("path", ["streamed", "persistent"])
+def test_small_batch_multi_chunk_rows(path):
+    """Rows wider than one 4096-column chunk in every projection (H = 4608,
+    q_dim = 6144, F = 9216: RMSNorm statistics over several chunks, partial
+    sums carried across chunks), 8 query heads per kv head, K = 3, B = 2."""
+    cfg = synth.MTPShape("wide_bf16", H=4608, n_q=48, n_kv=6, head_dim=128, ffn=9216, vocab=20001, batch=2, K=3,
+                         dtype="bf16", ctx_lo=1, ctx_hi=200, paged_shuffle=True, seed_index=54)
+    case = Case(cfg, norm="random", lens=[200, 37], persistent_max_batch=-1 if path == "streamed" else 4)
+    _, _, ids, logits = check_forced(case, [0, 1], LOGIT_TOL)
+    check_free(case, [0, 1], ids, logits, LOGIT_TOL)
 
 
 def test_tensor_core_path_batch_40_gqa8():
@@ -179,6 +197,38 @@ def test_gqa_eight_heads_per_kv_head_f32():
     check_forced(case, [0, 1, 2], F32_LOGIT_TOL)
 
 
+@pytest.mark.parametrize("path", ["streamed", "persistent", "tensor_cores"])
+def test_device_errors_bf16(path):
+    """pending != 0 on entry and a block table that is too short are reported
+    through the error word; the request's cache is left untouched at every
+    step (a request that starts with pending != 0 is never appended to), and
+    the context drafts correctly afterwards."""
+    import mtp_self_speculative_gb300 as M
+    cfg = synth.MTPShape("err_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=5003, batch=2, K=3,
+                         dtype="bf16", ctx_lo=150, ctx_hi=200, seed_index=55)
+    case = Case(cfg, norm="random", persistent_max_batch=4 if path == "persistent" else -1,
+                tc_min_batch=1 if path == "tensor_cores" else 1 << 20)
+    ids = torch.empty((2, 3), dtype=torch.int32, device="cuda")
+    kv = case.kv0.copy()
+    kv.pending[:] = 1
+    kvd = upload_kv(kv)
+    M.mtp_draft(case.ctx, *case.inputs, kvd, 3, ids)
+    assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_DEVICE_ARGS
+    got = download_kv(kvd)
+    np.testing.assert_array_equal(got.k_pool, kv.k_pool)
+    np.testing.assert_array_equal(got.v_pool, kv.v_pool)
+    np.testing.assert_array_equal(got.pending, kv.pending)
+    kv = case.kv0.copy()
+    kv.block_table = kv.block_table[:, :8].copy()      # room for 128 slots only
+    kvd = upload_kv(kv)
+    M.mtp_draft(case.ctx, *case.inputs, kvd, 3, ids)
+    assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_CAPACITY
+    got = download_kv(kvd)
+    np.testing.assert_array_equal(got.k_pool, kv.k_pool)
+    # the context still drafts correctly afterwards
+    check_forced(case, [0, 1], LOGIT_TOL)
+
+
 def test_device_errors_leave_no_fault():
     """pending != 0 on entry and a block table too short are reported through
     the error word; the writes are skipped."""
@@ -191,6 +241,9 @@ def test_device_errors_leave_no_fault():
     ids = torch.empty((1, 3), dtype=torch.int32, device="cuda")
     M.mtp_draft(case.ctx, *case.inputs, kvd, 3, ids)
     assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_DEVICE_ARGS
+    got = download_kv(kvd)
+    np.testing.assert_array_equal(got.k_pool, kv.k_pool)
+    np.testing.assert_array_equal(got.pending, kv.pending)
     kv = case.kv0.copy()
     kv.block_table = kv.block_table[:, :8].copy()      # room for 128 slots only
     kvd = upload_kv(kv)
