@@ -238,7 +238,7 @@ def gpu_id_for_smi(local_rank: int) -> str:
 class Workload:
     """Device-resident inputs and outputs of one draft+verify step."""
 
-    def __init__(self, cfg: synth.MTPShape, K: int):
+    def __init__(self, cfg: synth.MTPShape, K: int, persistent_max_batch: int = 0):
         import torch
         import mtp_self_speculative_gb300 as M
         self.cfg, self.K = cfg, K
@@ -258,7 +258,8 @@ class Workload:
         self.wdev = {k: dev(v) for k, v in self.w.items()}
         self.ctx = M.mtp_init(M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps,
                                             cfg.rope_theta, cfg.dtype, B, K, cfg.block_size,
-                                            int(self.lens.max()) + K + 8), self.wdev)
+                                            int(self.lens.max()) + K + 8,
+                                            persistent_max_batch=persistent_max_batch), self.wdev)
         self.kv = M.KVCache(dev(self.kv0.k_pool), dev(self.kv0.v_pool), dev(self.kv0.block_table),
                             dev(self.kv0.seq_len), dev(self.kv0.pending))
         self.L0 = dev(self.lens.astype(np.int32))
@@ -314,7 +315,7 @@ def run_ours(args, rank, world, local_rank):
     if cfg.H == 0:
         raise SystemExit("workload %s has no draft head; pick a draft workload" % cfg.name)
     K = cfg.K
-    wl = Workload(cfg, K)
+    wl = Workload(cfg, K, args.persistent_max_batch)
     stream = torch.cuda.current_stream()
 
     # bandwidth yardstick in the same run: 1 GiB device-to-device copy
@@ -583,6 +584,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--persistent-max-batch", type=int, default=0,
+                    help="largest batch for the persistent draft kernel (0: never, the library default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")

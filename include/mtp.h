@@ -78,8 +78,9 @@ typedef struct {
                             n_q*head_dim % 64 == 0, B <= 256); 0 = 5       */
   int persistent_max_batch; /* batches of 1 .. this many requests run all K
                             draft steps in one persistent cooperative kernel
-                            (bf16, head_dim 128); 0 = 4, negative = never;
-                            capped at 4 and at max_batch                    */
+                            (bf16, head_dim 128) instead of the per-step
+                            streamed kernels; 0 or negative = never (the
+                            default); capped at 4 and at max_batch          */
 } mtp_config;
 
 /* Borrowed head weights (device pointers, layouts [out, in] row-major).

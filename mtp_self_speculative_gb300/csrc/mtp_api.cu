@@ -104,6 +104,19 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // overrides the default for tuning.
   ctx->gemv_stream_mask = 0x3F;
   if (const char* env = getenv("MTP_GEMV_STREAM")) ctx->gemv_stream_mask = (int)strtol(env, nullptr, 0);
+  // Shared-memory budget of the streamed kernel per kind, in KB;
+  // MTP_GEMV_BUDGET ("eh,qkv,o,gu,down,lm") overrides it for tuning.
+  for (int i = 0; i < 6; ++i) ctx->gemv_budget_kb[i] = 220;
+  if (const char* env = getenv("MTP_GEMV_BUDGET")) {
+    const char* q = env;
+    for (int i = 0; i < 6 && *q; ++i) {
+      char* end = nullptr;
+      const long v = strtol(q, &end, 10);
+      if (end == q) break;
+      if (v >= 32 && v <= 220) ctx->gemv_budget_kb[i] = (int)v;
+      q = (*end == ',') ? end + 1 : end;
+    }
+  }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
     free(ctx);
@@ -203,7 +216,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   }
   // persistent draft kernel workspace: attention records, counters, argmax
   // keys and the grid-barrier words
-  ctx->p_max_batch = c.persistent_max_batch < 0 ? 0 : (c.persistent_max_batch == 0 ? 4 : c.persistent_max_batch);
+  ctx->p_max_batch = c.persistent_max_batch > 0 ? c.persistent_max_batch : 0;
   if (ctx->p_max_batch > 4) ctx->p_max_batch = 4;
   if (ctx->p_max_batch > c.max_batch) ctx->p_max_batch = c.max_batch;
   if (!(with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128)) ctx->p_max_batch = 0;
@@ -371,11 +384,6 @@ mtp_status mtp_profile_begin(mtp_ctx* ctx, int kernel, int capacity) {
 mtp_status mtp_profile_end(mtp_ctx* ctx, float* ms_out, int max_out, int* n_out) {
   if (!ctx || !n_out || (max_out > 0 && !ms_out)) return MTP_ERR_INVALID;
   ctx->prof_kernel = -1;
-  // Which small-batch projection kinds use the bulk-copy streamed kernel
-  // (bit = kind: eh, qkv, o, gate_up, down, lm_head); MTP_GEMV_STREAM
-  // overrides the default for tuning.
-  ctx->gemv_stream_mask = 0x3F;
-  if (const char* env = getenv("MTP_GEMV_STREAM")) ctx->gemv_stream_mask = (int)strtol(env, nullptr, 0);
   const int n = ctx->prof_n;
   *n_out = 0;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;

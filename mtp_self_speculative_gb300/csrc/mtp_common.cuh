@@ -235,6 +235,7 @@ struct mtp_ctx {
   // small-batch projections: bit k set = kernel kind k streams its weights
   // through shared memory with bulk copies (else register streaming)
   int gemv_stream_mask;
+  int gemv_budget_kb[6];         // shared memory per streamed-kernel CTA, per kind
   // persistent draft kernel (batches 1..p_max_batch; 0 = off)
   int p_max_batch;
   void* p_ws;

@@ -398,60 +398,108 @@ constexpr uint32_t kGemvWaitLimit = 1u << 24;
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__device__ __forceinline__ float cons_sum(float v, float* red) {
-  v = warp_sum(v);
-  const int cw = (threadIdx.x >> 5) - 1, l = threadIdx.x & 31;
-  cons_bar();
-  if (l == 0) red[cw] = v;
-  cons_bar();
-  return warp_sum((l < kTmaConsumers) ? red[l] : 0.0f);
+// Eight consecutive values of an fp32 (activations, L2 only) or T row.
+template <typename T, typename S>
+__device__ __forceinline__ void load8_row(const S* p, float (&x)[8]) {
+  if constexpr (sizeof(S) == 4) {
+    const float4 t0 = __ldcg(reinterpret_cast<const float4*>(p));
+    const float4 t1 = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = t0.x; x[1] = t0.y; x[2] = t0.z; x[3] = t0.w; x[4] = t1.x; x[5] = t1.y; x[6] = t1.z; x[7] = t1.w;
+  } else {
+    const uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+    x[0] = bf16_lo(t.x); x[1] = bf16_hi(t.x); x[2] = bf16_lo(t.y); x[3] = bf16_hi(t.y);
+    x[4] = bf16_lo(t.z); x[5] = bf16_hi(t.z); x[6] = bf16_lo(t.w); x[7] = bf16_hi(t.w);
+  }
 }
 
+// Copy n values (fp32 or T; n % 8 == 0) into dst (fp32) times the norm
+// weight w (if any); returns this thread's sum of squares of the raw
+// values.  Source and weight loads are independent and vectorised, so a
+// 4096-wide row costs each consumer thread two groups: about one L2 round
+// trip.
 template <typename T, typename S>
-__device__ __forceinline__ void cons_stage_row(float* dst, const S* src, int n, const T* w, float eps, float* red) {
+__device__ __forceinline__ float cons_stage_raw(float* dst, const S* src, int n, const T* w) {
   const int ct = threadIdx.x - 32;
   float ss = 0.0f;
-  for (int i = ct; i < n; i += 256) {
-    float v;
-    if constexpr (sizeof(S) == 4) v = src[i];
-    else v = Elem<T>::load1(reinterpret_cast<const T*>(src) + i);
-    dst[i] = v;
-    ss = fmaf(v, v, ss);
+#pragma unroll 2
+  for (int i8 = ct; i8 < (n >> 3); i8 += 256) {
+    float x[8], wv[8];
+    load8_row<T, S>(src + (size_t)i8 * 8, x);
+    if (w) load8_row<T, T>(w + (size_t)i8 * 8, wv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ss = fmaf(x[e], x[e], ss);
+      if (w) x[e] *= wv[e];
+    }
+    float4* d = reinterpret_cast<float4*>(dst + (size_t)i8 * 8);
+    d[0] = make_float4(x[0], x[1], x[2], x[3]);
+    d[1] = make_float4(x[4], x[5], x[6], x[7]);
   }
-  if (w == nullptr) return;
-  const float scale = rsqrtf(cons_sum(ss, red) / (float)n + eps);
-  for (int i = ct; i < n; i += 256) dst[i] = dst[i] * scale * Elem<T>::load1(w + i);
+  return ss;
 }
 
+// Stage the normalised input row(s) of all nb requests: one pass that stores
+// x * w and sums x^2 for every vector, one block reduction for all of them,
+// then the scalar RMS factors applied in shared memory.
 template <typename T, int KIND>
 __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
+  constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
+  float ss[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss[i] = 0.0f;
   for (int b = 0; b < nb; ++b) {
     float* dst = xs + (size_t)b * C;
+    float s0 = 0.0f, s1 = 0.0f;
     if constexpr (KIND == EH_PROJ) {
       if (a.k == 1) {
-        cons_stage_row<T, T>(dst, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h, a.eps, red);
-        cons_stage_row<T, T>(dst + a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e, a.eps, red);
+        s0 = cons_stage_raw<T, T>(dst, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h);
+        s1 = cons_stage_raw<T, T>(dst + a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e);
       } else {
-        cons_stage_row<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_h, a.eps, red);
         int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
                              : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+        s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_h);
         if (id < 0 || id >= a.V) {
           if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
           id = 0;
         }
-        cons_stage_row<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e, a.eps, red);
+        s1 = cons_stage_raw<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
       }
     } else if constexpr (KIND == QKV_ROPE) {
-      cons_stage_row<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in, a.eps, red);
+      s0 = cons_stage_raw<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
     } else if constexpr (KIND == O_PROJ) {
-      cons_stage_row<T, float>(dst, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr, a.eps, red);
+      cons_stage_raw<T, float>(dst, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr);
     } else if constexpr (KIND == GATE_UP) {
-      cons_stage_row<T, float>(dst, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post, a.eps, red);
+      s0 = cons_stage_raw<T, float>(dst, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post);
     } else if constexpr (KIND == DOWN) {
-      cons_stage_row<T, float>(dst, a.act + (size_t)b * a.F, a.F, (const T*)nullptr, a.eps, red);
+      cons_stage_raw<T, float>(dst, a.act + (size_t)b * a.F, a.F, (const T*)nullptr);
     } else {
-      cons_stage_row<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_f, a.eps, red);
+      s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_f);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j == b) {
+        ss[2 * j] = s0;
+        ss[2 * j + 1] = s1;
+      }
+  }
+  if constexpr (kNorm) {
+    const int cw = (threadIdx.x >> 5) - 1, l = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float t = warp_sum(ss[i]);
+      if (l == 0 && i < 2 * nb) red[cw * 8 + i] = t;
+    }
+    cons_bar();
+    const int ct = threadIdx.x - 32;
+    const int nvec = (KIND == EH_PROJ) ? 2 : 1;
+    for (int b = 0; b < nb; ++b)
+      for (int v = 0; v < nvec; ++v) {
+        float t = 0.0f;
+        for (int w = 0; w < kTmaConsumers; ++w) t += red[w * 8 + 2 * b + v];
+        const float sc = rsqrtf(t / (float)a.H + a.eps);
+        float* dst = xs + (size_t)b * C + (size_t)v * a.H;
+        for (int i = ct; i < a.H; i += 256) dst[i] *= sc;
+      }
   }
   cons_bar();
 }
@@ -460,7 +508,7 @@ template <typename T, int KIND, int NB>
 __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs<T> a, int stages, int consumers) {
   extern __shared__ __align__(128) unsigned char gsm[];
   __shared__ __align__(8) uint64_t full_bar[kMaxTmaStages], empty_bar[kMaxTmaStages];
-  __shared__ float red[kTmaConsumers];
+  __shared__ float red[kTmaConsumers * 8];
   __shared__ unsigned long long cta_best[kTmaConsumers][NB];
   __shared__ int am_last;
 
@@ -489,6 +537,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // weights are read once per step
       for (int it = 0; it < n; ++it) {
         const int s = it % stages;
         if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)(((it / stages) & 1) ^ 1), kGemvWaitLimit)) {
@@ -501,14 +550,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
         unsigned char* st = gsm + (size_t)s * stage_stride;
         if (w1 == w0 + C) {
           mbar_expect_tx(&full_bar[s], 2 * row_bytes);
-          bulk_g2s(st, w0, 2 * row_bytes, &full_bar[s]);
+          bulk_g2s_hint(st, w0, 2 * row_bytes, &full_bar[s], pol);
         } else if (w1) {
           mbar_expect_tx(&full_bar[s], 2 * row_bytes);
-          bulk_g2s(st, w0, row_bytes, &full_bar[s]);
-          bulk_g2s(st + row_bytes, w1, row_bytes, &full_bar[s]);
+          bulk_g2s_hint(st, w0, row_bytes, &full_bar[s], pol);
+          bulk_g2s_hint(st + row_bytes, w1, row_bytes, &full_bar[s], pol);
         } else {
           mbar_expect_tx(&full_bar[s], row_bytes);
-          bulk_g2s(st, w0, row_bytes, &full_bar[s]);
+          bulk_g2s_hint(st, w0, row_bytes, &full_bar[s], pol);
         }
       }
     }
@@ -626,7 +675,7 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
     const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;
     const size_t stage_stride = ((size_t)2 * C * sizeof(T) + 127) & ~(size_t)127;
     const size_t xs_bytes = (size_t)nbt * C * sizeof(float);
-    const size_t budget = 220 * 1024;
+    const size_t budget = (size_t)ctx->gemv_budget_kb[KIND] * 1024;
     int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;
     if (max_stages > kMaxTmaStages) max_stages = kMaxTmaStages;
     // stages = consumers * k: pick the consumer count (4..8) that keeps the most stages

@@ -256,10 +256,12 @@ def test_device_errors_leave_no_fault():
 # ------------------------------------------------------------- full sizes
 
 @pytest.mark.slow
-def test_qwen3_8b_b1_full_size():
+@pytest.mark.parametrize("path", ["streamed", "persistent"])
+def test_qwen3_8b_b1_full_size(path):
     """Qwen3-8B-shaped head, bf16, B=1, context 4096, K=5 -- the bench's
-    workload and launch configuration."""
-    case = Case(synth.QWEN3_8B_B1)
+    workload and launch configuration (streamed per-step kernels), and the
+    same on the persistent kernel."""
+    case = Case(synth.QWEN3_8B_B1, persistent_max_batch=4 if path == "persistent" else 0)
     worst, exact, ids, logits = check_forced(case, [0], LOGIT_TOL)
     check_free(case, [0], ids, logits, LOGIT_TOL)
 
