@@ -142,7 +142,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   };
   const size_t o_hid = take(maxB * H * 4), o_x = take(maxB * H * 4), o_q = take(maxB * qd * 4);
   const size_t o_attn = take(maxB * qd * 4), o_h1 = take(maxB * H * 4), o_act = take(maxB * F * 4);
-  const size_t o_part = take(part_rows * (c.head_dim + 2) * 4);
+  const size_t o_part = take(part_rows * (c.head_dim + 4) * 4);
   const size_t o_acnt = take(maxB * c.n_kv_heads * 4);
   const size_t o_lmk = take(maxB * 8), o_lmc = take(4);
   const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(maxB * 4);

@@ -37,7 +37,7 @@ struct AttnArgs {
   const float* q;        // [B, n_q * d] rotated queries
   float* out;            // [B, n_q * d]
   uint16_t* out_bf16;    // [B, n_q * d] bf16 copy for the tensor-core O-proj, or null
-  float* part;           // [B, n_q, max_splits, d + 2]
+  float* part;           // [B, n_q, max_splits, d + 4]: max, sum, -, -, o[d]
   int* cnt;              // [B, n_kv]
   int* err;
   const T* k_pool;
@@ -110,9 +110,8 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 
 // Merge the per-warp online-softmax states of this CTA, then either write the
 // output (one split) or a partial (M, L, O) and, in the last CTA of the
-// (request, kv head), combine all splits.  The combine stages each split's
-// (M, L) in shared memory, turns them into weights in parallel, and sums the
-// partial outputs with independent loads.
+// (request, kv head), combine all splits: thread (head, 4 dims) merges the
+// partials online, sixteen partials' loads in flight at a time.
 template <typename T, int HD, int G>
 __device__ __forceinline__ void attn_store_out(const AttnArgs<T>& a, int b, int g, int h, int d, float v) {
   const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
@@ -120,14 +119,14 @@ __device__ __forceinline__ void attn_store_out(const AttnArgs<T>& a, int b, int 
   if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(v);
 }
 
-constexpr int kMaxSplits = 64;
+constexpr int kCombineBatch = 16;
 
 template <typename T, int HD, int G>
 __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, float (*wm)[G], float (*wl)[G], int s,
                                    int g, int b, int nsplit) {
-  __shared__ float cm[G][kMaxSplits], cw[G][kMaxSplits];
+  constexpr int RS = HD + 4;  // partial row stride (16-byte aligned rows)
   __shared__ int am_last;
-  float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * (HD + 2);
+  float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * RS;
   for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
     const int h = idx / HD, d = idx - h * HD;
     float M = -INFINITY;
@@ -143,42 +142,58 @@ __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, floa
     if (nsplit == 1) {
       attn_store_out<T, HD, G>(a, b, g, h, d, O / L);
     } else {
-      float* pp = part_base + ((size_t)h * a.max_splits + s) * (HD + 2);
+      float* pp = part_base + ((size_t)h * a.max_splits + s) * RS;
       if (d == 0) { pp[0] = M; pp[1] = L; }
-      pp[2 + d] = O;
+      pp[4 + d] = O;
     }
   }
   if (nsplit == 1) return;
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) am_last = (atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1) == nsplit - 1);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    am_last = (atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1) == nsplit - 1);
+    if (am_last) __threadfence();
+  }
   __syncthreads();
   if (!am_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < G * nsplit; i += kAttnThreads) {
-    const int h = i / nsplit, j = i - h * nsplit;
-    const float* pj = part_base + ((size_t)h * a.max_splits + j) * (HD + 2);
-    cm[h][j] = __ldcg(pj);
-    cw[h][j] = __ldcg(pj + 1);
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, cm[h][j]);
-    float L = 0.0f;
-    for (int j = 0; j < nsplit; ++j) L += cw[h][j] * exp2f(cm[h][j] - M);
-    const float inv = 1.0f / L;
-    for (int j = 0; j < nsplit; ++j) cw[h][j] = exp2f(cm[h][j] - M) * inv;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
-    const int h = idx / HD, d = idx - h * HD;
-    const float* ph = part_base + (size_t)h * a.max_splits * (HD + 2) + 2 + d;
-    float O = 0.0f;
-#pragma unroll 8
-    for (int j = 0; j < nsplit; ++j) O = fmaf(cw[h][j], __ldcg(ph + (size_t)j * (HD + 2)), O);
-    attn_store_out<T, HD, G>(a, b, g, h, d, O);
+  for (int it = threadIdx.x; it < G * (HD / 4); it += kAttnThreads) {
+    const int h = it / (HD / 4), d4 = it - h * (HD / 4);
+    const float* ph = part_base + (size_t)h * a.max_splits * RS;
+    float Mr = -INFINITY, Lr = 0.0f;
+    float4 Or = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int j0 = 0; j0 < nsplit; j0 += kCombineBatch) {
+      float mj[kCombineBatch], lj[kCombineBatch];
+      float4 oj[kCombineBatch];
+#pragma unroll
+      for (int q = 0; q < kCombineBatch; ++q) {
+        mj[q] = -INFINITY;
+        lj[q] = 0.0f;
+        oj[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (j0 + q < nsplit) {
+          const float* r = ph + (size_t)(j0 + q) * RS;
+          mj[q] = __ldcg(r);
+          lj[q] = __ldcg(r + 1);
+          oj[q] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kCombineBatch; ++q) {
+        if (mj[q] == -INFINITY) continue;
+        const float Mn = fmaxf(Mr, mj[q]);
+        const float co = (Mr == -INFINITY) ? 0.0f : exp2f(Mr - Mn), cn = exp2f(mj[q] - Mn);
+        Lr = Lr * co + lj[q] * cn;
+        Or.x = Or.x * co + oj[q].x * cn;
+        Or.y = Or.y * co + oj[q].y * cn;
+        Or.z = Or.z * co + oj[q].z * cn;
+        Or.w = Or.w * co + oj[q].w * cn;
+        Mr = Mn;
+      }
+    }
+    const float inv = 1.0f / Lr;
+    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 0, Or.x * inv);
+    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 1, Or.y * inv);
+    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 2, Or.z * inv);
+    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 3, Or.w * inv);
   }
   if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
 }
@@ -201,6 +216,20 @@ __device__ __forceinline__ void attn_finish(const AttnArgs<T>& a, unsigned char*
   attn_finish_merged<T, HD, G>(a, wacc, wm, wl, s, g, b, nsplit);
 }
 
+// The CTA's slice of the request's block table, blocks s*bps .. s*bps +
+// bps - 1 (those below max_blocks), into shared memory in one coalesced
+// pass.  No kernel writes the block table, so this runs before the
+// dependency wait; the tiles' copies then need no dependent L2 read each.
+template <typename T>
+__device__ __forceinline__ void load_block_slice(const AttnArgs<T>& a, int* s_bt, int s, int b) {
+  const int blk0 = s * a.bps;
+  const int n = min(a.bps, a.max_blocks - blk0);
+  for (int i = threadIdx.x; i < n; i += kAttnThreads) s_bt[i] = a.block_table[(size_t)b * a.max_blocks + blk0 + i];
+}
+
+// Shared-memory bytes of the block-table slice (16-byte multiple).
+__host__ __device__ __forceinline__ size_t block_slice_bytes(int bps) { return ((size_t)bps * 4 + 15) & ~(size_t)15; }
+
 template <typename T, int HD, int G>
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T> a) {
   constexpr int DPL = HD / 32;
@@ -212,11 +241,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
   __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
 
+  constexpr size_t kStageBytes = (size_t)kAttnWarps * kStages * 2 * TILE * sizeof(T);
+  constexpr size_t kMergeBytes = (size_t)kAttnWarps * G * HD * sizeof(float);
+  int* s_bt = reinterpret_cast<int*>(smem_raw + (kStageBytes > kMergeBytes ? kStageBytes : kMergeBytes));
+
   pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < kAttnWarps * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
   fence_mbar_init();
+  load_block_slice(a, s_bt, s, b);
   __syncthreads();
   pdl_wait();
 
@@ -247,7 +281,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
   T* my_stage = stage_base + (size_t)warp * kStages * 2 * TILE;
   const size_t head_stride = (size_t)16 * HD;  // elements per (block, kv head) tile
   auto tile_src = [&](int bi, const T* pool) -> const T* {
-    int blk = (bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    int blk = (bi < a.max_blocks) ? s_bt[bi - blk0] : -1;
     if (blk < 0 || blk >= a.num_blocks) {
       set_error(a.err, MTP_ERR_CAPACITY);
       blk = 0;
@@ -369,12 +403,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
   __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
 
+  int* s_bt = reinterpret_cast<int*>(smem_raw + (size_t)kAttnWarps * kStages * 2 * TILE_BYTES);
+
   pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;
   if (threadIdx.x < kAttnWarps * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
   fence_mbar_init();
+  load_block_slice(a, s_bt, s, b);
   __syncthreads();
   pdl_wait();
 
@@ -394,7 +431,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   unsigned char* my_stage = smem_raw + (size_t)warp * kStages * 2 * TILE_BYTES;
   auto tile_row = [&](int bi) -> int {
-    int blk = (bi < a.max_blocks) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    int blk = (bi < a.max_blocks) ? s_bt[bi - blk0] : -1;
     if (blk < 0 || blk >= a.num_blocks) {
       set_error(a.err, MTP_ERR_CAPACITY);
       blk = 0;
@@ -458,7 +495,7 @@ template <typename T, int HD, int G>
 static cudaError_t attn_launch(mtp_ctx* ctx, cudaStream_t s, const AttnArgs<T>& a, int B, int splits) {
   constexpr size_t stage_bytes = (size_t)kAttnWarps * kStages * 2 * 16 * HD * sizeof(T);
   constexpr size_t merge_bytes = (size_t)kAttnWarps * G * HD * sizeof(float);
-  constexpr size_t smem = stage_bytes > merge_bytes ? stage_bytes : merge_bytes;
+  const size_t smem = (stage_bytes > merge_bytes ? stage_bytes : merge_bytes) + block_slice_bytes(a.bps);
   auto kern = attn_kernel<T, HD, G>;
   ensure_smem((const void*)kern, smem);
   return launch_pdl(kern, dim3(splits, ctx->cfg.n_kv_heads, B), dim3(kAttnThreads), smem, s, a);
@@ -530,7 +567,7 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
     const CUtensorMap& km = *kmp;
     const CUtensorMap& vm = *vmp;
     const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
-    const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096;
+    const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096 + block_slice_bytes(a.bps);
     dim3 grid(splits, c.n_kv_heads, B);
     switch (G) {
       case 1: ensure_smem((const void*)attn_mma_kernel<1>, smem);

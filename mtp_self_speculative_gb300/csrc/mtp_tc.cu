@@ -95,6 +95,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same with an L2 cache policy (weights: evict first).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFF);
   d |= (uint64_t)1 << 16;               // leading offset (unused for swizzled K-major)
@@ -187,9 +197,19 @@ struct EpiCtx {
   const QkvMeta* meta;
 };
 
-// Pair kinds, one output pair: rows i and i + 64 of the tile for batch row b.
-__device__ __forceinline__ void tc_pair_store(const TcArgs& a, const QkvMeta* meta, int tile, int i, int b, float v0,
-                                              float v1) {
+// Rotary factors of QKV pair (i, i + 64) of head `tile` for batch row b
+// (identity for value heads, gate/up pairs and positions out of range).
+__device__ __forceinline__ float2 tc_pair_rope(const TcArgs& a, const QkvMeta* meta, int tile, int i, int b) {
+  if (a.kind != TC_QKV || tile >= a.n_q + a.n_kv) return make_float2(1.0f, 0.0f);
+  const int pos = meta->pos[b];
+  if (pos < 0) return make_float2(1.0f, 0.0f);
+  return __ldg(a.rope + (size_t)pos * 64 + i);
+}
+
+// Pair kinds, one output pair: rows i and i + 64 of the tile for batch row b;
+// cs = tc_pair_rope(...).
+__device__ __forceinline__ void tc_pair_store_cs(const TcArgs& a, const QkvMeta* meta, int tile, int i, int b,
+                                                 float v0, float v1, float2 cs) {
   if (a.kind == TC_GU) {
     const int f = tile * 64 + i;
     if (f < a.F) a.act_bf16[(size_t)b * a.F + f] = f32_to_bf16_rne(v0 / (1.0f + __expf(-v0)) * v1);
@@ -200,7 +220,6 @@ __device__ __forceinline__ void tc_pair_store(const TcArgs& a, const QkvMeta* me
   const int pos = meta->pos[b];
   if (pos < 0) return;
   if (grp < a.n_q) {
-    const float2 cs = a.rope[(size_t)pos * 64 + i];
     float* qb = a.q + (size_t)b * a.q_dim + grp * 128;
     qb[i] = v0 * cs.x - v1 * cs.y;
     qb[i + 64] = v1 * cs.x + v0 * cs.y;
@@ -212,7 +231,6 @@ __device__ __forceinline__ void tc_pair_store(const TcArgs& a, const QkvMeta* me
   uint16_t* pool;
   int g;
   if (grp < a.n_q + a.n_kv) {
-    const float2 cs = a.rope[(size_t)pos * 64 + i];
     o0 = v0 * cs.x - v1 * cs.y;
     o1 = v1 * cs.x + v0 * cs.y;
     pool = a.k_pool;
@@ -226,29 +244,43 @@ __device__ __forceinline__ void tc_pair_store(const TcArgs& a, const QkvMeta* me
   dst[i + 64] = f32_to_bf16_rne(o1);
 }
 
-// Plain kinds, one output: row r of the layer output for batch row b.
-__device__ __forceinline__ void tc_plain_store(const TcArgs& a, int r, int b, float v) {
+// Residual input of plain output row r for batch row b (x for O, h1 for
+// DOWN, none for EH).
+__device__ __forceinline__ float tc_plain_residual(const TcArgs& a, int r, int b) {
+  if (r >= a.H || a.kind == TC_EH) return 0.0f;
+  const size_t o = (size_t)b * a.H + r;
+  return __ldcg(a.kind == TC_O ? a.x + o : a.h1 + o);
+}
+
+// Plain kinds, one output: row r of the layer output for batch row b;
+// res = tc_plain_residual(...).
+__device__ __forceinline__ void tc_plain_store_res(const TcArgs& a, int r, int b, float v, float res) {
   if (r >= a.H) return;
   const size_t o = (size_t)b * a.H + r;
   if (a.kind == TC_EH) {
     a.x[o] = v;
   } else if (a.kind == TC_O) {
-    a.h1[o] = a.x[o] + v;
+    a.h1[o] = res + v;
   } else {
-    const float hv = a.h1[o] + v;
+    const float hv = res + v;
     a.hid[o] = hv;
     if (a.hidden_out && a.k == a.K) a.hidden_out[o] = hv;
   }
 }
 
+
 // Apply the epilogue to 16 columns [c0, c0 + 16) of this thread's row.
 __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const float (&v)[16]) {
   const int kind = a.kind;
   if (kind == TC_EH || kind == TC_O || kind == TC_DOWN) {
+    // all sixteen residuals are loaded before the first store
     const int r = e.tile * 128 + e.m;
+    float res[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) res[j] = (c0 + j < a.B) ? tc_plain_residual(a, r, c0 + j) : 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < a.B) tc_plain_store(a, r, c0 + j, v[j]);
+      if (c0 + j < a.B) tc_plain_store_res(a, r, c0 + j, v[j], res[j]);
     return;
   }
   if (kind == TC_LM) {
@@ -278,9 +310,13 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
   }
   epi_bar();
   if (!upper) {
+    float2 cs[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < a.B) tc_pair_store(a, e.meta, e.tile, e.m, c0 + j, v[j], e.xbuf[e.m * 16 + j]);
+      cs[j] = (c0 + j < a.B) ? tc_pair_rope(a, e.meta, e.tile, e.m, c0 + j) : make_float2(1.0f, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (c0 + j < a.B) tc_pair_store_cs(a, e.meta, e.tile, e.m, c0 + j, v[j], e.xbuf[e.m * 16 + j], cs[j]);
   }
   epi_bar();
 }
@@ -290,10 +326,35 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+// Read four floats of a peer's shared memory.  Volatile keeps it after the
+// cluster barrier; no memory clobber, so independent loads and stores around
+// it can overlap.
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
   return v;
+}
+
+// Four consecutive output rows r..r+3 (r % 4 == 0, all below H) of a plain
+// kind for batch row b.
+__device__ __forceinline__ float4 tc_plain_residual4(const TcArgs& a, int r, int b) {
+  if (a.kind == TC_EH) return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const size_t o = (size_t)b * a.H + r;
+  return __ldcg(reinterpret_cast<const float4*>((a.kind == TC_O ? a.x : a.h1) + o));
+}
+__device__ __forceinline__ void tc_plain_store4(const TcArgs& a, int r, int b, float4 v, float4 res) {
+  const size_t o = (size_t)b * a.H + r;
+  const float4 t = make_float4(res.x + v.x, res.y + v.y, res.z + v.z, res.w + v.w);
+  if (a.kind == TC_EH) {
+    *reinterpret_cast<float4*>(a.x + o) = v;
+  } else if (a.kind == TC_O) {
+    *reinterpret_cast<float4*>(a.h1 + o) = t;
+  } else {
+    *reinterpret_cast<float4*>(a.hid + o) = t;
+    if (a.hidden_out && a.k == a.K) *reinterpret_cast<float4*>(a.hidden_out + o) = t;
+  }
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -373,18 +434,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: segments in order, their k-blocks in order
+      // producer: segments in order, their k-blocks in order.  Weight tiles
+      // are read once per step: evict first, so that the activation operand
+      // every tile re-reads stays in L2.
+      const uint64_t pol = l2_evict_first_policy();
       auto issue_a = [&](int st, int tile, int kb) {
         unsigned char* dst = smem + (size_t)st * stage_bytes;
         if (a.kind == TC_GU) {
-          tma_load_2d(dst, &maps.a0, kb * 64, tile * 64, &full_bar[st]);
-          tma_load_2d(dst + 8192, &maps.a1, kb * 64, tile * 64, &full_bar[st]);
+          tma_load_2d_hint(dst, &maps.a0, kb * 64, tile * 64, &full_bar[st], pol);
+          tma_load_2d_hint(dst + 8192, &maps.a1, kb * 64, tile * 64, &full_bar[st], pol);
         } else if (a.kind == TC_QKV) {
-          if (tile < a.n_q) tma_load_2d(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st]);
-          else if (tile < a.n_q + a.n_kv) tma_load_2d(dst, &maps.a1, kb * 64, (tile - a.n_q) * 128, &full_bar[st]);
-          else tma_load_2d(dst, &maps.a2, kb * 64, (tile - a.n_q - a.n_kv) * 128, &full_bar[st]);
+          if (tile < a.n_q) tma_load_2d_hint(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st], pol);
+          else if (tile < a.n_q + a.n_kv)
+            tma_load_2d_hint(dst, &maps.a1, kb * 64, (tile - a.n_q) * 128, &full_bar[st], pol);
+          else tma_load_2d_hint(dst, &maps.a2, kb * 64, (tile - a.n_q - a.n_kv) * 128, &full_bar[st], pol);
         } else {
-          tma_load_2d(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st]);
+          tma_load_2d_hint(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st], pol);
         }
       };
       auto issue_b = [&](int st, int kb) {
@@ -530,20 +595,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       uint32_t base[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) base[j] = (j < S) ? mapa(part_local, (uint32_t)j) : 0u;
-      const int items = (c_hi - c_lo) * rows;
+      // item = (column, four consecutive rows): one float4 load per rank, all
+      // issued before the sum; then the item's side inputs and its stores
+      const int nq = rows / 4;
+      const int items = (c_hi - c_lo) * nq;
       for (int idx = threadIdx.x - 64; idx < items; idx += kTcEpiThreads) {
-        const int c = c_lo + idx / rows, mm = idx % rows;
+        const int c = c_lo + idx / nq, mq = (idx % nq) * 4;
         if (c >= a.B) continue;
-        float v0 = 0.0f, v1 = 0.0f;
-        const uint32_t off0 = (uint32_t)((c * 128 + mm) * 4), off1 = off0 + 64 * 4;
+        const uint32_t off0 = (uint32_t)((c * 128 + mq) * 4), off1 = off0 + 64 * 4;
+        float4 r0[8], r1[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (j < S) {
-            v0 += ld_dsmem(base[j] + off0);
-            if (rows == 64) v1 += ld_dsmem(base[j] + off1);
+            r0[j] = ld_dsmem4(base[j] + off0);
+            if (rows == 64) r1[j] = ld_dsmem4(base[j] + off1);
           }
-        if (rows == 64) tc_pair_store(a, &qkv_meta, tile, mm, c, v0, v1);
-        else tc_plain_store(a, tile * 128 + mm, c, v0);
+        float4 v0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), v1 = v0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < S) {
+            v0.x += r0[j].x; v0.y += r0[j].y; v0.z += r0[j].z; v0.w += r0[j].w;
+            if (rows == 64) { v1.x += r1[j].x; v1.y += r1[j].y; v1.z += r1[j].z; v1.w += r1[j].w; }
+          }
+        if (rows == 64) {
+          float2 cs[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cs[e] = tc_pair_rope(a, &qkv_meta, tile, mq + e, c);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 0, c, v0.x, v1.x, cs[0]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 1, c, v0.y, v1.y, cs[1]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 2, c, v0.z, v1.z, cs[2]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 3, c, v0.w, v1.w, cs[3]);
+        } else {
+          const int r = tile * 128 + mq;
+          tc_plain_store4(a, r, c, v0, tc_plain_residual4(a, r, c));
+        }
       }
     }
     __syncwarp();
