@@ -127,7 +127,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   const size_t maxB = c.max_batch;
   ctx->q_dim = c.n_q_heads * c.head_dim;
   ctx->kv_dim = c.n_kv_heads * c.head_dim;
-  ctx->attn_target_ctas = 2 * sms;
+  ctx->attn_target_ctas = 16 * sms;  // about eight waves of two CTAs per SM: ragged batches stay balanced
   ctx->attn_max_splits = 64;
   const size_t H = with_w ? c.hidden : 0, F = with_w ? c.ffn : 0;
   const size_t qd = with_w ? ctx->q_dim : 0;

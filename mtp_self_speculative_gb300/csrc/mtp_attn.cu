@@ -501,8 +501,10 @@ static cudaError_t attn_launch(mtp_ctx* ctx, cudaStream_t s, const AttnArgs<T>& 
   return launch_pdl(kern, dim3(splits, ctx->cfg.n_kv_heads, B), dim3(kAttnThreads), smem, s, a);
 }
 
-// Blocks per split for a batch of B requests and max_blocks capacity:
-// aim for about two CTAs per SM, never more than max_splits splits.
+// Blocks per split for a batch of B requests and max_blocks capacity: aim
+// for about attn_target_ctas CTAs (several waves, so that the splits of the
+// longest requests of a ragged batch do not set the kernel's length), never
+// more than max_splits splits nor fewer than min_bps blocks per split.
 static int attn_bps(const mtp_ctx* ctx, int B, int max_blocks, int min_bps) {
   const long long pairs = (long long)B * ctx->cfg.n_kv_heads;
   long long splits = (ctx->attn_target_ctas + pairs - 1) / pairs;
