@@ -201,6 +201,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     };
     const size_t t_eh = take2(mb * 2 * c.hidden * 2), t_xn = take2(mb * c.hidden * 2);
     const size_t t_at = take2(mb * ctx->q_dim * 2), t_act = take2(mb * c.ffn * 2);
+    const size_t t_ssq = take2((size_t)(c.hidden / 128) * mb * 4);
     if (cudaMalloc(&ctx->tc_ws, o2) != cudaSuccess || cudaMemset(ctx->tc_ws, 0, o2) != cudaSuccess) {
       cudaGetLastError();
       if (ctx->tc_ws) cudaFree(ctx->tc_ws);
@@ -213,6 +214,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     ctx->tc_xn = (uint16_t*)(tb + t_xn);
     ctx->tc_attn = (uint16_t*)(tb + t_at);
     ctx->tc_act = (uint16_t*)(tb + t_act);
+    ctx->tc_ssq = (float*)(tb + t_ssq);
   }
   // persistent draft kernel workspace: attention records, counters, argmax
   // keys and the grid-barrier words

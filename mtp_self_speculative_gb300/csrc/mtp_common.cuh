@@ -220,7 +220,8 @@ struct mtp_ctx {
   void* tc_ws;
   int tc_min_batch;
   uint16_t* tc_xin_eh;          // [maxB, 2H] bf16 eh_proj input
-  uint16_t* tc_xn;              // [maxB, H]  bf16 normalised GEMM input
+  uint16_t* tc_xn;              // [maxB, H]  bf16 GEMM input y * w (RMS factor applied by the consumer)
+  float* tc_ssq;                // [H / 128, maxB] per-tile sums of squares of y
   uint16_t* tc_attn;            // [maxB, q_dim] bf16 attention output
   uint16_t* tc_act;             // [maxB, F]  bf16 silu(g) * u
   // timing

@@ -38,8 +38,10 @@
 // in shared memory, one 64-bit atomicMax per request per CTA, last CTA writes
 // the draft ids).
 //
-// RMSNorm inputs are produced by small prep kernels (one CTA per request)
-// that write bf16 GEMM operands.
+// The eh_proj input (two RMSNorms with their own scales) comes from a small
+// prep kernel; every other RMSNorm is folded into the neighbouring GEMMs: the
+// producing GEMM's epilogue writes bf16(y * w) and per-tile sums of y^2, the
+// consuming GEMM scales its accumulators by each request's RMS factor.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdio.h>
@@ -83,6 +85,16 @@ struct TcArgs {
   int* err;
   int* req_bad;
   const float2* rope;
+  // RMSNorm of the next projection's input, folded into this one:
+  // EH, O and DOWN (producers) also write xn_out = bf16(y * w_next) and, per
+  // 128-row tile and request, the sum of y^2 into ssq[tile * B + b]; QKV, GU
+  // and the LM head (consumers, scale_in) multiply their accumulators by
+  // rsqrt(sum over tiles / H + eps) of each request.
+  const uint16_t* w_next;
+  uint16_t* xn_out;
+  float* ssq;
+  int scale_in;
+  float eps;
 };
 
 // ------------------------------------------------------------ primitives
@@ -193,6 +205,7 @@ __device__ void qkv_meta_fill(const TcArgs& a, QkvMeta* meta, int tid, int nthre
 struct EpiCtx {
   int tile, m, lane, quarter;  // m = row of the tile held by this thread
   float* xbuf;                 // [64][16] exchange buffer
+  const float* rms;            // [B] RMS factor per request (1 unless folded)
   unsigned long long* cta_best;
   const QkvMeta* meta;
 };
@@ -273,14 +286,30 @@ __device__ __forceinline__ void tc_plain_store_res(const TcArgs& a, int r, int b
 __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const float (&v)[16]) {
   const int kind = a.kind;
   if (kind == TC_EH || kind == TC_O || kind == TC_DOWN) {
-    // all sixteen residuals are loaded before the first store
+    // all sixteen residuals are loaded before the first store; the outputs'
+    // squares are summed over the tile's 128 rows (warp, then the four
+    // warps through xbuf) for the next RMSNorm
     const int r = e.tile * 128 + e.m;
+    const float wn = bf16_lo((uint32_t)__ldg(a.w_next + r));
     float res[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) res[j] = (c0 + j < a.B) ? tc_plain_residual(a, r, c0 + j) : 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (c0 + j < a.B) tc_plain_store_res(a, r, c0 + j, v[j], res[j]);
+    for (int j = 0; j < 16; ++j) {
+      const float y = (kind == TC_EH) ? v[j] : res[j] + v[j];
+      if (c0 + j < a.B) {
+        tc_plain_store_res(a, r, c0 + j, v[j], res[j]);
+        a.xn_out[(size_t)(c0 + j) * a.H + r] = f32_to_bf16_rne(y * wn);
+      }
+      const float q = warp_sum((c0 + j < a.B) ? y * y : 0.0f);
+      if (e.lane == 0) e.xbuf[e.quarter * 16 + j] = q;
+    }
+    epi_bar();
+    const int t = threadIdx.x - 64;
+    if (t < 16 && c0 + t < a.B)
+      a.ssq[(size_t)e.tile * a.B + c0 + t] =
+          e.xbuf[t] + e.xbuf[16 + t] + e.xbuf[32 + t] + e.xbuf[48 + t];
+    epi_bar();
     return;
   }
   if (kind == TC_LM) {
@@ -290,8 +319,9 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
     for (int j = 0; j < 16; ++j) {
       const int b = c0 + j;
       if (b >= a.B) continue;  // uniform across the warp
-      if (a.logits && row_ok) a.logits[((size_t)b * a.K + (a.k - 1)) * a.V + r] = v[j];
-      const uint32_t ord = row_ok ? ordered_bits(v[j]) : 0u;
+      const float z = v[j] * e.rms[b];
+      if (a.logits && row_ok) a.logits[((size_t)b * a.K + (a.k - 1)) * a.V + r] = z;
+      const uint32_t ord = row_ok ? ordered_bits(z) : 0u;
       const uint32_t mx = __reduce_max_sync(0xffffffffu, ord);
       const uint32_t bal = __ballot_sync(0xffffffffu, ord == mx);
       if (e.lane == (b & 31)) {
@@ -316,7 +346,10 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
       cs[j] = (c0 + j < a.B) ? tc_pair_rope(a, e.meta, e.tile, e.m, c0 + j) : make_float2(1.0f, 0.0f);
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (c0 + j < a.B) tc_pair_store_cs(a, e.meta, e.tile, e.m, c0 + j, v[j], e.xbuf[e.m * 16 + j], cs[j]);
+      if (c0 + j < a.B) {
+        const float sc = e.rms[c0 + j];
+        tc_pair_store_cs(a, e.meta, e.tile, e.m, c0 + j, v[j] * sc, e.xbuf[e.m * 16 + j] * sc, cs[j]);
+      }
   }
   epi_bar();
 }
@@ -344,17 +377,25 @@ __device__ __forceinline__ float4 tc_plain_residual4(const TcArgs& a, int r, int
   const size_t o = (size_t)b * a.H + r;
   return __ldcg(reinterpret_cast<const float4*>((a.kind == TC_O ? a.x : a.h1) + o));
 }
-__device__ __forceinline__ void tc_plain_store4(const TcArgs& a, int r, int b, float4 v, float4 res) {
+// Stores the four outputs, their bf16(y * w_next) copy for the next GEMM, and
+// returns the sum of their squares.
+__device__ __forceinline__ float tc_plain_store4(const TcArgs& a, int r, int b, float4 v, float4 res) {
   const size_t o = (size_t)b * a.H + r;
-  const float4 t = make_float4(res.x + v.x, res.y + v.y, res.z + v.z, res.w + v.w);
+  const float4 t = (a.kind == TC_EH) ? v : make_float4(res.x + v.x, res.y + v.y, res.z + v.z, res.w + v.w);
   if (a.kind == TC_EH) {
-    *reinterpret_cast<float4*>(a.x + o) = v;
+    *reinterpret_cast<float4*>(a.x + o) = t;
   } else if (a.kind == TC_O) {
     *reinterpret_cast<float4*>(a.h1 + o) = t;
   } else {
     *reinterpret_cast<float4*>(a.hid + o) = t;
     if (a.hidden_out && a.k == a.K) *reinterpret_cast<float4*>(a.hidden_out + o) = t;
   }
+  const uint2 wn = __ldg(reinterpret_cast<const uint2*>(a.w_next + r));
+  uint2 xo;
+  xo.x = (uint32_t)f32_to_bf16_rne(t.x * bf16_lo(wn.x)) | ((uint32_t)f32_to_bf16_rne(t.y * bf16_hi(wn.x)) << 16);
+  xo.y = (uint32_t)f32_to_bf16_rne(t.z * bf16_lo(wn.y)) | ((uint32_t)f32_to_bf16_rne(t.w * bf16_hi(wn.y)) << 16);
+  *reinterpret_cast<uint2*>(a.xn_out + o) = xo;
+  return t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -394,6 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   __shared__ volatile int abort_flag;
   __shared__ int last_flag, stop_snap;
   __shared__ float xbuf[64 * 16];
+  __shared__ float s_rms[256];
   __shared__ unsigned long long cta_best[256];
   __shared__ QkvMeta qkv_meta;
 
@@ -511,11 +553,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     const int quarter = warp & 3;
     const int m = quarter * 32 + lane;
     const int epi_tid = threadIdx.x - 64;
+    // RMS factor of each request's input (consumers of a folded RMSNorm):
+    // the tiles' sums of squares in tile order
+    const int ntile_h = a.H / 128;
+    for (int b = epi_tid; b < a.B; b += kTcEpiThreads) {
+      float r = 1.0f;
+      if (a.scale_in) {
+        float t = 0.0f;
+#pragma unroll 8
+        for (int ti = 0; ti < ntile_h; ++ti) t += __ldcg(a.ssq + (size_t)ti * a.B + b);
+        r = rsqrtf(t / (float)a.H + a.eps);
+      }
+      s_rms[b] = r;
+    }
+    epi_bar();
     EpiCtx e;
     e.m = m;
     e.lane = lane;
     e.quarter = quarter;
     e.xbuf = xbuf;
+    e.rms = s_rms;
     e.cta_best = cta_best;
     e.meta = &qkv_meta;
     if (a.kind == TC_QKV) {
@@ -621,13 +678,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
           float2 cs[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) cs[e] = tc_pair_rope(a, &qkv_meta, tile, mq + e, c);
-          tc_pair_store_cs(a, &qkv_meta, tile, mq + 0, c, v0.x, v1.x, cs[0]);
-          tc_pair_store_cs(a, &qkv_meta, tile, mq + 1, c, v0.y, v1.y, cs[1]);
-          tc_pair_store_cs(a, &qkv_meta, tile, mq + 2, c, v0.z, v1.z, cs[2]);
-          tc_pair_store_cs(a, &qkv_meta, tile, mq + 3, c, v0.w, v1.w, cs[3]);
+          const float sc = a.scale_in ? s_rms[c] : 1.0f;
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 0, c, v0.x * sc, v1.x * sc, cs[0]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 1, c, v0.y * sc, v1.y * sc, cs[1]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 2, c, v0.z * sc, v1.z * sc, cs[2]);
+          tc_pair_store_cs(a, &qkv_meta, tile, mq + 3, c, v0.w * sc, v1.w * sc, cs[3]);
         } else {
+          // the warp holds all 128 rows of column c: its sum of squares is the
+          // tile's partial for the next RMSNorm
           const int r = tile * 128 + mq;
-          tc_plain_store4(a, r, c, v0, tc_plain_residual4(a, r, c));
+          const float q = warp_sum(tc_plain_store4(a, r, c, v0, tc_plain_residual4(a, r, c)));
+          if (lane == 0) a.ssq[(size_t)tile * a.B + c] = q;
         }
       }
     }
@@ -744,15 +805,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_eh_kernel(const PrepEhArgs 
   prep_row(nullptr, e, a.w_e, out + a.H, a.H, a.eps, red);
 }
 
-// out[b] = bf16(RMSNorm(src_b) w)
-__global__ void __launch_bounds__(kPrepThreads) prep_norm_kernel(const float* src, const uint16_t* w, uint16_t* out,
-                                                                 int C, float eps) {
-  __shared__ float red[kPrepThreads / 32];
-  pdl_trigger();
-  pdl_wait();
-  const int b = blockIdx.x;
-  prep_row(src + (size_t)b * C, nullptr, w, out + (size_t)b * C, C, eps, red);
-}
 
 // -------------------------------------------------------------- host side
 
@@ -927,6 +979,12 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   a.err = ctx->err; a.rope = ctx->rope; a.req_bad = ctx->req_bad;
   a.stages = pl->stages;
   a.ksplit = pl->S;
+  a.eps = c.eps;
+  a.ssq = ctx->tc_ssq;
+  a.xn_out = ctx->tc_xn;
+  a.scale_in = (kind == TC_QKV || kind == TC_GU || kind == TC_LM) ? 1 : 0;
+  a.w_next = (const uint16_t*)(kind == TC_EH ? ctx->w.w_norm_in : kind == TC_O ? ctx->w.w_norm_post
+                               : kind == TC_DOWN ? ctx->w.w_norm_f : nullptr);
   const int kid = (kind == TC_EH) ? MTP_KERNEL_EH_PROJ : (kind == TC_QKV) ? MTP_KERNEL_QKV_ROPE
                   : (kind == TC_O) ? MTP_KERNEL_O_PROJ : (kind == TC_GU) ? MTP_KERNEL_GATE_UP
                   : (kind == TC_DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
@@ -951,12 +1009,6 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   return e;
 }
 
-static cudaError_t prep_norm(mtp_ctx* ctx, cudaStream_t s, int B, const float* src, const void* w, int C) {
-  ctx->launches++;
-  return launch_pdl(prep_norm_kernel, dim3(B), dim3(kPrepThreads), 0, s, src, (const uint16_t*)w, ctx->tc_xn, C,
-                    ctx->cfg.eps);
-}
-
 cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
                                  const void* embeds, const int32_t* positions, const mtp_kv* kv,
                                  const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out) {
@@ -970,15 +1022,14 @@ cudaError_t launch_draft_step_tc(mtp_ctx* ctx, cudaStream_t s, int B, int k, int
   pa.out = ctx->tc_xin_eh; pa.err = ctx->err; pa.pending = kv->pending; pa.req_bad = ctx->req_bad;
   ctx->launches++;
   if ((e = launch_pdl(prep_eh_kernel, dim3(B), dim3(kPrepThreads), 0, s, pa)) != cudaSuccess) return e;
+  // EH, O and DOWN also write the next projection's bf16 input and its
+  // per-tile sums of squares (RMSNorm folded into the GEMMs)
   if ((e = tc_launch(ctx, s, TC_EH, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
-  if ((e = prep_norm(ctx, s, B, ctx->x, ctx->w.w_norm_in, c.hidden)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_QKV, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
   if ((e = launch_attention(ctx, s, B, k, kv)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_O, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
-  if ((e = prep_norm(ctx, s, B, ctx->h1, ctx->w.w_norm_post, c.hidden)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_GU, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
   if ((e = tc_launch(ctx, s, TC_DOWN, B, k, K, positions, kv, draft_ids, logits, hidden_out)) != cudaSuccess) return e;
-  if ((e = prep_norm(ctx, s, B, ctx->hid, ctx->w.w_norm_f, c.hidden)) != cudaSuccess) return e;
   return tc_launch(ctx, s, TC_LM, B, k, K, positions, kv, draft_ids, logits, hidden_out);
 }
 
