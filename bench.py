@@ -313,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
     import mtp_self_speculative_gb300 as M
     cfg = WORKLOADS[args.workload]
     if cfg.H == 0:
-        raise SystemExit("workload %s has no draft head; pick a draft workload" % cfg.name)
+        return run_verify_workload(args, cfg, rank, world, local_rank)
     K = cfg.K
     wl = Workload(cfg, K, args.persistent_max_batch)
     stream = torch.cuda.current_stream()
@@ -501,6 +501,137 @@ def run_e2e(wl: Workload, n: int) -> dict:
 
 
 # ------------------------------------------------------- CPU / oracle legs
+
+VERIFY_METRIC = "MTP verify + KV commit calls/s (64 requests, K_b uniform 1..8); % HBM roofline"
+
+
+def run_verify_workload(args, cfg, rank, world, local_rank):
+    """The verify + rollback workload (no draft head): one call is mtp_verify
+    over the ragged target-logit rows followed by mtp_kv_commit_accepted
+    (extra=1).  Verify and commit are timed separately and together with
+    CUDA events around each call; seq_len and pending are restored after
+    every call, outside the events."""
+    import torch
+    torch.cuda.set_device(local_rank)
+    import mtp_self_speculative_gb300 as M
+    import oracle as O
+    vi = synth.make_verify_inputs(cfg)
+    lens = synth.context_lengths(cfg)
+    kv0 = synth.make_kv(cfg, lens, extra_slots=int(vi.num_drafts.max()) + 1, prefill_slots=lens + vi.num_drafts)
+    kv0.pending = vi.num_drafts.astype(np.int32).copy()
+    B = len(lens)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+    ctx = M.mtp_init(M.make_config(1, cfg.n_q, cfg.n_kv, cfg.head_dim, 8, cfg.vocab, dtype=cfg.dtype, max_batch=B,
+                                   max_k=vi.max_k, block_size=cfg.block_size))
+    kv = M.KVCache(dev(kv0.k_pool), dev(kv0.v_pool), dev(kv0.block_table), dev(kv0.seq_len), dev(kv0.pending))
+    seq0, pend0 = dev(kv0.seq_len), dev(kv0.pending)
+    logits, ro, drafts, nd = dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts)
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    bon = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # larger than L2
+
+    def reset():
+        kv.seq_len.copy_(seq0)
+        kv.pending.copy_(pend0)
+        flush.fill_(1)  # the 111 MB of logits would otherwise stay in the 126 MB L2
+
+    for _ in range(args.warmup):
+        M.mtp_verify(ctx, logits, ro, drafts, nd, acc, bon)
+        M.mtp_kv_commit_accepted(ctx, kv, acc, extra=1)
+        reset()
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    acc_o, bon_o = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, cfg.dtype)
+    assert np.array_equal(acc.cpu().numpy(), acc_o) and np.array_equal(bon.cpu().numpy(), bon_o)
+
+    n = min(args.steps, 1000)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    launches0 = M.mtp_launch_count(ctx)
+    sampler = ClockSampler(gpu_id_for_smi(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i][0].record(stream)
+        M.mtp_verify(ctx, logits, ro, drafts, nd, acc, bon)
+        ev[i][1].record(stream)
+        M.mtp_kv_commit_accepted(ctx, kv, acc, extra=1)
+        ev[i][2].record(stream)
+        reset()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    launches = (M.mtp_launch_count(ctx) - launches0) / n
+    t_ver = [e[0].elapsed_time(e[1]) for e in ev]
+    t_com = [e[1].elapsed_time(e[2]) for e in ev]
+    t_all = statistics.median([a + b for a, b in zip(t_ver, t_com)])
+    t_all = reduce_max(t_all, world)
+    # end to end: host logits copied in, accepted counts and bonus ids read back
+    h_logits = logits.cpu().pin_memory()
+    h_acc = torch.empty_like(acc, device="cpu").pin_memory()
+    h_bon = torch.empty_like(bon, device="cpu").pin_memory()
+    ne = max(5, min(n // 10, 50))
+    t0 = time.perf_counter()
+    for _ in range(ne):
+        logits.copy_(h_logits, non_blocking=True)
+        M.mtp_verify(ctx, logits, ro, drafts, nd, acc, bon)
+        M.mtp_kv_commit_accepted(ctx, kv, acc, extra=1)
+        h_acc.copy_(acc, non_blocking=True)
+        h_bon.copy_(bon, non_blocking=True)
+        stream.synchronize()
+        reset()
+    e2e_s = (time.perf_counter() - t0) / ne
+    assert M.mtp_get_device_error(ctx) == 0
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    ver_bytes = int(vi.row_offsets[-1]) * cfg.vocab * cfg.elem_bytes
+    kv_row = 2 * cfg.n_kv * cfg.head_dim * cfg.elem_bytes
+    com_bytes = int(np.sum(vi.num_drafts - np.minimum(acc_o + 1, vi.num_drafts))) * kv_row
+    tv = statistics.median(t_ver)
+    ver_gbs = ver_bytes / (tv * 1e-3) / 1e9
+    world_calls = world / (t_all * 1e-3)
+    # the oracle as it stands on the host: the same verify + commit
+    kv_c = kv0.copy()
+    t = time.perf_counter()
+    reps = 0
+    while reps < 3 or time.perf_counter() - t < 2.0:
+        O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, cfg.dtype)
+        kv_c = kv0.copy()
+        O.kv_commit(kv_c, np.minimum(acc_o + 1, vi.num_drafts), cfg.dtype)
+        reps += 1
+    cpu = reps / (time.perf_counter() - t)
+    line = {
+        "metric": VERIFY_METRIC, "value": world_calls, "unit": "calls/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": t_all, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) logits with planted spikes)",
+        "config": {"workload": cfg.name, "batch": B, "k_range": [int(vi.num_drafts.min()), int(vi.num_drafts.max())],
+                   "vocab": cfg.vocab, "verify_rows": int(vi.row_offsets[-1]), "context": int(lens[0]),
+                   "l2": "L2 flushed between calls (256 MB write, outside the timed events); "
+                         "%.1f MB of logits per call" % (ver_bytes / 1e6)},
+        "verify_ms": tv, "commit_ms": statistics.median(t_com),
+        "roofline": {"kernel": "verify", "bound": "hbm", "achieved": ver_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": ver_gbs / peak, "peak_source": peak_kind + " hbm_gbs", "traffic": None,
+                     "bytes_per_launch": ver_bytes},
+        "commit_bytes": com_bytes,
+        "e2e": {"value": 1.0 / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": ver_bytes,
+                "d2h_bytes_per_step": 2 * B * 4},
+        "gpu_launches": launches,
+        "cpu_baseline": {"value": cpu, "unit": "calls/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": "%d full call(s): float64 numpy verify + commit of the same inputs" % reps},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
 
 def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1) -> dict:
     """The float64 oracle as it stands, one full step (K draft steps, verify,

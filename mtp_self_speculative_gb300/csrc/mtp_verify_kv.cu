@@ -38,23 +38,27 @@ struct VerifyArgs {
   int V, max_k, splits, num_rows;
 };
 
+// Running (value, index) maximum over one 16-byte vector of consecutive ids
+// starting at base.  Each thread visits increasing ids, so a strict
+// comparison keeps the lowest id among equal values (-0 equals +0).
 template <typename T>
-__device__ __forceinline__ void scan_vec(const uint4& u, int base, unsigned long long& best);
+__device__ __forceinline__ void scan_vec(const uint4& u, int base, float& bv, int& bi);
 template <>
-__device__ __forceinline__ void scan_vec<uint16_t>(const uint4& u, int base, unsigned long long& best) {
+__device__ __forceinline__ void scan_vec<uint16_t>(const uint4& u, int base, float& bv, int& bi) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    best = umax64(best, argmax_key(bf16_lo(w[i]), (uint32_t)(base + 2 * i)));
-    best = umax64(best, argmax_key(bf16_hi(w[i]), (uint32_t)(base + 2 * i + 1)));
+    const float lo = bf16_lo(w[i]), hi = bf16_hi(w[i]);
+    if (lo > bv || bi < 0) { bv = lo; bi = base + 2 * i; }
+    if (hi > bv) { bv = hi; bi = base + 2 * i + 1; }
   }
 }
 template <>
-__device__ __forceinline__ void scan_vec<float>(const uint4& u, int base, unsigned long long& best) {
-  best = umax64(best, argmax_key(__uint_as_float(u.x), (uint32_t)base));
-  best = umax64(best, argmax_key(__uint_as_float(u.y), (uint32_t)(base + 1)));
-  best = umax64(best, argmax_key(__uint_as_float(u.z), (uint32_t)(base + 2)));
-  best = umax64(best, argmax_key(__uint_as_float(u.w), (uint32_t)(base + 3)));
+__device__ __forceinline__ void scan_vec<float>(const uint4& u, int base, float& bv, int& bi) {
+  const float f[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (f[i] > bv || bi < 0) { bv = f[i]; bi = base + i; }
 }
 
 template <typename T>
@@ -85,7 +89,9 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(const VerifyArgs
   unsigned long long best = 0ull;
   if (c0 < c1) {
     constexpr int VPE = Elem<T>::kPerVec;
-    // scalar head until 16-byte alignment, vector body, scalar tail
+    constexpr int kBatch = 8;  // 16-byte loads in flight per thread
+    // scalar head until 16-byte alignment, vector body, scalar tail; each
+    // part keeps a running (value, index) maximum, folded into the key once
     int c = c0;
     const int misalign = (int)(((uintptr_t)(row + c) & 15) / sizeof(T));
     int head_end = misalign ? min(c1, c + (VPE - misalign)) : c;
@@ -94,10 +100,22 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_kernel(const VerifyArgs
     c = head_end;
     const int nvec = (c1 - c) / VPE;
     const T* vbase = row + c;
-    for (int v = threadIdx.x; v < nvec; v += kVerifyThreads) {
-      const uint4 u = ld_stream(vbase + (size_t)v * VPE);
-      scan_vec<T>(u, c + v * VPE, best);
+    float bv = -INFINITY;
+    int bi = -1;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kVerifyThreads * kBatch) {
+      uint4 u[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int v = v0 + q * kVerifyThreads;
+        u[q] = v < nvec ? ld_stream(vbase + (size_t)v * VPE) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int v = v0 + q * kVerifyThreads;
+        if (v < nvec) scan_vec<T>(u[q], c + v * VPE, bv, bi);
+      }
     }
+    if (bi >= 0) best = umax64(best, argmax_key(bv, (uint32_t)bi));
     for (int i = c + nvec * VPE + threadIdx.x; i < c1; i += kVerifyThreads)
       best = umax64(best, argmax_key(Elem<T>::load1(row + i), (uint32_t)i));
   }
