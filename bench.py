@@ -97,14 +97,36 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def step_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True) -> dict:
+def mat_bytes(cfg: synth.MTPShape, rows: int, cols: int, fmt: str, table: bool = False) -> int:
+    """Stored bytes of one weight matrix: dense elements, or the quantized
+    format (projections: 4-bit codes plus an fp16 scale and a byte zero point
+    per 64 columns; the embedding / LM head table: int8 codes plus an fp16
+    scale per row)."""
+    if fmt == "dense":
+        return rows * cols * cfg.elem_bytes
+    if table:
+        return rows * cols + rows * 2
+    return rows * cols // 2 + rows * (cols // 64) * 3
+
+
+def weight_bytes(cfg: synth.MTPShape, fmt: str = "dense") -> int:
+    """Bytes of all weights read once per draft step (tied LM head = embed)."""
+    if fmt == "dense":
+        return cfg.weight_bytes()
+    H, F, V, qd, kvd = cfg.H, cfg.ffn, cfg.vocab, cfg.q_dim, cfg.kv_dim
+    mats = (mat_bytes(cfg, H, 2 * H, fmt) + mat_bytes(cfg, qd + 2 * kvd, H, fmt) + mat_bytes(cfg, H, qd, fmt)
+            + mat_bytes(cfg, 2 * F, H, fmt) + mat_bytes(cfg, H, F, fmt) + mat_bytes(cfg, V, H, fmt, table=True))
+    return mats + 5 * H * cfg.elem_bytes
+
+
+def step_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True, fmt: str = "dense") -> dict:
     """Algorithmic bytes of one step: every weight and KV entry read once per
     draft step, plus the writes of logits, ids and new KV entries."""
     e = cfg.elem_bytes
     B = len(lens)
-    w = cfg.weight_bytes()
+    w = weight_bytes(cfg, fmt)
     kv_row = 2 * cfg.n_kv * cfg.head_dim * e           # K and V of one slot
-    lm = cfg.vocab * cfg.H * e + cfg.H * e              # LM head rows + final norm weight
+    lm = mat_bytes(cfg, cfg.vocab, cfg.H, fmt, table=True) + cfg.H * e   # LM head rows + final norm weight
     draft = 0
     for k in range(1, K + 1):
         kv_read = int(np.sum(lens + k)) * kv_row
@@ -116,7 +138,8 @@ def step_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool 
             "weights": w}
 
 
-def kernel_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True) -> dict:
+def kernel_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: bool = True,
+                 fmt: str = "dense") -> dict:
     """Algorithmic bytes of one launch of each kernel (draft kernels: one
     draft step, attention averaged over k = 1..K)."""
     e = cfg.elem_bytes
@@ -124,16 +147,17 @@ def kernel_bytes(cfg: synth.MTPShape, lens: np.ndarray, K: int, with_logits: boo
     H, F, V, qd, kvd = cfg.H, cfg.ffn, cfg.vocab, cfg.q_dim, cfg.kv_dim
     kv_row = 2 * kvd * e
     mean_ctx = float(np.sum(lens)) + B * (K + 1) / 2.0
+    m = lambda r, c, table=False: mat_bytes(cfg, r, c, fmt, table)
     return {
-        "eh_proj": H * 2 * H * e + 2 * H * e + B * 2 * H * e + B * H * 4,
-        "qkv_rope": (qd + 2 * kvd) * H * e + H * e + B * H * 4 + B * (qd * 4 + kv_row),
+        "eh_proj": m(H, 2 * H) + 2 * H * e + B * 2 * H * e + B * H * 4,
+        "qkv_rope": m(qd + 2 * kvd, H) + H * e + B * H * 4 + B * (qd * 4 + kv_row),
         "attention": mean_ctx * kv_row + B * qd * 8,
-        "o_proj": H * qd * e + B * (qd + 2 * H) * 4,
-        "gate_up": 2 * F * H * e + H * e + B * (H * 4 + F * 4),
-        "down": H * F * e + B * (F * 4 + 2 * H * 4),
-        "lm_head": V * H * e + H * e + B * H * 4 + (B * V * 4 if with_logits else 0),
+        "o_proj": m(H, qd) + B * (qd + 2 * H) * 4,
+        "gate_up": m(2 * F, H) + H * e + B * (H * 4 + F * 4),
+        "down": m(H, F) + B * (F * 4 + 2 * H * 4),
+        "lm_head": m(V, H, True) + H * e + B * H * 4 + (B * V * 4 if with_logits else 0),
         "verify": B * (K + 1) * V * e,
-        "draft_persistent": step_bytes(cfg, lens, K, with_logits)["draft"],
+        "draft_persistent": step_bytes(cfg, lens, K, with_logits, fmt)["draft"],
     }
 
 
@@ -144,7 +168,7 @@ def kernel_breakdown(wl, steps: int) -> dict:
     boundaries, so these are per-kernel, not additive, figures."""
     import torch
     import mtp_self_speculative_gb300 as M
-    kb = kernel_bytes(wl.cfg, wl.lens, wl.K)
+    kb = kernel_bytes(wl.cfg, wl.lens, wl.K, fmt=wl.weight_format)
     peak = float(measured_peaks()[0]["hbm_gbs"])
     out = {}
     for kid, name in enumerate(M.KERNEL_NAMES):
@@ -238,10 +262,11 @@ def gpu_id_for_smi(local_rank: int) -> str:
 class Workload:
     """Device-resident inputs and outputs of one draft+verify step."""
 
-    def __init__(self, cfg: synth.MTPShape, K: int, persistent_max_batch: int = 0):
+    def __init__(self, cfg: synth.MTPShape, K: int, persistent_max_batch: int = 0, weight_format: str = "dense"):
         import torch
         import mtp_self_speculative_gb300 as M
         self.cfg, self.K = cfg, K
+        self.weight_format = weight_format
         self.w = synth.make_weights(cfg, norm="ones")
         self.lens = synth.context_lengths(cfg)
         self.B = B = len(self.lens)
@@ -259,7 +284,8 @@ class Workload:
         self.ctx = M.mtp_init(M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps,
                                             cfg.rope_theta, cfg.dtype, B, K, cfg.block_size,
                                             int(self.lens.max()) + K + 8,
-                                            persistent_max_batch=persistent_max_batch), self.wdev)
+                                            persistent_max_batch=persistent_max_batch,
+                                            weight_format=weight_format), self.wdev)
         self.kv = M.KVCache(dev(self.kv0.k_pool), dev(self.kv0.v_pool), dev(self.kv0.block_table),
                             dev(self.kv0.seq_len), dev(self.kv0.pending))
         self.L0 = dev(self.lens.astype(np.int32))
@@ -315,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
     if cfg.H == 0:
         return run_verify_workload(args, cfg, rank, world, local_rank)
     K = cfg.K
-    wl = Workload(cfg, K, args.persistent_max_batch)
+    wl = Workload(cfg, K, args.persistent_max_batch, args.weights)
     stream = torch.cuda.current_stream()
 
     # bandwidth yardstick in the same run: 1 GiB device-to-device copy
@@ -402,7 +428,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
-    sb = step_bytes(cfg, wl.lens, K)
+    sb = step_bytes(cfg, wl.lens, K, fmt=args.weights)
     ms_per_step = elapsed_max / args.steps
     steps_s = world * args.steps / (elapsed_max * 1e-3)
     emitted = int(np.sum(acc + 1))
@@ -410,10 +436,11 @@ def run_ours(args, rank, world, local_rank):
     persistent = roof_kid == M.MTP_KERNEL_DRAFT_PERSISTENT
     roof_bytes = sb["draft"] if persistent else sb["lm_head_launch"]
     lm_gbs = roof_bytes / (lm_avg_ms * 1e-3) / 1e9
+    tkey = cfg.name if args.weights == "dense" else cfg.name + ":" + args.weights
     if persistent:
-        traffic = args.lm_traffic if args.lm_traffic is not None else PERSISTENT_TRAFFIC.get(cfg.name)
+        traffic = args.lm_traffic if args.lm_traffic is not None else PERSISTENT_TRAFFIC.get(tkey)
     else:
-        traffic = args.lm_traffic if args.lm_traffic is not None else LM_TRAFFIC.get(cfg.name)
+        traffic = args.lm_traffic if args.lm_traffic is not None else LM_TRAFFIC.get(tkey)
     peak = float(peaks["hbm_gbs"])
     line = {
         "metric": METRIC,
@@ -426,12 +453,14 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": cfg.dtype,
+        "dtype": cfg.dtype if args.weights == "dense" else "int4/int8 weights, f32 arithmetic, bf16 KV",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden/KV, uniform token ids)",
         "config": {"workload": cfg.name, "hidden": cfg.H, "q_heads": cfg.n_q, "kv_heads": cfg.n_kv,
                    "head_dim": cfg.head_dim, "ffn": cfg.ffn, "vocab": cfg.vocab, "batch": wl.B,
                    "draft_steps_K": K, "mtp_context": [int(wl.lens.min()), int(wl.lens.max())],
                    "tied_lm_head": True, "parallelism": "replicas" if world > 1 else "single",
+                   "weights": args.weights if args.weights == "dense" else
+                              "int4_g64 asymmetric projections, int8 symmetric per-row embedding/LM head",
                    "l2": "inputs larger than L2 (%.2f GB of weights streamed per draft step)" %
                          (sb["weights"] / 1e9)},
         "accepted_tok_s": {"emitted": emitted * steps_s, "accepted_drafts": int(np.sum(acc)) * steps_s,
@@ -442,7 +471,8 @@ def run_ours(args, rank, world, local_rank):
         "step_hbm": {"bytes_per_step": sb["total"],
                      "achieved_gbs": sb["total"] / (ms_per_step * 1e-3) / 1e9,
                      "frac_of_measured": sb["total"] / (ms_per_step * 1e-3) / 1e9 / peak},
-        "roofline": {"kernel": "draft_persistent" if persistent else "lm_head_argmax", "bound": "hbm",
+        "roofline": {"kernel": "draft_persistent" if persistent else
+                               ("lm_head_argmax" if args.weights == "dense" else "lm_head_argmax_int8"), "bound": "hbm",
                      "achieved": lm_gbs, "peak": peak, "unit": "GB/s", "frac": lm_gbs / peak,
                      "peak_source": peak_kind + " hbm_gbs", "traffic": traffic,
                      "launches_timed": len(lm_ms), "bytes_per_launch": roof_bytes},
@@ -455,7 +485,7 @@ def run_ours(args, rank, world, local_rank):
     if e2e:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg)
+        line["cpu_baseline"] = cpu_baseline(cfg, fmt=args.weights)
     print(json.dumps(line), flush=True)
 
 
@@ -633,7 +663,16 @@ def run_verify_workload(args, cfg, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1) -> dict:
+def oracle_head(cfg: synth.MTPShape, w, fmt: str):
+    """The oracle's weights for the bench's weight format."""
+    import oracle as O
+    if fmt == "int4_g64":
+        from oracle import quant
+        return quant.quantized_weights(w, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+    return O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+
+
+def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1, fmt: str = "dense") -> dict:
     """The float64 oracle as it stands, one full step (K draft steps, verify,
     commit) for the same workload on the host cores."""
     import oracle as O
@@ -641,7 +680,7 @@ def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1) -> dict:
     lens = synth.context_lengths(cfg)
     kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
     di = synth.make_draft_inputs(cfg, w, lens)
-    W = O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+    W = oracle_head(cfg, w, fmt)
     vi = synth.make_verify_inputs(synth.shrink(cfg, k_lo=0, k_hi=0), num_drafts=np.full(len(lens), cfg.K, np.int32))
     t = time.perf_counter()
     for _ in range(sample_steps):
@@ -668,7 +707,7 @@ def run_reference(args, rank, world):
     lens = synth.context_lengths(cfg)
     kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
     di = synth.make_draft_inputs(cfg, w, lens)
-    W = O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
+    W = oracle_head(cfg, w, args.weights)
     vi = synth.make_verify_inputs(synth.shrink(cfg, k_lo=0, k_hi=0), num_drafts=np.full(len(lens), cfg.K, np.int32))
     hid, emb = O.widen(di.hidden, cfg.dtype), O.widen(di.embeds, cfg.dtype)
 
@@ -717,6 +756,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--persistent-max-batch", type=int, default=0,
                     help="largest batch for the persistent draft kernel (0: never, the library default)")
+    ap.add_argument("--weights", choices=["dense", "int4_g64"], default="dense",
+                    help="weight format of the head: dense (the workload's dtype) or the quantized format "
+                         "(int4 group-64 projections, int8 per-row embedding / LM head)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")

@@ -57,6 +57,17 @@ typedef enum {
 
 typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
 
+/* Storage of the head's weights inside the context.  DENSE: the caller's
+ * tensors are read in place (dtype).  INT4_G64: the format of the pages'
+ * quantized MTP component ("Why MTP gets its own quantization
+ * configuration": 4-bit asymmetric, group size 64, INT8 symmetric backup):
+ * mtp_init quantizes the caller's bf16 weights once into context-owned
+ * buffers -- projections to INT4 with groups of 64 input columns
+ * (mtp_quantize_int4_g64), the shared embedding / LM head to INT8 per row
+ * (mtp_quantize_int8_rows) -- and every draft reads only those.  Requires
+ * bf16, max_batch <= 4 and hidden, ffn, n_q_heads*head_dim multiples of 1024. */
+typedef enum { MTP_WEIGHTS_DENSE = 0, MTP_WEIGHTS_INT4_G64 = 1 } mtp_weight_format;
+
 /* Shape of the MTP head and the limits of one context. */
 typedef struct {
   int hidden;            /* H; multiple of 8                                  */
@@ -81,6 +92,7 @@ typedef struct {
                             (bf16, head_dim 128) instead of the per-step
                             streamed kernels; 0 or negative = never (the
                             default); capped at 4 and at max_batch          */
+  int weight_format;     /* mtp_weight_format; 0 = dense                     */
 } mtp_config;
 
 /* Borrowed head weights (device pointers, layouts [out, in] row-major).
@@ -216,6 +228,24 @@ mtp_status mtp_kv_rollback(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv);
  * zeroed, seq_len[b] = new_len[b], pending[b] = 0.  Requires
  * 0 <= new_len[b] <= seq_len[b] + pending[b] (device-checked). */
 mtp_status mtp_kv_truncate(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv, const int32_t* new_len);
+
+/* INT4 asymmetric quantization of a bf16 matrix [rows, cols] (row-major,
+ * cols a multiple of 64) in groups of 64 consecutive columns: for a group,
+ * lo = min(min w, 0), hi = max(max w, 0), s = (hi - lo) / 15 (1 if 0),
+ * z = clamp(rint(-lo / s), 0, 15), q = clamp(rint(w / s) + z, 0, 15), all in
+ * IEEE fp32 with round-half-to-even.  Outputs (device, caller-owned): q
+ * [rows, cols/2] bytes, column 2k in the low nibble of byte k; scales [rows,
+ * cols/64] fp16 (s rounded to nearest even); zeros [rows, cols/64] bytes.
+ * Dequantized weight: (q - z) * scale.  Asynchronous on `stream`;
+ * MTP_ERR_INVALID for NULL pointers or a bad shape. */
+mtp_status mtp_quantize_int4_g64(void* stream, const void* w, int rows, int cols, void* q, void* scales,
+                                 void* zeros);
+
+/* INT8 symmetric quantization of a bf16 matrix [rows, cols] per row:
+ * s = max |w| / 127 (1 if 0), q = clamp(rint(w / s), -127, 127) in IEEE fp32
+ * with round-half-to-even.  Outputs: q [rows, cols] int8, scales [rows] fp16.
+ * Dequantized weight: q * scale. */
+mtp_status mtp_quantize_int8_rows(void* stream, const void* w, int rows, int cols, void* q, void* scales);
 
 /* Synchronise the context's device, return the device error word as an
  * mtp_status (MTP_OK if none) and clear it. */

@@ -20,7 +20,7 @@ from ._lib import (  # noqa: F401
     KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
     MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
     MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
-    MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
+    MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
 )
 
 _clib = L.load()
@@ -97,10 +97,11 @@ class Context:
 
 def make_config(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps=1e-6, rope_theta=1e6, dtype="bf16",
                 max_batch=1, max_k=5, block_size=16, max_pos=32768, tc_min_batch=0,
-                persistent_max_batch=0) -> MTPConfig:
+                persistent_max_batch=0, weight_format="dense") -> MTPConfig:
     code = MTP_DTYPE_BF16 if dtype in ("bf16", MTP_DTYPE_BF16, torch.bfloat16) else MTP_DTYPE_F32
+    wf = MTP_WEIGHTS_INT4_G64 if weight_format in ("int4_g64", MTP_WEIGHTS_INT4_G64) else MTP_WEIGHTS_DENSE
     return MTPConfig(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, eps, rope_theta, code, max_batch, max_k,
-                     block_size, max_pos, tc_min_batch, persistent_max_batch)
+                     block_size, max_pos, tc_min_batch, persistent_max_batch, wf)
 
 
 def mtp_init(cfg: MTPConfig, weights: Optional[Dict[str, torch.Tensor]] = None, device: Optional[int] = None
@@ -159,6 +160,25 @@ def mtp_verify_noalloc(target_logits: torch.Tensor, row_offsets: torch.Tensor, d
                                     int(drafts.shape[1]), _ptr(num_drafts, torch.int32, "num_drafts"),
                                     _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus")),
            "mtp_verify_noalloc")
+
+
+def mtp_quantize_int4_g64(w: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,
+                          stream=None) -> None:
+    """INT4 asymmetric group-64 quantization of a bf16 matrix [rows, cols]:
+    q [rows, cols/2] uint8, scales [rows, cols/64] fp16 (or int16 bits),
+    zeros [rows, cols/64] uint8."""
+    rows, cols = int(w.shape[0]), int(w.shape[1])
+    _check(_clib.mtp_quantize_int4_g64(_stream(stream), _ptr(w, name="w"), rows, cols, _ptr(q, name="q"),
+                                       _ptr(scales, name="scales"), _ptr(zeros, name="zeros")),
+           "mtp_quantize_int4_g64")
+
+
+def mtp_quantize_int8_rows(w: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, stream=None) -> None:
+    """INT8 symmetric per-row quantization of a bf16 matrix [rows, cols]:
+    q [rows, cols] int8, scales [rows] fp16 (or int16 bits)."""
+    rows, cols = int(w.shape[0]), int(w.shape[1])
+    _check(_clib.mtp_quantize_int8_rows(_stream(stream), _ptr(w, name="w"), rows, cols, _ptr(q, name="q"),
+                                        _ptr(scales, name="scales")), "mtp_quantize_int8_rows")
 
 
 def mtp_kv_commit(ctx: Context, kv: KVCache, n_keep: torch.Tensor, stream=None) -> None:

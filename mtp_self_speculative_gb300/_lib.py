@@ -16,6 +16,7 @@ P_i32 = ctypes.c_void_p  # device int32 pointers are passed as plain addresses
 
 MTP_OK, MTP_ERR_INVALID, MTP_ERR_CUDA, MTP_ERR_OOM, MTP_ERR_CAPACITY, MTP_ERR_TIMEOUT, MTP_ERR_DEVICE_ARGS = range(7)
 MTP_DTYPE_F32, MTP_DTYPE_BF16 = 0, 1
+MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64 = 0, 1
 (MTP_KERNEL_EH_PROJ, MTP_KERNEL_QKV_ROPE, MTP_KERNEL_ATTENTION, MTP_KERNEL_O_PROJ, MTP_KERNEL_GATE_UP,
  MTP_KERNEL_DOWN, MTP_KERNEL_LM_HEAD, MTP_KERNEL_VERIFY, MTP_KERNEL_KV_EDIT, MTP_KERNEL_DRAFT_PERSISTENT,
  MTP_KERNEL_COUNT) = range(11)
@@ -27,7 +28,7 @@ class MTPConfig(ctypes.Structure):
     _fields_ = [("hidden", c_int), ("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
                 ("ffn", c_int), ("vocab", c_int), ("eps", c_float), ("rope_theta", c_float), ("dtype", c_int),
                 ("max_batch", c_int), ("max_k", c_int), ("block_size", c_int), ("max_pos", c_int),
-                ("tc_min_batch", c_int), ("persistent_max_batch", c_int)]
+                ("tc_min_batch", c_int), ("persistent_max_batch", c_int), ("weight_format", c_int)]
 
 
 WEIGHT_FIELDS = ["w_norm_h", "w_norm_e", "w_eh", "w_norm_in", "w_q", "w_k", "w_v", "w_o", "w_norm_post",
@@ -51,6 +52,8 @@ SIGNATURES = {
     "mtp_verify": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, P_i32, P_i32, c_int, P_i32, P_i32, P_i32]),
     "mtp_verify_noalloc": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int, P_i32, P_i32, c_int,
                                    P_i32, P_i32, P_i32]),
+    "mtp_quantize_int4_g64": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "mtp_quantize_int8_rows": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p]),
     "mtp_kv_commit": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
     "mtp_kv_commit_accepted": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32, c_int]),
     "mtp_kv_rollback": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV)]),

@@ -73,7 +73,66 @@ static bool config_ok(const mtp_config* c, bool with_weights) {
     if (c->hidden <= 0 || c->hidden % 8 || c->ffn <= 0 || c->ffn % 8) return false;
     if (!(c->eps > 0.0f) || !(c->rope_theta > 0.0f) || c->max_pos <= 0) return false;
   }
+  if (c->weight_format != MTP_WEIGHTS_DENSE && c->weight_format != MTP_WEIGHTS_INT4_G64) return false;
+  if (c->weight_format == MTP_WEIGHTS_INT4_G64) {
+    // quantized head: bf16 source weights, the small-batch kernels only, rows
+    // whose per-group metadata is a whole number of 16-byte bulk copies
+    if (!with_weights || c->dtype != MTP_DTYPE_BF16 || c->max_batch > 4) return false;
+    if (c->hidden % 1024 || c->ffn % 1024 || (c->n_q_heads * c->head_dim) % 1024) return false;
+  }
   return true;
+}
+
+// Quantize the caller's bf16 weights into context-owned INT4 / INT8 copies.
+static mtp_status quantize_head(mtp_ctx* ctx) {
+  const mtp_config& c = ctx->cfg;
+  const size_t H = c.hidden, F = c.ffn, V = c.vocab, qd = ctx->q_dim, kvd = ctx->kv_dim;
+  const size_t rows[8] = {H, qd, kvd, kvd, H, F, F, H};
+  const size_t cols[8] = {2 * H, H, H, H, qd, H, H, F};
+  const void* src[8] = {ctx->w.w_eh, ctx->w.w_q, ctx->w.w_k, ctx->w.w_v, ctx->w.w_o, ctx->w.w_gate, ctx->w.w_up,
+                        ctx->w.w_down};
+  const bool tied = ctx->w.lm_head == ctx->w.embed;
+  size_t off = 0, oq[8], os[8], oz[8];
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  for (int m = 0; m < 8; ++m) {
+    oq[m] = take(rows[m] * cols[m] / 2);
+    os[m] = take(rows[m] * (cols[m] / 64) * 2);
+    oz[m] = take(rows[m] * (cols[m] / 64));
+  }
+  const size_t o8 = take(V * H), os8 = take(V * 2);
+  const size_t o8l = tied ? o8 : take(V * H), os8l = tied ? os8 : take(V * 2);
+  if (cudaMalloc(&ctx->qw_buf, off) != cudaSuccess) {
+    cudaGetLastError();
+    ctx->qw_buf = nullptr;
+    return MTP_ERR_OOM;
+  }
+  char* base = (char*)ctx->qw_buf;
+  cudaError_t e = cudaSuccess;
+  for (int m = 0; m < 8 && e == cudaSuccess; ++m) {
+    ctx->qw_q4[m] = (uint8_t*)(base + oq[m]);
+    ctx->qw_s4[m] = (uint16_t*)(base + os[m]);
+    ctx->qw_z4[m] = (uint8_t*)(base + oz[m]);
+    e = launch_quant_int4(0, src[m], (int)rows[m], (int)cols[m], ctx->qw_q4[m], ctx->qw_s4[m], ctx->qw_z4[m]);
+  }
+  ctx->qw_q8 = (int8_t*)(base + o8);
+  ctx->qw_s8 = (uint16_t*)(base + os8);
+  ctx->qw_q8_lm = (int8_t*)(base + o8l);
+  ctx->qw_s8_lm = (uint16_t*)(base + os8l);
+  if (e == cudaSuccess) e = launch_quant_int8(0, ctx->w.embed, (int)V, (int)H, ctx->qw_q8, ctx->qw_s8);
+  if (e == cudaSuccess && !tied) e = launch_quant_int8(0, ctx->w.lm_head, (int)V, (int)H, ctx->qw_q8_lm, ctx->qw_s8_lm);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(ctx->qw_buf);
+    ctx->qw_buf = nullptr;
+    return MTP_ERR_CUDA;
+  }
+  ctx->quantized = 1;
+  return MTP_OK;
 }
 
 mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int device, mtp_ctx** out) {
@@ -191,7 +250,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // tensor-core path workspace
   ctx->tc_min_batch = c.tc_min_batch > 0 ? c.tc_min_batch : 5;
   if (with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128 && c.hidden % 128 == 0 && c.ffn % 64 == 0 &&
-      ctx->q_dim % 64 == 0 && c.max_batch >= ctx->tc_min_batch) {
+      ctx->q_dim % 64 == 0 && c.max_batch >= ctx->tc_min_batch && c.weight_format == MTP_WEIGHTS_DENSE) {
     const size_t mb = (size_t)c.max_batch;
     size_t o2 = 0;
     auto take2 = [&](size_t bytes) {
@@ -221,7 +280,8 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->p_max_batch = c.persistent_max_batch > 0 ? c.persistent_max_batch : 0;
   if (ctx->p_max_batch > 4) ctx->p_max_batch = 4;
   if (ctx->p_max_batch > c.max_batch) ctx->p_max_batch = c.max_batch;
-  if (!(with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128)) ctx->p_max_batch = 0;
+  if (!(with_w && c.dtype == MTP_DTYPE_BF16 && c.head_dim == 128) || c.weight_format != MTP_WEIGHTS_DENSE)
+    ctx->p_max_batch = 0;
   if (ctx->p_max_batch > 0) {
     const size_t pb = (size_t)ctx->p_max_batch;
     size_t o3 = 0;
@@ -237,6 +297,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     if (cudaMalloc(&ctx->p_ws, o3) != cudaSuccess || cudaMemset(ctx->p_ws, 0, o3) != cudaSuccess) {
       cudaGetLastError();
       if (ctx->p_ws) cudaFree(ctx->p_ws);
+  if (ctx->qw_buf) cudaFree(ctx->qw_buf);
       if (ctx->tc_ws) cudaFree(ctx->tc_ws);
       cudaFree(ctx->ws);
       free(ctx);
@@ -247,6 +308,13 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     ctx->p_seg_cnt = (int*)(pbase + p_cnt);
     ctx->p_keys = (unsigned long long*)(pbase + p_keys);
     ctx->p_gbar = (unsigned long long*)(pbase + p_bar);
+  }
+  if (c.weight_format == MTP_WEIGHTS_INT4_G64) {
+    const mtp_status st = quantize_head(ctx);
+    if (st != MTP_OK) {
+      mtp_destroy(ctx);
+      return st;
+    }
   }
   *out = ctx;
   return MTP_OK;
@@ -262,6 +330,7 @@ void mtp_destroy(mtp_ctx* ctx) {
   cudaFree(ctx->ws);
   if (ctx->tc_ws) cudaFree(ctx->tc_ws);
   if (ctx->p_ws) cudaFree(ctx->p_ws);
+  if (ctx->qw_buf) cudaFree(ctx->qw_buf);
   free(ctx->tc_plan_cache);
   free(ctx->attn_map_cache);
   free(ctx);
@@ -288,6 +357,14 @@ mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, cons
   if (!hidden || !embeds || !positions || !draft_ids || !kv_ok(kv)) return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  if (ctx->quantized) {
+    for (int k = 1; k <= K; ++k) {
+      cudaError_t e = launch_draft_step_q(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
+                                          logits, hidden_out);
+      if (e != cudaSuccess) return after_launch(e);
+    }
+    return after_launch(cudaGetLastError());
+  }
   if (persistent_supported(ctx, B))
     return after_launch(launch_draft_persistent(ctx, s, B, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
                                                 logits, hidden_out));

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/mtp.h"
@@ -244,6 +245,16 @@ struct mtp_ctx {
   int* p_seg_cnt;                // [p_max_batch * n_kv]
   unsigned long long* p_keys;    // [max_k, p_max_batch]
   unsigned long long* p_gbar;    // grid barrier: arrivals, completed barriers, abort flag (128 B apart)
+  // quantized head (weight_format MTP_WEIGHTS_INT4_G64): owned copies
+  int quantized;
+  void* qw_buf;
+  uint8_t* qw_q4[8];             // INT4 codes of eh, q, k, v, o, gate, up, down
+  uint16_t* qw_s4[8];            // fp16 scales [out, in / 64]
+  uint8_t* qw_z4[8];             // zero points [out, in / 64]
+  int8_t* qw_q8;                 // INT8 embedding [V, H]
+  uint16_t* qw_s8;               // fp16 row scales [V]
+  int8_t* qw_q8_lm;              // INT8 LM head (== qw_q8 when tied)
+  uint16_t* qw_s8_lm;
   int p_nslots[3];               // launch plan per batch width 1, 2, 4 (0 = not yet made)
   int p_warps[3];
   size_t p_smem[3];
@@ -280,6 +291,12 @@ cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K,
                               const void* embeds, const int32_t* positions, const mtp_kv* kv,
                               const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
 cudaError_t launch_attention(mtp_ctx* ctx, cudaStream_t s, int B, int k, const mtp_kv* kv);
+cudaError_t launch_draft_step_q(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
+                                const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                                const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out);
+cudaError_t launch_quant_int4(cudaStream_t s, const void* w, int rows, int cols, void* q, void* scales,
+                              void* zeros);
+cudaError_t launch_quant_int8(cudaStream_t s, const void* w, int rows, int cols, void* q, void* scales);
 bool tc_supported(const mtp_ctx* ctx, int B);
 bool persistent_supported(const mtp_ctx* ctx, int B);
 cudaError_t launch_draft_persistent(mtp_ctx* ctx, cudaStream_t s, int B, int K, const void* hidden,

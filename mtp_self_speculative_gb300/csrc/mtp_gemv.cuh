@@ -1,0 +1,330 @@
+// Shared pieces of the small-batch projection kernels (bf16/fp32 streamed
+// GEMV in mtp_gemv.cu, quantized GEMV in mtp_quant.cu): the step arguments,
+// the row-pair mapping of every projection kind, input staging and the
+// epilogues ("MTP (Multi-Token Prediction)", "Architecture").
+#pragma once
+
+#include "mtp_common.cuh"
+
+namespace mtp {
+
+enum GemvKind { EH_PROJ = 0, QKV_ROPE = 1, O_PROJ = 2, GATE_UP = 3, DOWN = 4, LM_HEAD = 5 };
+
+template <typename T>
+struct StepArgs {
+  int B, H, q_dim, kv_dim, F, V, n_q, n_kv, hd, bs;
+  float eps;
+  int k, K;
+  int max_pos, num_blocks, max_blocks;
+  const T *w_norm_h, *w_norm_e, *w_eh, *w_norm_in, *w_q, *w_k, *w_v, *w_o;
+  const T *w_norm_post, *w_gate, *w_up, *w_down, *w_norm_f, *embed, *lm_head;
+  const T* hidden_in;
+  const T* embeds_in;
+  const int32_t* positions;
+  const int32_t* chain_ids;
+  int32_t* draft_ids;
+  float* logits;
+  float* hidden_out;
+  T* k_pool;
+  T* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_len;
+  int32_t* pending;
+  float *hid, *x, *q, *attn, *h1, *act;
+  unsigned long long* lm_keys;
+  int* lm_cnt;
+  int* err;
+  int* req_bad;
+  const float2* rope;
+  // Quantized head (null when dense): per projection kind (EH, QKV as q/k/v,
+  // O, gate, up, down) packed INT4 codes [out, in/2], fp16 scales and uint8
+  // zero points [out, in/64]; INT8 codes [V, H] and fp16 row scales [V] of
+  // the shared embedding / LM head.
+  const uint8_t *q4[8];
+  const uint16_t *s4[8];
+  const uint8_t *z4[8];
+  const int8_t* q8;
+  const uint16_t* s8;
+  const int8_t* q8_lm;     // LM head codes / scales (the embedding's when tied)
+  const uint16_t* s8_lm;
+};
+
+// Matrix slots of the quantized projections in StepArgs::q4/s4/z4.
+enum QMat { QM_EH = 0, QM_Q = 1, QM_K = 2, QM_V = 3, QM_O = 4, QM_GATE = 5, QM_UP = 6, QM_DOWN = 7 };
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 8;
+
+template <typename T>
+__device__ __forceinline__ int gemv_cols(const StepArgs<T>& a, int kind) {
+  switch (kind) {
+    case EH_PROJ: return 2 * a.H;
+    case O_PROJ: return a.q_dim;
+    case DOWN: return a.F;
+    default: return a.H;
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ int gemv_pairs(const StepArgs<T>& a, int kind) {
+  switch (kind) {
+    case EH_PROJ: return a.H / 2;
+    case QKV_ROPE: return (a.q_dim + 2 * a.kv_dim) / 2;
+    case O_PROJ: return a.H / 2;
+    case GATE_UP: return a.F;
+    case DOWN: return a.H / 2;
+    default: return (a.V + 1) / 2;
+  }
+}
+
+// Rows (r0, r1) of pair p and their weight pointers.  r1 < 0: no second row.
+template <typename T, int KIND>
+__device__ __forceinline__ void pair_rows(const StepArgs<T>& a, int p, int C, int& r0, int& r1,
+                                          const T*& w0, const T*& w1) {
+  if constexpr (KIND == QKV_ROPE) {
+    const int hp = a.hd / 2;
+    const int grp = p / hp, i = p - grp * hp;
+    r0 = grp * a.hd + i;
+    r1 = r0 + hp;
+    const T* base;
+    int rr;
+    if (r0 < a.q_dim) { base = a.w_q; rr = r0; }
+    else if (r0 < a.q_dim + a.kv_dim) { base = a.w_k; rr = r0 - a.q_dim; }
+    else { base = a.w_v; rr = r0 - a.q_dim - a.kv_dim; }
+    w0 = base + (size_t)rr * C;
+    w1 = w0 + (size_t)hp * C;
+  } else if constexpr (KIND == GATE_UP) {
+    r0 = p;
+    r1 = p;
+    w0 = a.w_gate + (size_t)p * C;
+    w1 = a.w_up + (size_t)p * C;
+  } else {
+    const T* W = (KIND == EH_PROJ) ? a.w_eh : (KIND == O_PROJ) ? a.w_o : (KIND == DOWN) ? a.w_down : a.lm_head;
+    const int R = (KIND == LM_HEAD) ? a.V : a.H;
+    r0 = 2 * p;
+    r1 = (2 * p + 1 < R) ? 2 * p + 1 : -1;
+    w0 = W + (size_t)r0 * C;
+    w1 = (r1 >= 0) ? w0 + C : nullptr;
+  }
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+// Epilogue for one pair and one batch row (runs on lane 0).
+template <typename T, int KIND>
+__device__ __forceinline__ void epilogue(const StepArgs<T>& a, int b, int r0, int r1, float v0, float v1,
+                                         unsigned long long& best) {
+  if constexpr (KIND == EH_PROJ) {
+    a.x[(size_t)b * a.H + r0] = v0;
+    if (r1 >= 0) a.x[(size_t)b * a.H + r1] = v1;
+  } else if constexpr (KIND == O_PROJ) {
+    a.h1[(size_t)b * a.H + r0] = a.x[(size_t)b * a.H + r0] + v0;
+    if (r1 >= 0) a.h1[(size_t)b * a.H + r1] = a.x[(size_t)b * a.H + r1] + v1;
+  } else if constexpr (KIND == DOWN) {
+    const float o0 = a.h1[(size_t)b * a.H + r0] + v0;
+    a.hid[(size_t)b * a.H + r0] = o0;
+    if (a.hidden_out && a.k == a.K) a.hidden_out[(size_t)b * a.H + r0] = o0;
+    if (r1 >= 0) {
+      const float o1 = a.h1[(size_t)b * a.H + r1] + v1;
+      a.hid[(size_t)b * a.H + r1] = o1;
+      if (a.hidden_out && a.k == a.K) a.hidden_out[(size_t)b * a.H + r1] = o1;
+    }
+  } else if constexpr (KIND == GATE_UP) {
+    a.act[(size_t)b * a.F + r0] = silu(v0) * v1;
+  } else if constexpr (KIND == LM_HEAD) {
+    float* lg = a.logits ? a.logits + ((size_t)b * a.K + (a.k - 1)) * a.V : nullptr;
+    if (lg) lg[r0] = v0;
+    best = umax64(best, argmax_key(v0, (uint32_t)r0));
+    if (r1 >= 0) {
+      if (lg) lg[r1] = v1;
+      best = umax64(best, argmax_key(v1, (uint32_t)r1));
+    }
+  } else {  // QKV_ROPE
+    const int hp = a.hd / 2;
+    const int grp = r0 / a.hd, i = r0 - grp * a.hd;
+    const int pos = a.positions[b] + a.k - 1;
+    if (pos < 0 || pos >= a.max_pos) {
+      set_error(a.err, MTP_ERR_CAPACITY);
+      return;
+    }
+    if (grp < a.n_q) {
+      const float2 cs = a.rope[(size_t)pos * hp + i];
+      float* qb = a.q + (size_t)b * a.q_dim;
+      qb[r0] = v0 * cs.x - v1 * cs.y;
+      qb[r1] = v1 * cs.x + v0 * cs.y;
+      return;
+    }
+    if (__ldcg(a.req_bad + b) || a.pending[b] != a.k - 1) {
+      set_error(a.err, MTP_ERR_DEVICE_ARGS);
+      return;
+    }
+    const int slot = a.seq_len[b] + a.k - 1;
+    const int bi = slot / a.bs, off = slot - bi * a.bs;
+    int blk = (bi < a.max_blocks && slot >= 0) ? a.block_table[(size_t)b * a.max_blocks + bi] : -1;
+    if (blk < 0 || blk >= a.num_blocks) {
+      set_error(a.err, MTP_ERR_CAPACITY);
+      return;
+    }
+    float o0 = v0, o1 = v1;
+    T* pool;
+    int g;
+    if (grp < a.n_q + a.n_kv) {
+      const float2 cs = a.rope[(size_t)pos * hp + i];
+      o0 = v0 * cs.x - v1 * cs.y;
+      o1 = v1 * cs.x + v0 * cs.y;
+      pool = a.k_pool;
+      g = grp - a.n_q;
+    } else {
+      pool = a.v_pool;
+      g = grp - a.n_q - a.n_kv;
+    }
+    T* dst = pool + (((size_t)blk * a.n_kv + g) * a.bs + off) * a.hd;
+    Elem<T>::store1(dst + i, o0);
+    Elem<T>::store1(dst + i + hp, o1);
+  }
+}
+
+constexpr int kTmaConsumers = 8;
+constexpr int kTmaThreads = 32 * (kTmaConsumers + 1);
+constexpr int kMaxTmaStages = 16;
+constexpr uint32_t kGemvWaitLimit = 1u << 24;
+
+__device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Eight consecutive values of an fp32 (activations, L2 only) or T row.
+template <typename T, typename S>
+__device__ __forceinline__ void load8_row(const S* p, float (&x)[8]) {
+  if constexpr (sizeof(S) == 4) {
+    const float4 t0 = __ldcg(reinterpret_cast<const float4*>(p));
+    const float4 t1 = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = t0.x; x[1] = t0.y; x[2] = t0.z; x[3] = t0.w; x[4] = t1.x; x[5] = t1.y; x[6] = t1.z; x[7] = t1.w;
+  } else {
+    const uint4 t = __ldg(reinterpret_cast<const uint4*>(p));
+    x[0] = bf16_lo(t.x); x[1] = bf16_hi(t.x); x[2] = bf16_lo(t.y); x[3] = bf16_hi(t.y);
+    x[4] = bf16_lo(t.z); x[5] = bf16_hi(t.z); x[6] = bf16_lo(t.w); x[7] = bf16_hi(t.w);
+  }
+}
+
+// Copy n values (fp32 or T; n % 8 == 0) into dst (fp32) times the norm
+// weight w (if any); returns this thread's sum of squares of the raw
+// values.  Source and weight loads are independent and vectorised, so a
+// 4096-wide row costs each consumer thread two groups: about one L2 round
+// trip.
+template <typename T, typename S>
+__device__ __forceinline__ float cons_stage_raw(float* dst, const S* src, int n, const T* w) {
+  const int ct = threadIdx.x - 32;
+  float ss = 0.0f;
+#pragma unroll 2
+  for (int i8 = ct; i8 < (n >> 3); i8 += 256) {
+    float x[8], wv[8];
+    load8_row<T, S>(src + (size_t)i8 * 8, x);
+    if (w) load8_row<T, T>(w + (size_t)i8 * 8, wv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ss = fmaf(x[e], x[e], ss);
+      if (w) x[e] *= wv[e];
+    }
+    float4* d = reinterpret_cast<float4*>(dst + (size_t)i8 * 8);
+    d[0] = make_float4(x[0], x[1], x[2], x[3]);
+    d[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+  return ss;
+}
+
+// Stage the normalised input row(s) of all nb requests: one pass that stores
+// x * w and sums x^2 for every vector, one block reduction for all of them,
+// then the scalar RMS factors applied in shared memory.
+// The same for one row of the INT8 embedding table: q8 codes times the row
+// scale, times the norm weight w.
+template <typename T>
+__device__ __forceinline__ float cons_stage_raw_q8(float* dst, const int8_t* src, float scale, int n, const T* w) {
+  const int ct = threadIdx.x - 32;
+  float ss = 0.0f;
+#pragma unroll 2
+  for (int i8 = ct; i8 < (n >> 3); i8 += 256) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)i8 * 8));
+    float x[8], wv[8];
+    load8_row<T, T>(w + (size_t)i8 * 8, wv);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t word = e < 4 ? u.x : u.y;
+      x[e] = (float)(int8_t)((word >> (8 * (e & 3))) & 0xFFu) * scale;
+      ss = fmaf(x[e], x[e], ss);
+      x[e] *= wv[e];
+    }
+    float4* d = reinterpret_cast<float4*>(dst + (size_t)i8 * 8);
+    d[0] = make_float4(x[0], x[1], x[2], x[3]);
+    d[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+  return ss;
+}
+
+template <typename T, int KIND>
+__device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
+  constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
+  float ss[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss[i] = 0.0f;
+  for (int b = 0; b < nb; ++b) {
+    float* dst = xs + (size_t)b * C;
+    float s0 = 0.0f, s1 = 0.0f;
+    if constexpr (KIND == EH_PROJ) {
+      if (a.k == 1) {
+        s0 = cons_stage_raw<T, T>(dst, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h);
+        s1 = cons_stage_raw<T, T>(dst + a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e);
+      } else {
+        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
+                             : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+        s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_h);
+        if (id < 0 || id >= a.V) {
+          if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
+          id = 0;
+        }
+        if (a.q8)  // quantized shared embedding: the same table as the LM head
+          s1 = cons_stage_raw_q8<T>(dst + a.H, a.q8 + (size_t)id * a.H,
+                                    __half2float(__ushort_as_half(__ldg(a.s8 + id))), a.H, a.w_norm_e);
+        else
+          s1 = cons_stage_raw<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
+      }
+    } else if constexpr (KIND == QKV_ROPE) {
+      s0 = cons_stage_raw<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
+    } else if constexpr (KIND == O_PROJ) {
+      cons_stage_raw<T, float>(dst, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr);
+    } else if constexpr (KIND == GATE_UP) {
+      s0 = cons_stage_raw<T, float>(dst, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post);
+    } else if constexpr (KIND == DOWN) {
+      cons_stage_raw<T, float>(dst, a.act + (size_t)b * a.F, a.F, (const T*)nullptr);
+    } else {
+      s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j == b) {
+        ss[2 * j] = s0;
+        ss[2 * j + 1] = s1;
+      }
+  }
+  if constexpr (kNorm) {
+    const int cw = (threadIdx.x >> 5) - 1, l = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float t = warp_sum(ss[i]);
+      if (l == 0 && i < 2 * nb) red[cw * 8 + i] = t;
+    }
+    cons_bar();
+    const int ct = threadIdx.x - 32;
+    const int nvec = (KIND == EH_PROJ) ? 2 : 1;
+    for (int b = 0; b < nb; ++b)
+      for (int v = 0; v < nvec; ++v) {
+        float t = 0.0f;
+        for (int w = 0; w < kTmaConsumers; ++w) t += red[w * 8 + 2 * b + v];
+        const float sc = rsqrtf(t / (float)a.H + a.eps);
+        float* dst = xs + (size_t)b * C + (size_t)v * a.H;
+        for (int i = ct; i < a.H; i += 256) dst[i] *= sc;
+      }
+  }
+  cons_bar();
+}
+
+}  // namespace mtp

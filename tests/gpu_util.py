@@ -43,15 +43,18 @@ def download_kv(kvd) -> synth.KVState:
 
 
 def make_context(cfg: synth.MTPShape, wdev=None, max_batch=None, max_k=None, max_pos=None, tc_min_batch=0,
-                 persistent_max_batch=0):
+                 persistent_max_batch=0, weight_format="dense"):
     import mtp_self_speculative_gb300 as M
     c = M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps, cfg.rope_theta,
                       cfg.dtype, max_batch or cfg.batch, max_k or cfg.K, cfg.block_size,
-                      max_pos or (cfg.ctx_hi + 64), tc_min_batch, persistent_max_batch)
+                      max_pos or (cfg.ctx_hi + 64), tc_min_batch, persistent_max_batch, weight_format)
     return M.mtp_init(c, wdev)
 
 
-def oracle_weights(cfg: synth.MTPShape, w) -> O.MTPWeights64:
+def oracle_weights(cfg: synth.MTPShape, w, weight_format="dense") -> O.MTPWeights64:
+    if weight_format == "int4_g64":
+        from oracle import quant
+        return quant.quantized_weights(w, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
     return O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
 
 

@@ -19,8 +19,11 @@ pytestmark = pytest.mark.gpu
 
 
 class Case:
-    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77, tc_min_batch=0, persistent_max_batch=0):
+    def __init__(self, cfg, norm="ones", lens=None, K=None, chain_stream=77, tc_min_batch=0, persistent_max_batch=0,
+                 weight_format="dense"):
         self.cfg = cfg
+        self.weight_format = weight_format
+        self._W = None
         self.K = K or cfg.K
         self.w = synth.make_weights(cfg, norm=norm)
         self.lens = synth.context_lengths(cfg) if lens is None else np.asarray(lens, dtype=np.int32)
@@ -31,7 +34,7 @@ class Case:
         self.wdev = upload_weights(self.w)
         self.ctx = make_context(cfg, self.wdev, max_batch=self.B, max_k=self.K,
                                 max_pos=int(self.lens.max()) + self.K + 8, tc_min_batch=tc_min_batch,
-                                persistent_max_batch=persistent_max_batch)
+                                persistent_max_batch=persistent_max_batch, weight_format=weight_format)
         self.inputs = (dev(self.di.hidden), dev(self.di.embeds), dev(self.di.positions))
 
     def gpu_draft(self, forced=True, kvd=None):
@@ -51,7 +54,9 @@ class Case:
         """Oracle draft on ``subset``; appends into ``kv`` (default: a copy of
         the initial cache)."""
         cfg = self.cfg
-        W = oracle_weights(cfg, self.w)
+        if self._W is None:
+            self._W = oracle_weights(cfg, self.w, self.weight_format)
+        W = self._W
         kv = self.kv0.copy() if kv is None else kv
         view = synth.KVState(kv.k_pool, kv.v_pool, kv.block_table[subset], kv.seq_len[subset].copy(),
                              np.zeros(len(subset), dtype=np.int32), kv.block_size)
