@@ -83,57 +83,6 @@ static bool config_ok(const mtp_config* c, bool with_weights) {
   return true;
 }
 
-// Quantize the caller's bf16 weights into context-owned INT4 / INT8 copies.
-static mtp_status quantize_head(mtp_ctx* ctx) {
-  const mtp_config& c = ctx->cfg;
-  const size_t H = c.hidden, F = c.ffn, V = c.vocab, qd = ctx->q_dim, kvd = ctx->kv_dim;
-  const size_t rows[8] = {H, qd, kvd, kvd, H, F, F, H};
-  const size_t cols[8] = {2 * H, H, H, H, qd, H, H, F};
-  const void* src[8] = {ctx->w.w_eh, ctx->w.w_q, ctx->w.w_k, ctx->w.w_v, ctx->w.w_o, ctx->w.w_gate, ctx->w.w_up,
-                        ctx->w.w_down};
-  const bool tied = ctx->w.lm_head == ctx->w.embed;
-  size_t off = 0, oq[8], os[8], oz[8];
-  auto take = [&](size_t bytes) {
-    const size_t o = off;
-    off = align_up(off + bytes, 256);
-    return o;
-  };
-  for (int m = 0; m < 8; ++m) {
-    oq[m] = take(rows[m] * cols[m] / 2);
-    os[m] = take(rows[m] * (cols[m] / 64) * 2);
-    oz[m] = take(rows[m] * (cols[m] / 64));
-  }
-  const size_t o8 = take(V * H), os8 = take(V * 2);
-  const size_t o8l = tied ? o8 : take(V * H), os8l = tied ? os8 : take(V * 2);
-  if (cudaMalloc(&ctx->qw_buf, off) != cudaSuccess) {
-    cudaGetLastError();
-    ctx->qw_buf = nullptr;
-    return MTP_ERR_OOM;
-  }
-  char* base = (char*)ctx->qw_buf;
-  cudaError_t e = cudaSuccess;
-  for (int m = 0; m < 8 && e == cudaSuccess; ++m) {
-    ctx->qw_q4[m] = (uint8_t*)(base + oq[m]);
-    ctx->qw_s4[m] = (uint16_t*)(base + os[m]);
-    ctx->qw_z4[m] = (uint8_t*)(base + oz[m]);
-    e = launch_quant_int4(0, src[m], (int)rows[m], (int)cols[m], ctx->qw_q4[m], ctx->qw_s4[m], ctx->qw_z4[m]);
-  }
-  ctx->qw_q8 = (int8_t*)(base + o8);
-  ctx->qw_s8 = (uint16_t*)(base + os8);
-  ctx->qw_q8_lm = (int8_t*)(base + o8l);
-  ctx->qw_s8_lm = (uint16_t*)(base + os8l);
-  if (e == cudaSuccess) e = launch_quant_int8(0, ctx->w.embed, (int)V, (int)H, ctx->qw_q8, ctx->qw_s8);
-  if (e == cudaSuccess && !tied) e = launch_quant_int8(0, ctx->w.lm_head, (int)V, (int)H, ctx->qw_q8_lm, ctx->qw_s8_lm);
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(ctx->qw_buf);
-    ctx->qw_buf = nullptr;
-    return MTP_ERR_CUDA;
-  }
-  ctx->quantized = 1;
-  return MTP_OK;
-}
 
 mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int device, mtp_ctx** out) {
   if (!out) return MTP_ERR_INVALID;

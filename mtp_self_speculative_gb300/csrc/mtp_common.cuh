@@ -154,6 +154,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false if the phase did not complete within `limit` polls.
+// Non-blocking probe of a phase (producers that serve several queues).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -248,13 +258,11 @@ struct mtp_ctx {
   // quantized head (weight_format MTP_WEIGHTS_INT4_G64): owned copies
   int quantized;
   void* qw_buf;
-  uint8_t* qw_q4[8];             // INT4 codes of eh, q, k, v, o, gate, up, down
-  uint16_t* qw_s4[8];            // fp16 scales [out, in / 64]
-  uint8_t* qw_z4[8];             // zero points [out, in / 64]
-  int8_t* qw_q8;                 // INT8 embedding [V, H]
+  uint8_t* qw_tiles[6];          // per projection kind (and the LM head): fragment-ordered tiles
+  int8_t* qw_q8;                 // INT8 embedding [V, H] (row gather for the next step's input)
   uint16_t* qw_s8;               // fp16 row scales [V]
-  int8_t* qw_q8_lm;              // INT8 LM head (== qw_q8 when tied)
-  uint16_t* qw_s8_lm;
+  uint16_t* qw_s8_lm;            // LM-head row scales (== qw_s8 when tied)
+  float qw_lm_sigma;             // power-of-two input scale of the LM head's fp16 operand
   int p_nslots[3];               // launch plan per batch width 1, 2, 4 (0 = not yet made)
   int p_warps[3];
   size_t p_smem[3];
@@ -297,6 +305,7 @@ cudaError_t launch_draft_step_q(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
 cudaError_t launch_quant_int4(cudaStream_t s, const void* w, int rows, int cols, void* q, void* scales,
                               void* zeros);
 cudaError_t launch_quant_int8(cudaStream_t s, const void* w, int rows, int cols, void* q, void* scales);
+mtp_status quantize_head(mtp_ctx* ctx);
 bool tc_supported(const mtp_ctx* ctx, int B);
 bool persistent_supported(const mtp_ctx* ctx, int B);
 cudaError_t launch_draft_persistent(mtp_ctx* ctx, cudaStream_t s, int B, int K, const void* hidden,

@@ -36,20 +36,18 @@ struct StepArgs {
   int* err;
   int* req_bad;
   const float2* rope;
-  // Quantized head (null when dense): per projection kind (EH, QKV as q/k/v,
-  // O, gate, up, down) packed INT4 codes [out, in/2], fp16 scales and uint8
-  // zero points [out, in/64]; INT8 codes [V, H] and fp16 row scales [V] of
-  // the shared embedding / LM head.
-  const uint8_t *q4[8];
-  const uint16_t *s4[8];
-  const uint8_t *z4[8];
+  // Quantized head (null when dense): fragment-ordered tile streams per
+  // GemvKind (INT4 projections, INT8 LM head), the INT8 embedding [V, H] with
+  // its fp16 row scales [V] (row gather), the LM head's row scales and the
+  // power-of-two scale of the LM head's fp16 input operand.
+  const uint8_t* qt[6];
   const int8_t* q8;
   const uint16_t* s8;
-  const int8_t* q8_lm;     // LM head codes / scales (the embedding's when tied)
   const uint16_t* s8_lm;
+  float lm_sigma;
 };
 
-// Matrix slots of the quantized projections in StepArgs::q4/s4/z4.
+// Source matrices of the quantized projections (canonical quantized copies).
 enum QMat { QM_EH = 0, QM_Q = 1, QM_K = 2, QM_V = 3, QM_O = 4, QM_GATE = 5, QM_UP = 6, QM_DOWN = 7 };
 
 constexpr int kThreads = 256;
@@ -235,31 +233,6 @@ __device__ __forceinline__ float cons_stage_raw(float* dst, const S* src, int n,
 // Stage the normalised input row(s) of all nb requests: one pass that stores
 // x * w and sums x^2 for every vector, one block reduction for all of them,
 // then the scalar RMS factors applied in shared memory.
-// The same for one row of the INT8 embedding table: q8 codes times the row
-// scale, times the norm weight w.
-template <typename T>
-__device__ __forceinline__ float cons_stage_raw_q8(float* dst, const int8_t* src, float scale, int n, const T* w) {
-  const int ct = threadIdx.x - 32;
-  float ss = 0.0f;
-#pragma unroll 2
-  for (int i8 = ct; i8 < (n >> 3); i8 += 256) {
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src + (size_t)i8 * 8));
-    float x[8], wv[8];
-    load8_row<T, T>(w + (size_t)i8 * 8, wv);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t word = e < 4 ? u.x : u.y;
-      x[e] = (float)(int8_t)((word >> (8 * (e & 3))) & 0xFFu) * scale;
-      ss = fmaf(x[e], x[e], ss);
-      x[e] *= wv[e];
-    }
-    float4* d = reinterpret_cast<float4*>(dst + (size_t)i8 * 8);
-    d[0] = make_float4(x[0], x[1], x[2], x[3]);
-    d[1] = make_float4(x[4], x[5], x[6], x[7]);
-  }
-  return ss;
-}
-
 template <typename T, int KIND>
 __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
   constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
@@ -281,11 +254,7 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
           if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
           id = 0;
         }
-        if (a.q8)  // quantized shared embedding: the same table as the LM head
-          s1 = cons_stage_raw_q8<T>(dst + a.H, a.q8 + (size_t)id * a.H,
-                                    __half2float(__ushort_as_half(__ldg(a.s8 + id))), a.H, a.w_norm_e);
-        else
-          s1 = cons_stage_raw<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
+        s1 = cons_stage_raw<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
       }
     } else if constexpr (KIND == QKV_ROPE) {
       s0 = cons_stage_raw<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
