@@ -100,10 +100,9 @@ cudaError_t launch_quant_int8(cudaStream_t s, const void* w, int rows, int cols,
 
 constexpr int kQ4Tile = 560;    // 512 B codes (16 B a lane), 8 scale pairs, 8 zero-point pairs
 constexpr int kQ8Tile = 1024;   // two 512 B halves (16 B a lane each)
-constexpr int kQ4UnitBytes = 9 * 1024;    // streamed unit (one bulk copy) at most: INT4 tiles
+constexpr int kQ4UnitBytes = 36 * 1024;   // streamed unit (one bulk copy) at most: INT4 tiles
 constexpr int kQ8UnitBytes = 16 * 1024;   // the same for the INT8 LM head
 constexpr int kQStages = 32;    // ring stages at most
-constexpr int kQMaxRb = 16;     // row blocks of one CTA in the projection kernel at most
 
 // Canonical quantized copies of the eight projection matrices.
 struct QCanon {
@@ -336,6 +335,41 @@ __device__ __forceinline__ void q_load16(const StepArgs<uint16_t>& a, int b, int
 
 constexpr int kStageRegItems = 2;   // 16-value items a thread keeps in registers between the passes
 
+// Item idx = (b, group, k-step j), j fastest: batch row, first column.
+__device__ __forceinline__ void q_item(int idx, int G, int& b, int& c) {
+  const int bg = idx >> 2;
+  b = bg / G;
+  c = 64 * (bg - b * G) + 16 * (idx & 3);
+}
+
+// The norm weights of a thread's register items (constant: loaded before
+// the dependency wait, so that the staging after it needs one round trip).
+template <int KIND>
+__device__ __forceinline__ void stage_q_weights(const StepArgs<uint16_t>& a, int C, int nb,
+                                                float (&wr)[kStageRegItems][16]) {
+  if constexpr (KIND != O_PROJ && KIND != DOWN) {
+    const int ct = threadIdx.x - 32;
+    const int G = C / 64;
+#pragma unroll
+    for (int it = 0; it < kStageRegItems; ++it) {
+      const int idx = ct + 256 * it;
+      if (idx < nb * G * 4) {
+        int b, c;
+        q_item(idx, G, b, c);
+        float w0[8], w1[8];
+        const uint16_t* wp = q_norm_weight<KIND>(a, c);
+        load8_row<uint16_t, uint16_t>(wp, w0);
+        load8_row<uint16_t, uint16_t>(wp + 8, w1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wr[it][e] = w0[e];
+          wr[it][8 + e] = w1[e];
+        }
+      }
+    }
+  }
+}
+
 // Stage the B operand of all nb batch rows: y = x * rms factor * norm weight
 // (RMSNorm kinds; EH normalises its two halves separately), times `sigma`,
 // rounded to bf16 (F16 false) or fp16 (F16 true), in the register order of
@@ -351,7 +385,7 @@ constexpr int kStageRegItems = 2;   // 16-value items a thread keeps in register
 // once, all loads in flight together.
 template <int KIND, bool F16>
 __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, float* Xs, int C, int nb, float sigma,
-                               float* red, int* sid, float* srs) {
+                               float* red, int* sid, float* srs, const float (&wr)[kStageRegItems][16]) {
   constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
   const int ct = threadIdx.x - 32;
   const int cw = ct >> 5, l = ct & 31;
@@ -370,10 +404,8 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
     cons_bar();
   }
   auto item = [&](int idx, int& b, int& grp, int& c, int& id) {
-    const int bg = idx >> 2;
-    b = bg / G;
-    grp = bg - b * G;
-    c = 64 * grp + 16 * (idx & 3);
+    q_item(idx, G, b, c);
+    grp = c >> 6;
     id = (KIND == EH_PROJ && a.k > 1) ? sid[b] : 0;
   };
   float xr[kStageRegItems][16];
@@ -433,7 +465,7 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
       if ((i & 7) >= nb) Xs[i] = 0.0f;
   // rounding and layout; a warp runs while any of its lanes has an item, so
   // that the group sums can use full-warp shuffles
-  auto emit = [&](int idx, bool valid, float (&x)[16]) {
+  auto emit = [&](int idx, bool valid, float (&x)[16], const float (&w)[16]) {
     int b = 0, grp = 0, c = 0, id = 0;
     if (valid) item(idx, b, grp, c, id);
     float X = 0.0f;
@@ -441,15 +473,8 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
       const int half = (KIND == EH_PROJ && c >= a.H) ? 1 : 0;
       const float scale = (kNorm ? srs[2 * b + half] : 1.0f) * sigma;
       if constexpr (kNorm) {
-        float w0[8], w1[8];
-        const uint16_t* wp = q_norm_weight<KIND>(a, c);
-        load8_row<uint16_t, uint16_t>(wp, w0);
-        load8_row<uint16_t, uint16_t>(wp + 8, w1);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          x[e] *= w0[e];
-          x[8 + e] *= w1[e];
-        }
+        for (int e = 0; e < 16; ++e) x[e] *= w[e];
       }
       uint32_t h[16];
 #pragma unroll
@@ -478,19 +503,30 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
 #pragma unroll
   for (int it = 0; it < kStageRegItems; ++it) {
     const int idx = ct + 256 * it;
-    if (256 * it + 32 * cw < nitems) emit(idx, idx < nitems, xr[it]);
+    if (256 * it + 32 * cw < nitems) emit(idx, idx < nitems, xr[it], wr[it]);
   }
   for (int base = 256 * kStageRegItems; base < nitems; base += 256) {
     const int idx = base + ct;
     if (base + 32 * cw >= nitems) break;
-    float x[16];
+    float x[16], w[16];
     const bool valid = idx < nitems;
     if (valid) {
       int b, grp, c, id;
       item(idx, b, grp, c, id);
       q_load16<KIND>(a, b, c, id, x);
+      if constexpr (kNorm) {
+        float w0[8], w1[8];
+        const uint16_t* wp = q_norm_weight<KIND>(a, c);
+        load8_row<uint16_t, uint16_t>(wp, w0);
+        load8_row<uint16_t, uint16_t>(wp + 8, w1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          w[e] = w0[e];
+          w[8 + e] = w1[e];
+        }
+      }
     }
-    emit(idx, valid, x);
+    emit(idx, valid, x, w);
   }
   cons_bar();
 }
@@ -498,19 +534,21 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
 // ---------------------------------------------- INT4 projection kernel
 
 // One CTA owns row blocks [rb0, rb1) (16 rows = 8 epilogue pairs each) and
-// streams their tiles, gpc groups per unit, row block by row block; unit u
-// goes to stage u % stages and consumer warp u % consumers (stages a
-// multiple of consumers, so every stage serves one warp).  The producer
-// serves the warps' queues independently (a stage is refilled as soon as its
-// warp frees it), so a warp that falls behind does not hold up the others.  Per group a warp runs four m16n8k16 steps on
-// fresh accumulators and folds them into its running sums:
+// streams their tiles in chunks of gpc groups, one bulk copy per chunk
+// (copies of 16 KB and more keep the memory system busy; smaller ones do
+// not).  Every consumer warp takes part in every chunk: warp w handles
+// groups w, w + A, ... of it and releases the stage (its empty barrier
+// counts the A warps), so all warps walk the stages in the same order.  Per
+// group a warp runs four m16n8k16 steps on fresh accumulators and folds
+// them into its running sums of the row block:
 //   tot += s * (acc - (16 + z) * Xs[group][batch]),
-// since the operand holds 16 + code.  A warp's sums for a row block go to
-// shared memory when it moves on; after the stream the partials are added
-// in warp order (deterministic) and the pair epilogue runs.
+// since the operand holds 16 + code.  At the end of a row block the warps
+// park their sums in one half of a double buffer, meet at a barrier, and
+// warp rb % A adds them in warp order (deterministic) and runs the pair
+// epilogue while the others go on.
 template <int KIND, int NB>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-    gemv_q4_mma_kernel(const StepArgs<uint16_t> a, int stages, int consumers, int max_rb, int gpc) {
+    gemv_q4_mma_kernel(const StepArgs<uint16_t> a, int stages, int gpc) {
   extern __shared__ __align__(128) unsigned char gsm[];
   __shared__ __align__(8) uint64_t full_bar[kQStages], empty_bar[kQStages];
   __shared__ float red[kTmaConsumers * 8];
@@ -518,25 +556,25 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   __shared__ float srs[8];
 
   pdl_trigger();
+  constexpr int A = kTmaConsumers;
   const int C = q_cols(KIND, a.H, a.q_dim, a.F);
   const int G = C / 64;
   const int upr = G / gpc;
   const int NRB = q_pairs(KIND, a.H, a.q_dim, a.kv_dim, a.F, a.V) / 8;
   const int rb0 = (int)(((long long)blockIdx.x * NRB) / gridDim.x);
   const int rb1 = (int)(((long long)(blockIdx.x + 1) * NRB) / gridDim.x);
-  const int nrb = rb1 - rb0;
-  const int nunits = nrb * upr;
+  const int nunits = (rb1 - rb0) * upr;
   const uint32_t kUnit = (uint32_t)gpc * kQ4Tile;
   const int nb = a.B;
   unsigned char* xf = gsm + (size_t)stages * kUnit;                     // [G][2][nb * 4][16 B]
   float* Xs = reinterpret_cast<float*>(xf + (size_t)G * 2 * NB * 64);   // [G][8]
-  float* part = Xs + (size_t)G * 8;                                    // [max_rb][consumers][4][32]
+  float* pbuf = Xs + (size_t)G * 8;                                    // [2][A][4][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], A);
     }
     fence_mbar_init();
   }
@@ -546,125 +584,112 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       const unsigned char* src = a.qt[KIND] + (size_t)rb0 * G * kQ4Tile;
-      int nx[kTmaConsumers];   // next unit of each warp's queue
-#pragma unroll
-      for (int w = 0; w < kTmaConsumers; ++w) nx[w] = w;
-      int remaining = nunits;
-      uint32_t idle = 0;
-      while (remaining > 0) {
-        bool progress = false;
-#pragma unroll
-        for (int w = 0; w < kTmaConsumers; ++w) {
-          const int u = nx[w];
-          if (w >= consumers || u >= nunits) continue;
-          const int s = u % stages;
-          if (!mbar_test_wait(&empty_bar[s], (uint32_t)(((u / stages) & 1) ^ 1))) continue;
-          mbar_expect_tx(&full_bar[s], kUnit);
-          bulk_g2s_hint(gsm + (size_t)s * kUnit, src + (size_t)u * kUnit, kUnit, &full_bar[s], pol);
-          nx[w] = u + consumers;
-          --remaining;
-          progress = true;
-        }
-        if (progress) idle = 0;
-        else if (++idle > kGemvWaitLimit) {
+      int s = 0;
+      uint32_t ph = 0;
+      for (int u = 0; u < nunits; ++u) {
+        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u, kGemvWaitLimit)) {
           set_error(a.err, MTP_ERR_TIMEOUT);
           break;
+        }
+        mbar_expect_tx(&full_bar[s], kUnit);
+        bulk_g2s_hint(gsm + (size_t)s * kUnit, src + (size_t)u * kUnit, kUnit, &full_bar[s], pol);
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
         }
       }
     }
     return;
   }
 
+  float wr[kStageRegItems][16];
+  stage_q_weights<KIND>(a, C, nb, wr);
   pdl_wait();
   const int ct = threadIdx.x - 32;
   if (KIND == EH_PROJ && a.k == 1 && blockIdx.x == 0)
     for (int b = ct; b < a.B; b += 256) a.req_bad[b] = (a.pending[b] != 0);
-  for (int i = ct; i < nrb * consumers * 128; i += 256) part[i] = 0.0f;
-  stage_q_inputs<KIND, false>(a, xf, Xs, C, nb, 1.0f, red, sid, srs);
+  stage_q_inputs<KIND, false>(a, xf, Xs, C, nb, 1.0f, red, sid, srs, wr);
 
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
   const bool has_b = g < nb;
   const size_t xrow = (size_t)nb * 64;          // bytes of one (group, half) slice of xf
-  int cur = -1;
   float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int u = cw; cw < consumers && u < nunits; u += consumers) {
-    const int rbl = u / upr, ch = u - rbl * upr;
-    if (rbl != cur) {
-      if (cur >= 0) {
-        float* pp = part + ((size_t)cur * consumers + cw) * 128;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pp[e * 32 + lane] = tot[e];
-      }
-      cur = rbl;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) tot[e] = 0.0f;
-    }
-    const int s = u % stages;
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], (uint32_t)((u / stages) & 1), kGemvWaitLimit))) {
+  bool failed = false;                          // a wait ran out: skip the data, keep the barriers
+  int s = 0, rbl = 0, ch = 0;
+  uint32_t ph = 0;
+  unsigned long long best_unused = 0ull;
+  for (int u = 0; u < nunits; ++u) {
+    if (!failed && !__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], ph, kGemvWaitLimit))) {
       if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
-      break;
+      failed = true;
     }
-    const unsigned char* st = gsm + (size_t)s * kUnit;
+    if (!failed) {
+      const unsigned char* st = gsm + (size_t)s * kUnit;
 #pragma unroll 2
-    for (int gi = 0; gi < gpc; ++gi) {
-      const int grp = ch * gpc + gi;
-      const unsigned char* tp = st + gi * kQ4Tile;
-      const uint4 wq = *reinterpret_cast<const uint4*>(tp + 16 * lane);
-      const uint32_t sp = *reinterpret_cast<const uint32_t*>(tp + 512 + 4 * g);
-      const uint32_t zp = *reinterpret_cast<const uint16_t*>(tp + 544 + 2 * g);
-      uint4 xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
-      if (has_b) {
-        xa = *reinterpret_cast<const uint4*>(xf + (size_t)(grp * 2) * xrow + 16 * lane);
-        xb = *reinterpret_cast<const uint4*>(xf + (size_t)(grp * 2 + 1) * xrow + 16 * lane);
+      for (int gi = cw; gi < gpc; gi += A) {
+        const int grp = ch * gpc + gi;
+        const unsigned char* tp = st + gi * kQ4Tile;
+        const uint4 wq = *reinterpret_cast<const uint4*>(tp + 16 * lane);
+        const uint32_t sp = *reinterpret_cast<const uint32_t*>(tp + 512 + 4 * g);
+        const uint32_t zp = *reinterpret_cast<const uint16_t*>(tp + 544 + 2 * g);
+        uint4 xa = make_uint4(0, 0, 0, 0), xb = make_uint4(0, 0, 0, 0);
+        if (has_b) {
+          xa = *reinterpret_cast<const uint4*>(xf + (size_t)(grp * 2) * xrow + 16 * lane);
+          xb = *reinterpret_cast<const uint4*>(xf + (size_t)(grp * 2 + 1) * xrow + 16 * lane);
+        }
+        const float2 X = *reinterpret_cast<const float2*>(Xs + grp * 8 + 2 * t);
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        uint32_t r[4];
+        q4_operands(wq.x, r);
+        mma_bf16_zc(acc, r, xa.x, xa.y);
+        q4_operands(wq.y, r);
+        mma_bf16_zc(acc, r, xa.z, xa.w);
+        q4_operands(wq.z, r);
+        mma_bf16_zc(acc, r, xb.x, xb.y);
+        q4_operands(wq.w, r);
+        mma_bf16_zc(acc, r, xb.z, xb.w);
+        const float s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
+        const float s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
+        const float c0 = __uint_as_float(0x4B000000u | (zp & 0xFFu)) - 8388592.0f;   // 16 + z of row g
+        const float c1 = __uint_as_float(0x4B000000u | (zp >> 8)) - 8388592.0f;      // 16 + z of row g + 8
+        tot[0] = fmaf(s0, fmaf(-c0, X.x, acc[0]), tot[0]);
+        tot[1] = fmaf(s0, fmaf(-c0, X.y, acc[1]), tot[1]);
+        tot[2] = fmaf(s1, fmaf(-c1, X.x, acc[2]), tot[2]);
+        tot[3] = fmaf(s1, fmaf(-c1, X.y, acc[3]), tot[3]);
       }
-      const float2 X = *reinterpret_cast<const float2*>(Xs + grp * 8 + 2 * t);
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      uint32_t r[4];
-      q4_operands(wq.x, r);
-      mma_bf16_zc(acc, r, xa.x, xa.y);
-      q4_operands(wq.y, r);
-      mma_bf16_zc(acc, r, xa.z, xa.w);
-      q4_operands(wq.z, r);
-      mma_bf16_zc(acc, r, xb.x, xb.y);
-      q4_operands(wq.w, r);
-      mma_bf16_zc(acc, r, xb.z, xb.w);
-      const float s0 = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
-      const float s1 = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
-      const float c0 = __uint_as_float(0x4B000000u | (zp & 0xFFu)) - 8388592.0f;   // 16 + z of row g
-      const float c1 = __uint_as_float(0x4B000000u | (zp >> 8)) - 8388592.0f;      // 16 + z of row g + 8
-      tot[0] = fmaf(s0, fmaf(-c0, X.x, acc[0]), tot[0]);
-      tot[1] = fmaf(s0, fmaf(-c0, X.y, acc[1]), tot[1]);
-      tot[2] = fmaf(s1, fmaf(-c1, X.x, acc[2]), tot[2]);
-      tot[3] = fmaf(s1, fmaf(-c1, X.y, acc[3]), tot[3]);
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[s])) : "memory");
-  }
-  if (cur >= 0 && cw < consumers) {
-    float* pp = part + ((size_t)cur * consumers + cw) * 128;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) pp[e * 32 + lane] = tot[e];
-  }
-  cons_bar();
-
-  // combine the warps' partials (fixed order) and run the pair epilogue
-  unsigned long long best_unused = 0ull;
-  for (int i = ct; i < nrb * 32; i += 256) {
-    const int rbl = i >> 5, ln = i & 31;
-    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int w = 0; w < consumers; ++w) {
-      const float* pp = part + ((size_t)rbl * consumers + w) * 128;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] += pp[e * 32 + ln];
+    if (++s == stages) {
+      s = 0;
+      ph ^= 1u;
     }
-    const int gg = ln >> 2, tt = ln & 3;
-    int r0, r1, m0, m1, rr0, rr1;
-    qpair_rows<KIND>(a, 8 * (rb0 + rbl) + gg, r0, r1, m0, m1, rr0, rr1);
+    if (++ch == upr) {
+      // row block complete: park the sums, meet, one warp combines
+      float* pb = pbuf + ((size_t)(rbl & 1) * A + cw) * 128;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int b = 2 * tt + e;
-      if (b < nb) epilogue<uint16_t, KIND>(a, b, r0, r1, v[e], v[2 + e], best_unused);
+      for (int e = 0; e < 4; ++e) {
+        pb[e * 32 + lane] = tot[e];
+        tot[e] = 0.0f;
+      }
+      cons_bar();
+      if (cw == rbl % A && !failed) {
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const float* pr = pbuf + (size_t)(rbl & 1) * A * 128;
+        for (int w = 0; w < A; ++w)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] += pr[w * 128 + e * 32 + lane];
+        int r0, r1, m0, m1, rr0, rr1;
+        qpair_rows<KIND>(a, 8 * (rb0 + rbl) + g, r0, r1, m0, m1, rr0, rr1);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int b = 2 * t + e;
+          if (b < nb) epilogue<uint16_t, KIND>(a, b, r0, r1, v[e], v[2 + e], best_unused);
+        }
+      }
+      ch = 0;
+      ++rbl;
     }
   }
 }
@@ -677,7 +702,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // l % upr of the warp's (l / upr)-th row block and goes to stage
 // u % stages (a multiple of consumers), so every stage serves one warp in
 // order; units past the warp's last row block are never issued.  The
-// producer serves the warps' queues independently.  The fp16
+// producer warp serves the warps' queues independently, one lane each.  The fp16
 // B operand is the normalised input times a power-of-two sigma chosen at
 // creation so that no value can overflow; the row scale and 1 / sigma are
 // applied when a row block is complete, followed by the logits and the
@@ -723,45 +748,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   __syncthreads();
 
   if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      int nl[kTmaConsumers];   // next unit of each warp's queue (in that warp's order)
-      int remaining = 0;
-#pragma unroll
-      for (int w = 0; w < kTmaConsumers; ++w) {
-        nl[w] = 0;
-        if (w < consumers && w < nrb) remaining += ((nrb - w + consumers - 1) / consumers) * upr;
+    // producer: lane w serves consumer warp w's queue (its row blocks in
+    // order, upr units each; stage and phase kept incrementally)
+    const uint64_t pol = l2_evict_first_policy();
+    int rbl = lane, ch = 0, s = lane;
+    uint32_t ph = 0;
+    bool todo = lane < consumers && rbl < nrb;
+    uint32_t idle = 0;
+    while (__any_sync(0xffffffffu, todo)) {
+      bool issued = false;
+      if (todo && mbar_test_wait(&empty_bar[s], ph ^ 1u)) {
+        mbar_expect_tx(&full_bar[s], kUnit);
+        const unsigned char* src = a.qt[LM_HEAD] + ((size_t)(rb0 + rbl) * G + (size_t)ch * gpc) * kQ8Tile;
+        bulk_g2s_hint(gsm + (size_t)s * kUnit, src, kUnit, &full_bar[s], pol);
+        if (++ch == upr) {
+          ch = 0;
+          rbl += consumers;
+        }
+        s += consumers;
+        if (s >= stages) {
+          s -= stages;
+          ph ^= 1u;
+        }
+        todo = rbl < nrb;
+        issued = true;
       }
-      uint32_t idle = 0;
-      while (remaining > 0) {
-        bool progress = false;
-#pragma unroll
-        for (int w = 0; w < kTmaConsumers; ++w) {
-          if (w >= consumers) continue;
-          const int l = nl[w];
-          const int rbl = (l / upr) * consumers + w, ch = l - (l / upr) * upr;
-          if (rbl >= nrb) continue;
-          const int u = l * consumers + w, s = u % stages;
-          if (!mbar_test_wait(&empty_bar[s], (uint32_t)(((u / stages) & 1) ^ 1))) continue;
-          mbar_expect_tx(&full_bar[s], kUnit);
-          const unsigned char* src = a.qt[LM_HEAD] + ((size_t)(rb0 + rbl) * G + (size_t)ch * gpc) * kQ8Tile;
-          bulk_g2s_hint(gsm + (size_t)s * kUnit, src, kUnit, &full_bar[s], pol);
-          nl[w] = l + 1;
-          --remaining;
-          progress = true;
-        }
-        if (progress) idle = 0;
-        else if (++idle > kGemvWaitLimit) {
-          set_error(a.err, MTP_ERR_TIMEOUT);
-          break;
-        }
+      if (__any_sync(0xffffffffu, issued)) {
+        idle = 0;
+      } else if (++idle > kGemvWaitLimit) {
+        if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+        break;
       }
     }
     return;
   }
 
+  float wr[kStageRegItems][16];
+  stage_q_weights<LM_HEAD>(a, C, nb, wr);
   pdl_wait();
-  stage_q_inputs<LM_HEAD, true>(a, xf, nullptr, C, nb, a.lm_sigma, red, sid, srs);
+  stage_q_inputs<LM_HEAD, true>(a, xf, nullptr, C, nb, a.lm_sigma, red, sid, srs, wr);
   const float inv_sigma = 1.0f / a.lm_sigma;   // a power of two
 
   const int cw = warp - 1;
@@ -916,17 +941,17 @@ static cudaError_t launch_q4_nb(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uin
   const int G = C / 64;
   const int nrb_all = q_pairs(KIND, a.H, a.q_dim, a.kv_dim, a.F, a.V) / 8;
   const int grid = min(ctx->num_sms, nrb_all);
-  const int max_rb = (nrb_all + grid - 1) / grid;
-  if (max_rb > kQMaxRb) return cudaErrorInvalidConfiguration;
-  const size_t fixed = (size_t)G * 2 * NB * 64 + (size_t)G * 32;
-  const int gpc = q_gpc(G, kQ4Tile, kQ4UnitBytes);
-  int stages, consumers;
-  if (!q_plan((size_t)gpc * kQ4Tile, fixed, (size_t)max_rb * 512, &stages, &consumers))
-    return cudaErrorInvalidConfiguration;
-  const size_t smem = (size_t)stages * gpc * kQ4Tile + fixed + (size_t)max_rb * consumers * 512;
+  const size_t fixed = (size_t)G * 2 * NB * 64 + (size_t)G * 32 + (size_t)2 * kTmaConsumers * 512;
+  // the largest chunk (a divisor of G, at most kQ4UnitBytes) that leaves
+  // room for at least four stages
+  int gpc = q_gpc(G, kQ4Tile, kQ4UnitBytes);
+  while (gpc > 1 && (fixed + (size_t)4 * gpc * kQ4Tile > kQSmemBudget)) gpc = q_gpc(G, kQ4Tile, (gpc - 1) * kQ4Tile);
+  if (fixed + (size_t)2 * gpc * kQ4Tile > kQSmemBudget) return cudaErrorInvalidConfiguration;
+  int stages = (int)((kQSmemBudget - fixed) / ((size_t)gpc * kQ4Tile));
+  if (stages > kQStages) stages = kQStages;
+  const size_t smem = (size_t)stages * gpc * kQ4Tile + fixed;
   ensure_smem((const void*)gemv_q4_mma_kernel<KIND, NB>, smem);
-  return launch_pdl(gemv_q4_mma_kernel<KIND, NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, consumers,
-                    max_rb, gpc);
+  return launch_pdl(gemv_q4_mma_kernel<KIND, NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, gpc);
 }
 
 template <int KIND>
