@@ -42,7 +42,10 @@ import synth  # noqa: E402
 METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM roofline"
 # dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch from an ncu capture of the
 # current kernel (profiles/lm_head_argmax_qwen3_8b_mtp_b1.md); other workloads report null.
-LM_TRAFFIC = {"qwen3_8b_mtp_b1": 1244760000 + 3036928}
+LM_TRAFFIC = {
+    "qwen3_8b_mtp_b1": 1244760000 + 3036928,
+    "qwen3_8b_mtp_b1:int4_g64": 622737408 + 3309056,
+}
 # The same for one launch of the persistent draft kernel (all K steps); null until captured.
 PERSISTENT_TRAFFIC = {}
 WORKLOADS = {c.name: c for c in synth.CONFIGS}

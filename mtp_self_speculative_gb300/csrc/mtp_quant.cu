@@ -702,7 +702,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // l % upr of the warp's (l / upr)-th row block and goes to stage
 // u % stages (a multiple of consumers), so every stage serves one warp in
 // order; units past the warp's last row block are never issued.  The
-// producer warp serves the warps' queues independently, one lane each.  The fp16
+// producer serves the warps' queues independently (one lane polls them).  The fp16
 // B operand is the normalised input times a power-of-two sigma chosen at
 // creation so that no value can overflow; the row scale and 1 / sigma are
 // applied when a row block is complete, followed by the logits and the
@@ -748,36 +748,51 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   __syncthreads();
 
   if (warp == 0) {
-    // producer: lane w serves consumer warp w's queue (its row blocks in
-    // order, upr units each; stage and phase kept incrementally)
-    const uint64_t pol = l2_evict_first_policy();
-    int rbl = lane, ch = 0, s = lane;
-    uint32_t ph = 0;
-    bool todo = lane < consumers && rbl < nrb;
-    uint32_t idle = 0;
-    while (__any_sync(0xffffffffu, todo)) {
-      bool issued = false;
-      if (todo && mbar_test_wait(&empty_bar[s], ph ^ 1u)) {
-        mbar_expect_tx(&full_bar[s], kUnit);
-        const unsigned char* src = a.qt[LM_HEAD] + ((size_t)(rb0 + rbl) * G + (size_t)ch * gpc) * kQ8Tile;
-        bulk_g2s_hint(gsm + (size_t)s * kUnit, src, kUnit, &full_bar[s], pol);
-        if (++ch == upr) {
-          ch = 0;
-          rbl += consumers;
-        }
-        s += consumers;
-        if (s >= stages) {
-          s -= stages;
-          ph ^= 1u;
-        }
-        todo = rbl < nrb;
-        issued = true;
+    if (lane == 0) {
+      // one lane polls the warps' queues: a stage is refilled as soon as its
+      // warp frees it (stage and phase of each queue kept incrementally)
+      const uint64_t pol = l2_evict_first_policy();
+      int q_rbl[kTmaConsumers], q_ch[kTmaConsumers], q_s[kTmaConsumers];
+      uint32_t q_ph[kTmaConsumers];
+      int remaining = 0;
+#pragma unroll
+      for (int w = 0; w < kTmaConsumers; ++w) {
+        q_rbl[w] = w;
+        q_ch[w] = 0;
+        q_s[w] = w;
+        q_ph[w] = 0;
+        if (w < consumers && w < nrb) remaining += ((nrb - w + consumers - 1) / consumers) * upr;
       }
-      if (__any_sync(0xffffffffu, issued)) {
-        idle = 0;
-      } else if (++idle > kGemvWaitLimit) {
-        if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
-        break;
+      uint32_t idle = 0;
+      while (remaining > 0) {
+        bool progress = false;
+#pragma unroll
+        for (int w = 0; w < kTmaConsumers; ++w) {
+          if (w >= consumers || q_rbl[w] >= nrb) continue;
+          const int s = q_s[w];
+          if (!mbar_test_wait(&empty_bar[s], q_ph[w] ^ 1u)) continue;
+          mbar_expect_tx(&full_bar[s], kUnit);
+          const unsigned char* src =
+              a.qt[LM_HEAD] + ((size_t)(rb0 + q_rbl[w]) * G + (size_t)q_ch[w] * gpc) * kQ8Tile;
+          bulk_g2s_hint(gsm + (size_t)s * kUnit, src, kUnit, &full_bar[s], pol);
+          if (++q_ch[w] == upr) {
+            q_ch[w] = 0;
+            q_rbl[w] += consumers;
+          }
+          q_s[w] = s + consumers;
+          if (q_s[w] >= stages) {
+            q_s[w] -= stages;
+            q_ph[w] ^= 1u;
+          }
+          --remaining;
+          progress = true;
+        }
+        if (progress) {
+          idle = 0;
+        } else if (++idle > kGemvWaitLimit) {
+          set_error(a.err, MTP_ERR_TIMEOUT);
+          break;
+        }
       }
     }
     return;
