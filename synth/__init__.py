@@ -203,6 +203,7 @@ _STREAM = {
     "embed": 14, "hidden": 20, "token_ids": 21, "ctx_len": 22, "block_perm": 23,
     "k_pool": 24, "v_pool": 25, "verify_logits": 30, "spike_ids": 31, "accept_len": 32,
     "mismatch_ids": 33, "tail_ids": 34, "num_drafts": 35, "spike_noise": 36,
+    "loop_hash": 40,
 }
 
 
@@ -404,3 +405,34 @@ def expected_accept_len(K: int, alpha: float) -> float:
 
 def shrink(cfg: MTPShape, **kw) -> MTPShape:
     return replace(cfg, **kw)
+
+
+# ------------------------------------------------------- speculative loop
+
+def copy_head(cfg: MTPShape, w: Dict[str, np.ndarray], residual_scale: float = 0.01) -> Dict[str, np.ndarray]:
+    """A head whose drafts repeat their input token: eh_proj = [0 | I] (the
+    projection passes the normalised embedding through), o_proj and down_proj
+    scaled by ``residual_scale`` (the layer still runs, but adds little), so
+    the tied LM head's self-dot of the input row wins.  Used to give the
+    speculative-loop tests drafts that a sticky synthetic verifier accepts."""
+    H = cfg.H
+    out = dict(w)
+    eh = np.concatenate([np.zeros((H, H), dtype=np.float32), np.eye(H, dtype=np.float32)], axis=1)
+
+    def conv(x):
+        return f32_to_bf16_bits(x) if cfg.dtype == "bf16" else x.astype(np.float32)
+
+    def scaled(name):
+        x = bf16_to_f32(w[name]) if cfg.dtype == "bf16" else w[name].astype(np.float32)
+        return conv(x * np.float32(residual_scale))
+
+    out["w_eh"] = conv(eh)
+    out["w_o"] = scaled("w_o")
+    out["w_down"] = scaled("w_down")
+    return out
+
+
+def loop_start_hashes(cfg: MTPShape, B: int) -> np.ndarray:
+    """Seeded 64-bit hashes standing for each request's prompt (the
+    synthetic verifier's state at the start of the loop)."""
+    return raw_u64(cfg.seed, _STREAM["loop_hash"], B)
