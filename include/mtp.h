@@ -247,6 +247,78 @@ mtp_status mtp_quantize_int4_g64(void* stream, const void* w, int rows, int cols
  * Dequantized weight: q * scale. */
 mtp_status mtp_quantize_int8_rows(void* stream, const void* w, int rows, int cols, void* q, void* scales);
 
+/* ------------------------------------------------------------------------
+ * The speculative loop around the step (an end-to-end harness).
+ *
+ * No trained target model exists in this library's tests, so a
+ * deterministic synthetic verifier stands in for it; it is a pure function
+ * of the token prefix, so plain greedy decoding with it is well defined and
+ * the speculative loop must reproduce it token for token ("How OpenVINO MTP
+ * Speculative Decoding Works Internally": the speculative result is the
+ * main model's greedy result; "Speculative Decoding", "Overview").  Hashing
+ * is the SplitMix64 finaliser mix() on 64-bit words:
+ *   fold(h, t) = mix(h + 0x9E3779B97F4A7C15 * (t + 1))   (prefix + token t)
+ *   prediction after a prefix (hash h, last token l): l if
+ *     (mix(h ^ 0xD1B54A32D192ED03) >> 11) < sticky_thr, else
+ *     mix(h ^ 0x8CB92BA72F3D8DD7) mod V
+ *   logits: ((mix(h ^ (0x9E3779B97F4A7C15 * (v + 1))) >> 40) * 2^-24 - 0.5
+ *     in the context's dtype, 8.0 at the prediction
+ *   hidden state: 2 * ((mix(h ^ 0x2545F4914F6CDD1D ^ (0x9E3779B97F4A7C15 *
+ *     (i + 1))) >> 40) * 2^-24 - 0.5) in the context's dtype.
+ * ---------------------------------------------------------------------- */
+
+/* Verifier rows for B requests with K drafts each (0 <= K <= max_k): row
+ * b*(K+1) + j is the verifier's output for request b's prefix (seq_hash[b],
+ * last_tok[b]) extended by drafts[b*K .. b*K+j-1].  logits [B*(K+1), V] in
+ * the context's dtype; row_offsets [B+1] (optional) receives b*(K+1).
+ * drafts may be NULL when K = 0.  All device, caller-owned; asynchronous. */
+mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K, const uint64_t* seq_hash,
+                            const int32_t* last_tok, const int32_t* drafts, uint64_t sticky_thr, void* logits,
+                            int32_t* row_offsets);
+
+/* Advance the loop state after verification: request b emits drafts
+ * drafts[b*K .. b*K+accepted[b]-1] and bonus[b] (appended to
+ * out_tokens[b*out_cap + out_len[b] ...] while they fit; out_len[b] counts
+ * every emitted token, and a token past out_cap sets the device error
+ * MTP_ERR_CAPACITY), folds them into seq_hash[b], sets last_tok[b] =
+ * bonus[b], advances positions[b] by accepted[b] + 1, and writes the next
+ * step's inputs: hidden[b] = the verifier hidden state of the new prefix,
+ * embeds[b] = row bonus[b] of the context's embedding table ([B, H] each, the
+ * context's dtype).  accepted[b] outside 0..K or bonus[b] outside the
+ * vocabulary set MTP_ERR_DEVICE_ARGS and leave request b unchanged. */
+mtp_status mtp_loop_advance(mtp_ctx* ctx, void* stream, int B, int K, const int32_t* drafts,
+                            const int32_t* accepted, const int32_t* bonus, uint64_t* seq_hash, int32_t* last_tok,
+                            int32_t* positions, void* hidden, void* embeds, int32_t* out_tokens,
+                            int32_t* out_len, int out_cap);
+
+/* State and scratch of mtp_spec_loop (all device pointers, caller-owned). */
+typedef struct {
+  int B;                  /* requests (1..max_batch) */
+  int K;                  /* drafts per step (1..max_k); 0 = plain greedy decoding with the verifier */
+  uint64_t sticky_thr;    /* verifier parameter (see above) */
+  uint64_t* seq_hash;     /* [B] */
+  int32_t* last_tok;      /* [B] */
+  int32_t* positions;     /* [B] position of last_tok (the next draft input) */
+  void* hidden;           /* [B, H] verifier hidden state for the next draft */
+  void* embeds;           /* [B, H] embedding of last_tok */
+  int32_t* drafts;        /* [B, max(K, 1)] scratch */
+  int32_t* accepted;      /* [B] scratch (the last step's accepted counts on return) */
+  int32_t* bonus;         /* [B] scratch */
+  int32_t* num_drafts;    /* [B] scratch */
+  int32_t* row_offsets;   /* [B + 1] scratch */
+  void* target_logits;    /* [B * (K + 1), V] scratch, the context's dtype */
+  int32_t* out_tokens;    /* [B, out_cap] emitted tokens */
+  int32_t* out_len;       /* [B] emitted counts */
+  int out_cap;
+} mtp_loop;
+
+/* `iters` steps of the speculative loop on `stream`, no host synchronisation:
+ * mtp_draft (K drafts) -> mtp_synth_target -> mtp_verify ->
+ * mtp_kv_commit_accepted (extra = 1) -> mtp_loop_advance.  With K = 0 each
+ * step is one token of plain greedy decoding (no drafting, no cache edit).
+ * The cache must have room for the committed entries of all steps. */
+mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* loop, int iters);
+
 /* Synchronise the context's device, return the device error word as an
  * mtp_status (MTP_OK if none) and clear it. */
 mtp_status mtp_get_device_error(mtp_ctx* ctx);

@@ -20,7 +20,8 @@ from ._lib import (  # noqa: F401
     KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
     MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
     MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
-    MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64, MTPConfig, MTPKV, MTPWeights, WEIGHT_FIELDS,
+    MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64, MTPConfig, MTPKV,
+    MTPLoop, MTPWeights, WEIGHT_FIELDS,
 )
 
 _clib = L.load()
@@ -160,6 +161,74 @@ def mtp_verify_noalloc(target_logits: torch.Tensor, row_offsets: torch.Tensor, d
                                     int(drafts.shape[1]), _ptr(num_drafts, torch.int32, "num_drafts"),
                                     _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus")),
            "mtp_verify_noalloc")
+
+
+# ------------------------------------------------ speculative loop harness
+
+def mtp_synth_target(ctx: Context, seq_hash: torch.Tensor, last_tok: torch.Tensor, drafts: Optional[torch.Tensor],
+                     K: int, sticky_thr: int, logits: torch.Tensor, row_offsets: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    """Synthetic verifier rows (include/mtp.h): seq_hash is an int64 tensor
+    holding the 64-bit prefix hashes."""
+    B = int(last_tok.shape[0])
+    dt = torch_dtype(ctx.cfg.dtype)
+    _check(_clib.mtp_synth_target(ctx.handle, _stream(stream), B, int(K), _ptr(seq_hash, torch.int64, "seq_hash"),
+                                  _ptr(last_tok, torch.int32, "last_tok"), _ptr(drafts, torch.int32, "drafts"),
+                                  ctypes.c_uint64(int(sticky_thr)), _ptr(logits, dt, "logits"),
+                                  _ptr(row_offsets, torch.int32, "row_offsets")), "mtp_synth_target")
+
+
+def mtp_loop_advance(ctx: Context, K: int, drafts: Optional[torch.Tensor], accepted: torch.Tensor,
+                     bonus: torch.Tensor, seq_hash: torch.Tensor, last_tok: torch.Tensor, positions: torch.Tensor,
+                     hidden: torch.Tensor, embeds: torch.Tensor, out_tokens: torch.Tensor, out_len: torch.Tensor,
+                     stream=None) -> None:
+    B = int(accepted.shape[0])
+    dt = torch_dtype(ctx.cfg.dtype)
+    _check(_clib.mtp_loop_advance(ctx.handle, _stream(stream), B, int(K), _ptr(drafts, torch.int32, "drafts"),
+                                  _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus"),
+                                  _ptr(seq_hash, torch.int64, "seq_hash"), _ptr(last_tok, torch.int32, "last_tok"),
+                                  _ptr(positions, torch.int32, "positions"), _ptr(hidden, dt, "hidden"),
+                                  _ptr(embeds, dt, "embeds"), _ptr(out_tokens, torch.int32, "out_tokens"),
+                                  _ptr(out_len, torch.int32, "out_len"), int(out_tokens.shape[1])),
+           "mtp_loop_advance")
+
+
+class SpecLoop:
+    """Device state and scratch of mtp_spec_loop for B requests, K drafts per
+    step (K = 0: plain greedy decoding with the verifier), out_cap tokens."""
+
+    def __init__(self, ctx: Context, B: int, K: int, sticky_thr: int, out_cap: int, device="cuda"):
+        dt = torch_dtype(ctx.cfg.dtype)
+        H, V = ctx.cfg.hidden, ctx.cfg.vocab
+        i32 = dict(dtype=torch.int32, device=device)
+        self.B, self.K, self.sticky_thr = B, K, int(sticky_thr)
+        self.seq_hash = torch.zeros(B, dtype=torch.int64, device=device)
+        self.last_tok = torch.zeros(B, **i32)
+        self.positions = torch.zeros(B, **i32)
+        self.hidden = torch.zeros((B, H), dtype=dt, device=device)
+        self.embeds = torch.zeros((B, H), dtype=dt, device=device)
+        self.drafts = torch.zeros((B, max(K, 1)), **i32)
+        self.accepted = torch.zeros(B, **i32)
+        self.bonus = torch.zeros(B, **i32)
+        self.num_drafts = torch.zeros(B, **i32)
+        self.row_offsets = torch.zeros(B + 1, **i32)
+        self.target_logits = torch.zeros((B * (K + 1), V), dtype=dt, device=device)
+        self.out_tokens = torch.zeros((B, out_cap), **i32)
+        self.out_len = torch.zeros(B, **i32)
+
+    def struct(self) -> MTPLoop:
+        return MTPLoop(self.B, self.K, self.sticky_thr, self.seq_hash.data_ptr(), self.last_tok.data_ptr(),
+                       self.positions.data_ptr(), self.hidden.data_ptr(), self.embeds.data_ptr(),
+                       self.drafts.data_ptr(), self.accepted.data_ptr(), self.bonus.data_ptr(),
+                       self.num_drafts.data_ptr(), self.row_offsets.data_ptr(), self.target_logits.data_ptr(),
+                       self.out_tokens.data_ptr(), self.out_len.data_ptr(), int(self.out_tokens.shape[1]))
+
+
+def mtp_spec_loop(ctx: Context, kv: Optional[KVCache], loop: SpecLoop, iters: int, stream=None) -> None:
+    st = loop.struct()
+    kvs = kv.struct() if kv is not None else None
+    _check(_clib.mtp_spec_loop(ctx.handle, _stream(stream), ctypes.byref(kvs) if kvs is not None else None,
+                               ctypes.byref(st), int(iters)), "mtp_spec_loop")
 
 
 def mtp_quantize_int4_g64(w: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,

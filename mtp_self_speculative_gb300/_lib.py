@@ -44,6 +44,14 @@ class MTPKV(ctypes.Structure):
                 ("pending", c_void_p), ("num_blocks", c_int), ("max_blocks", c_int)]
 
 
+class MTPLoop(ctypes.Structure):
+    _fields_ = [("B", c_int), ("K", c_int), ("sticky_thr", ctypes.c_uint64), ("seq_hash", c_void_p),
+                ("last_tok", c_void_p), ("positions", c_void_p), ("hidden", c_void_p), ("embeds", c_void_p),
+                ("drafts", c_void_p), ("accepted", c_void_p), ("bonus", c_void_p), ("num_drafts", c_void_p),
+                ("row_offsets", c_void_p), ("target_logits", c_void_p), ("out_tokens", c_void_p),
+                ("out_len", c_void_p), ("out_cap", c_int)]
+
+
 # name -> (restype, argtypes); every symbol declared in include/mtp.h
 SIGNATURES = {
     "mtp_init": (c_int, [ctypes.POINTER(MTPConfig), ctypes.POINTER(MTPWeights), c_int, ctypes.POINTER(c_void_p)]),
@@ -58,6 +66,11 @@ SIGNATURES = {
     "mtp_kv_commit_accepted": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32, c_int]),
     "mtp_kv_rollback": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV)]),
     "mtp_kv_truncate": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
+    "mtp_synth_target": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, P_i32, P_i32, ctypes.c_uint64,
+                                 c_void_p, P_i32]),
+    "mtp_loop_advance": (c_int, [c_void_p, c_void_p, c_int, c_int, P_i32, P_i32, P_i32, c_void_p, P_i32, P_i32,
+                                 c_void_p, c_void_p, P_i32, P_i32, c_int]),
+    "mtp_spec_loop": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPLoop), c_int]),
     "mtp_get_device_error": (c_int, [c_void_p]),
     "mtp_destroy": (None, [c_void_p]),
     "mtp_status_str": (ctypes.c_char_p, [c_int]),

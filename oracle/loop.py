@@ -112,17 +112,19 @@ def greedy(h: int, last: int, thr: int, V: int, n: int) -> List[int]:
     return toks
 
 
-def spec_loop(W, kv, st: LoopState, K: int, thr: int, iters: int, dtype: str):
+def spec_loop(W, kv, st: LoopState, K: int, thr: int, iters: int, dtype: str, embed_rows=None):
     """`iters` speculative steps for every request, updating `st` and `kv`
-    (the oracle's draft, verify and commit).  Returns the accepted counts
-    per step [iters, B]."""
+    (the oracle's draft, verify and commit).  ``embed_rows`` gives the
+    embedding the verifier hands to the first draft step (default: the
+    head's own table; a quantized head's caller passes the dense table).
+    Returns the accepted counts per step [iters, B]."""
     B = len(st.last)
     V = W.lm_rows
     H = W.w_eh.shape[0]
     acc_hist = np.zeros((iters, B), dtype=np.int32)
     for it in range(iters):
         hidden = np.stack([target_hidden(st.seq_hash[b], H, dtype) for b in range(B)])
-        embeds = W.embed_rows(np.array(st.last))
+        embeds = (embed_rows or W.embed_rows)(np.array(st.last))
         res = draft(W, hidden, embeds, np.array(st.position, dtype=np.int32), kv, K)
         rows = []
         for b in range(B):
