@@ -343,6 +343,8 @@ def run_ours(args, rank, world, local_rank):
     cfg = WORKLOADS[args.workload]
     if cfg.H == 0:
         return run_verify_workload(args, cfg, rank, world, local_rank)
+    if args.loop:
+        return run_loop_workload(args, cfg, rank, world, local_rank)
     K = cfg.K
     wl = Workload(cfg, K, args.persistent_max_batch, args.weights)
     stream = torch.cuda.current_stream()
@@ -534,6 +536,137 @@ def run_e2e(wl: Workload, n: int) -> dict:
 
 
 # ------------------------------------------------------- CPU / oracle legs
+
+LOOP_METRIC = "speculative loop emitted tokens/s (draft + synthetic verifier + verify + commit)"
+
+
+def run_loop_workload(args, cfg, rank, world, local_rank):
+    """The full speculative loop (mtp_spec_loop) on the draft workload's
+    shape: the copy-head weight recipe (drafts repeat their input token) and
+    the synthetic verifier with a sticky probability of --loop-alpha, so that
+    drafts are accepted at a controlled rate.  One step = one loop iteration
+    (K drafts, K + 1 verifier rows, verify, commit, state advance); value =
+    emitted tokens per second over all requests."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    K = cfg.K
+    B = cfg.batch
+    lens = synth.context_lengths(cfg)
+    w = synth.copy_head(cfg, synth.make_weights(cfg, norm="ones"))
+    thr = int(args.loop_alpha * 2 ** 53)
+    total = args.warmup + args.steps + 2 * max(5, args.steps // 4) + 8
+    kv0 = synth.make_kv(cfg, lens, extra_slots=K * total + K + 1)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+    wdev = {k: dev(v) for k, v in w.items()}
+    ctx = M.mtp_init(M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps,
+                                   cfg.rope_theta, cfg.dtype, B, K, cfg.block_size,
+                                   int(lens.max()) + (K + 1) * total + 8,
+                                   weight_format=args.weights), wdev)
+    kv = M.KVCache(dev(kv0.k_pool), dev(kv0.v_pool), dev(kv0.block_table), dev(kv0.seq_len), dev(kv0.pending))
+    lp = M.SpecLoop(ctx, B, K, thr, out_cap=(K + 1) * total)
+    h0 = synth.loop_start_hashes(cfg, B)
+    last0 = synth.uniform_int(cfg.seed, 95, (B,), 0, cfg.vocab)
+    lp.seq_hash.copy_(torch.from_numpy(h0.view(np.int64)).cuda())
+    lp.last_tok.copy_(dev(last0))
+    lp.positions.copy_(dev(lens.astype(np.int32)))
+    lp.embeds.copy_(dev(w["embed"][last0]))
+    # the first step's hidden state: any value (the loop writes the verifier's from then on)
+    lp.hidden.copy_(dev(synth.make_draft_inputs(cfg, w, lens).hidden))
+    stream = torch.cuda.current_stream()
+
+    M.mtp_spec_loop(ctx, kv, lp, args.warmup)
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    n0 = int(lp.out_len.sum().item())
+    launches0 = M.mtp_launch_count(ctx)
+    sampler = ClockSampler(gpu_id_for_smi(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    M.mtp_spec_loop(ctx, kv, lp, args.steps)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    launches = M.mtp_launch_count(ctx) - launches0
+    ms = reduce_max(t0.elapsed_time(t1), world)
+    emitted = int(lp.out_len.sum().item()) - n0
+    assert M.mtp_get_device_error(ctx) == 0
+
+    # LM-head launches timed on the library's stream (separate pass)
+    nprof = max(5, args.steps // 4)
+    M.mtp_profile_begin(ctx, M.MTP_KERNEL_LM_HEAD, nprof * K)
+    M.mtp_spec_loop(ctx, kv, lp, nprof)
+    torch.cuda.synchronize()
+    lm_ms = M.mtp_profile_end(ctx, nprof * K)
+
+    # end to end: one host read of the emitted counts per step (synchronising)
+    ne = max(5, args.steps // 4)
+    h_len = torch.empty(B, dtype=torch.int32).pin_memory()
+    e0 = int(lp.out_len.sum().item())
+    te = time.perf_counter()
+    for _ in range(ne):
+        M.mtp_spec_loop(ctx, kv, lp, 1)
+        h_len.copy_(lp.out_len, non_blocking=True)
+        torch.cuda.synchronize()
+    te = time.perf_counter() - te
+    e_emitted = int(h_len.sum().item()) - e0
+    if rank != 0:
+        return
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    fmt = args.weights
+    lm_bytes = kernel_bytes(cfg, lens, K, with_logits=False, fmt=fmt)["lm_head"]
+    lm_gbs = lm_bytes / (statistics.mean(lm_ms) * 1e-3) / 1e9
+    value = world * emitted / (ms * 1e-3)
+    line = {
+        "metric": LOOP_METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype if fmt == "dense" else "int4/int8 weights, f32 arithmetic, bf16 KV",
+        "data": "synthetic (copy-head weights, deterministic synthetic verifier)",
+        "config": {"workload": "spec_loop_" + cfg.name, "batch": B, "draft_steps_K": K,
+                   "sticky_alpha": args.loop_alpha, "weights": fmt,
+                   "mean_emitted_per_step": emitted / (B * args.steps),
+                   "l2": "inputs larger than L2 (weights streamed every draft step)"},
+        "roofline": {"kernel": "lm_head_argmax" if fmt == "dense" else "lm_head_argmax_int8", "bound": "hbm",
+                     "achieved": lm_gbs, "peak": peak, "unit": "GB/s", "frac": lm_gbs / peak,
+                     "peak_source": peak_kind + " hbm_gbs", "traffic": None, "launches_timed": len(lm_ms),
+                     "bytes_per_launch": lm_bytes},
+        "e2e": {"value": world * e_emitted / te, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 4 * B},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = loop_cpu_baseline(cfg, w, lens, h0, last0, thr, fmt)
+    print(json.dumps(line), flush=True)
+
+
+def loop_cpu_baseline(cfg, w, lens, h0, last0, thr, fmt) -> dict:
+    """One step of the oracle's speculative loop on the same state."""
+    import oracle as O
+    import oracle.loop as OL
+    W = oracle_head(cfg, w, fmt)
+    kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
+    st = OL.LoopState([int(x) for x in h0], [int(x) for x in last0], [int(x) for x in lens],
+                      [[] for _ in range(len(lens))])
+    dense = None if fmt == "dense" else (lambda ids: O.widen(w["embed"][np.asarray(ids)], cfg.dtype))
+    t = time.perf_counter()
+    OL.spec_loop(W, kv, st, cfg.K, thr, 1, cfg.dtype, embed_rows=dense)
+    dt = time.perf_counter() - t
+    n = sum(len(o) for o in st.out)
+    return {"value": n / dt, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "1 loop step (K=%d draft steps, verifier rows, verify, commit), B=%d, float64 numpy" %
+                      (cfg.K, len(lens))}
+
 
 VERIFY_METRIC = "MTP verify + KV commit calls/s (64 requests, K_b uniform 1..8); % HBM roofline"
 
@@ -762,6 +895,10 @@ def main(argv=None):
     ap.add_argument("--weights", choices=["dense", "int4_g64"], default="dense",
                     help="weight format of the head: dense (the workload's dtype) or the quantized format "
                          "(int4 group-64 projections, int8 per-row embedding / LM head)")
+    ap.add_argument("--loop", action="store_true",
+                    help="time the full speculative loop (mtp_spec_loop with the synthetic verifier) instead")
+    ap.add_argument("--loop-alpha", type=float, default=0.8,
+                    help="probability that the synthetic verifier repeats the last token (--loop)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")
