@@ -568,7 +568,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
                                    int(lens.max()) + (K + 1) * total + 8,
                                    weight_format=args.weights), wdev)
     kv = M.KVCache(dev(kv0.k_pool), dev(kv0.v_pool), dev(kv0.block_table), dev(kv0.seq_len), dev(kv0.pending))
-    lp = M.SpecLoop(ctx, B, K, thr, out_cap=(K + 1) * total)
+    lp = M.SpecLoop(ctx, B, K, thr, out_cap=(K + 1) * total, conf_threshold=args.conf_threshold)
     h0 = synth.loop_start_hashes(cfg, B)
     last0 = synth.uniform_int(cfg.seed, 95, (B,), 0, cfg.vocab)
     lp.seq_hash.copy_(torch.from_numpy(h0.view(np.int64)).cuda())
@@ -633,7 +633,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
         "vs_baseline": None, "dtype": cfg.dtype if fmt == "dense" else "int4/int8 weights, f32 arithmetic, bf16 KV",
         "data": "synthetic (copy-head weights, deterministic synthetic verifier)",
         "config": {"workload": "spec_loop_" + cfg.name, "batch": B, "draft_steps_K": K,
-                   "sticky_alpha": args.loop_alpha, "weights": fmt,
+                   "sticky_alpha": args.loop_alpha, "weights": fmt, "conf_threshold": args.conf_threshold,
                    "mean_emitted_per_step": emitted / (B * args.steps),
                    "l2": "inputs larger than L2 (weights streamed every draft step)"},
         "roofline": {"kernel": "lm_head_argmax" if fmt == "dense" else "lm_head_argmax_int8", "bound": "hbm",
@@ -899,6 +899,8 @@ def main(argv=None):
                     help="time the full speculative loop (mtp_spec_loop with the synthetic verifier) instead")
     ap.add_argument("--loop-alpha", type=float, default=0.8,
                     help="probability that the synthetic verifier repeats the last token (--loop)")
+    ap.add_argument("--conf-threshold", type=float, default=0.0,
+                    help="with --loop: propose only the leading drafts whose probability exceeds it (0: off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")

@@ -267,14 +267,32 @@ mtp_status mtp_quantize_int8_rows(void* stream, const void* w, int rows, int col
  *     (i + 1))) >> 40) * 2^-24 - 0.5) in the context's dtype.
  * ---------------------------------------------------------------------- */
 
-/* Verifier rows for B requests with K drafts each (0 <= K <= max_k): row
- * b*(K+1) + j is the verifier's output for request b's prefix (seq_hash[b],
- * last_tok[b]) extended by drafts[b*K .. b*K+j-1].  logits [B*(K+1), V] in
- * the context's dtype; row_offsets [B+1] (optional) receives b*(K+1).
- * drafts may be NULL when K = 0.  All device, caller-owned; asynchronous. */
-mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K, const uint64_t* seq_hash,
-                            const int32_t* last_tok, const int32_t* drafts, uint64_t sticky_thr, void* logits,
-                            int32_t* row_offsets);
+/* Verifier rows for B requests with nd_b = num_drafts[b] drafts each (K for
+ * every request when num_drafts is NULL; 0 <= nd_b <= K <= max_k): request
+ * b's rows start at o_b = sum_{c<b} (nd_c + 1), and row o_b + j is the
+ * verifier's output for the prefix (seq_hash[b], last_tok[b]) extended by
+ * drafts[b*K .. b*K+j-1], j = 0..nd_b.  logits [B*(K+1), V] in the context's
+ * dtype (rows past the last are untouched); row_offsets [B+1] (optional)
+ * receives o_b.  drafts may be NULL when K = 0.  All device, caller-owned;
+ * asynchronous. */
+mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K, const int32_t* num_drafts,
+                            const uint64_t* seq_hash, const int32_t* last_tok, const int32_t* drafts,
+                            uint64_t sticky_thr, void* logits, int32_t* row_offsets);
+
+/* Dynamic draft length ("Speculative Decoding", "Fast Draft": the drafter
+ * keeps proposing while the candidate token's probability exceeds a
+ * threshold).  conf [B, K] receives the probability of each draft step's
+ * argmax token under its logits (logits [B, K, V] fp32 as mtp_draft writes
+ * them): 1 / sum_v exp(z_v - max z).  num_drafts [B] (optional) receives the
+ * length of the leading run of steps with conf > tau. */
+mtp_status mtp_draft_confidence(mtp_ctx* ctx, void* stream, int B, int K, const float* logits, float tau,
+                                float* conf, int32_t* num_drafts);
+
+/* The next step's draft count from recent acceptance (host-side; the pages
+ * adapt the number of assistant tokens per step without giving a rule): K + 2
+ * after a step whose `drafted` drafts were all accepted, K - 1 otherwise,
+ * clamped to [k_min, k_max]. */
+int mtp_adapt_k(int K, int accepted, int drafted, int k_min, int k_max);
 
 /* Advance the loop state after verification: request b emits drafts
  * drafts[b*K .. b*K+accepted[b]-1] and bonus[b] (appended to
@@ -310,11 +328,15 @@ typedef struct {
   int32_t* out_tokens;    /* [B, out_cap] emitted tokens */
   int32_t* out_len;       /* [B] emitted counts */
   int out_cap;
+  float conf_threshold;   /* > 0: propose only the leading drafts whose probability exceeds it */
+  float* draft_logits;    /* [B, K, V] fp32 scratch (with conf_threshold) */
+  float* conf;            /* [B, K] scratch (with conf_threshold) */
 } mtp_loop;
 
 /* `iters` steps of the speculative loop on `stream`, no host synchronisation:
- * mtp_draft (K drafts) -> mtp_synth_target -> mtp_verify ->
- * mtp_kv_commit_accepted (extra = 1) -> mtp_loop_advance.  With K = 0 each
+ * mtp_draft (K drafts) [-> mtp_draft_confidence: num_drafts from the
+ * threshold] -> mtp_synth_target -> mtp_verify -> mtp_kv_commit_accepted
+ * (extra = 1) -> mtp_loop_advance.  With K = 0 each
  * step is one token of plain greedy decoding (no drafting, no cache edit).
  * The cache must have room for the committed entries of all steps. */
 mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* loop, int iters);

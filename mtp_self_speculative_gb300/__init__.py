@@ -167,12 +167,13 @@ def mtp_verify_noalloc(target_logits: torch.Tensor, row_offsets: torch.Tensor, d
 
 def mtp_synth_target(ctx: Context, seq_hash: torch.Tensor, last_tok: torch.Tensor, drafts: Optional[torch.Tensor],
                      K: int, sticky_thr: int, logits: torch.Tensor, row_offsets: Optional[torch.Tensor] = None,
-                     stream=None) -> None:
+                     num_drafts: Optional[torch.Tensor] = None, stream=None) -> None:
     """Synthetic verifier rows (include/mtp.h): seq_hash is an int64 tensor
     holding the 64-bit prefix hashes."""
     B = int(last_tok.shape[0])
     dt = torch_dtype(ctx.cfg.dtype)
-    _check(_clib.mtp_synth_target(ctx.handle, _stream(stream), B, int(K), _ptr(seq_hash, torch.int64, "seq_hash"),
+    _check(_clib.mtp_synth_target(ctx.handle, _stream(stream), B, int(K), _ptr(num_drafts, torch.int32, "num_drafts"),
+                                  _ptr(seq_hash, torch.int64, "seq_hash"),
                                   _ptr(last_tok, torch.int32, "last_tok"), _ptr(drafts, torch.int32, "drafts"),
                                   ctypes.c_uint64(int(sticky_thr)), _ptr(logits, dt, "logits"),
                                   _ptr(row_offsets, torch.int32, "row_offsets")), "mtp_synth_target")
@@ -193,11 +194,27 @@ def mtp_loop_advance(ctx: Context, K: int, drafts: Optional[torch.Tensor], accep
            "mtp_loop_advance")
 
 
+def mtp_draft_confidence(ctx: Context, logits: torch.Tensor, tau: float, conf: torch.Tensor,
+                         num_drafts: Optional[torch.Tensor] = None, stream=None) -> None:
+    """conf [B, K] = probability of each draft step's argmax under logits
+    [B, K, V] (fp32); num_drafts [B] = leading run with conf > tau."""
+    B, K = int(logits.shape[0]), int(logits.shape[1])
+    _check(_clib.mtp_draft_confidence(ctx.handle, _stream(stream), B, K, _ptr(logits, torch.float32, "logits"),
+                                      float(tau), _ptr(conf, torch.float32, "conf"),
+                                      _ptr(num_drafts, torch.int32, "num_drafts")), "mtp_draft_confidence")
+
+
+def mtp_adapt_k(K: int, accepted: int, drafted: int, k_min: int, k_max: int) -> int:
+    return int(_clib.mtp_adapt_k(int(K), int(accepted), int(drafted), int(k_min), int(k_max)))
+
+
 class SpecLoop:
     """Device state and scratch of mtp_spec_loop for B requests, K drafts per
-    step (K = 0: plain greedy decoding with the verifier), out_cap tokens."""
+    step (K = 0: plain greedy decoding with the verifier), out_cap tokens;
+    conf_threshold > 0 proposes only the leading confident drafts."""
 
-    def __init__(self, ctx: Context, B: int, K: int, sticky_thr: int, out_cap: int, device="cuda"):
+    def __init__(self, ctx: Context, B: int, K: int, sticky_thr: int, out_cap: int, device="cuda",
+                 conf_threshold: float = 0.0):
         dt = torch_dtype(ctx.cfg.dtype)
         H, V = ctx.cfg.hidden, ctx.cfg.vocab
         i32 = dict(dtype=torch.int32, device=device)
@@ -215,13 +232,18 @@ class SpecLoop:
         self.target_logits = torch.zeros((B * (K + 1), V), dtype=dt, device=device)
         self.out_tokens = torch.zeros((B, out_cap), **i32)
         self.out_len = torch.zeros(B, **i32)
+        self.conf_threshold = float(conf_threshold)
+        on = conf_threshold > 0 and K > 0
+        self.draft_logits = torch.zeros((B, K, V) if on else (1,), dtype=torch.float32, device=device)
+        self.conf = torch.zeros((B, K) if on else (1,), dtype=torch.float32, device=device)
 
     def struct(self) -> MTPLoop:
         return MTPLoop(self.B, self.K, self.sticky_thr, self.seq_hash.data_ptr(), self.last_tok.data_ptr(),
                        self.positions.data_ptr(), self.hidden.data_ptr(), self.embeds.data_ptr(),
                        self.drafts.data_ptr(), self.accepted.data_ptr(), self.bonus.data_ptr(),
                        self.num_drafts.data_ptr(), self.row_offsets.data_ptr(), self.target_logits.data_ptr(),
-                       self.out_tokens.data_ptr(), self.out_len.data_ptr(), int(self.out_tokens.shape[1]))
+                       self.out_tokens.data_ptr(), self.out_len.data_ptr(), int(self.out_tokens.shape[1]),
+                       self.conf_threshold, self.draft_logits.data_ptr(), self.conf.data_ptr())
 
 
 def mtp_spec_loop(ctx: Context, kv: Optional[KVCache], loop: SpecLoop, iters: int, stream=None) -> None:

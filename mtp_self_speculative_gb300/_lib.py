@@ -49,7 +49,8 @@ class MTPLoop(ctypes.Structure):
                 ("last_tok", c_void_p), ("positions", c_void_p), ("hidden", c_void_p), ("embeds", c_void_p),
                 ("drafts", c_void_p), ("accepted", c_void_p), ("bonus", c_void_p), ("num_drafts", c_void_p),
                 ("row_offsets", c_void_p), ("target_logits", c_void_p), ("out_tokens", c_void_p),
-                ("out_len", c_void_p), ("out_cap", c_int)]
+                ("out_len", c_void_p), ("out_cap", c_int), ("conf_threshold", c_float), ("draft_logits", c_void_p),
+                ("conf", c_void_p)]
 
 
 # name -> (restype, argtypes); every symbol declared in include/mtp.h
@@ -66,8 +67,10 @@ SIGNATURES = {
     "mtp_kv_commit_accepted": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32, c_int]),
     "mtp_kv_rollback": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV)]),
     "mtp_kv_truncate": (c_int, [c_void_p, c_void_p, c_int, ctypes.POINTER(MTPKV), P_i32]),
-    "mtp_synth_target": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, P_i32, P_i32, ctypes.c_uint64,
-                                 c_void_p, P_i32]),
+    "mtp_synth_target": (c_int, [c_void_p, c_void_p, c_int, c_int, P_i32, c_void_p, P_i32, P_i32,
+                                 ctypes.c_uint64, c_void_p, P_i32]),
+    "mtp_draft_confidence": (c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_float, c_void_p, P_i32]),
+    "mtp_adapt_k": (c_int, [c_int, c_int, c_int, c_int, c_int]),
     "mtp_loop_advance": (c_int, [c_void_p, c_void_p, c_int, c_int, P_i32, P_i32, P_i32, c_void_p, P_i32, P_i32,
                                  c_void_p, c_void_p, P_i32, P_i32, c_int]),
     "mtp_spec_loop": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPLoop), c_int]),

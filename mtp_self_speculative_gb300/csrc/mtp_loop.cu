@@ -38,16 +38,31 @@ __device__ __forceinline__ void store_val<float>(float* p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void store_val<uint16_t>(uint16_t* p, float v) { *p = f32_to_bf16_rne(v); }
 
-// grid (V slices, B * (K + 1)); each thread recomputes its row's prefix hash
-// (at most K folds) and writes a strided share of the slice.
+// grid (V slices, B * (K + 1)); request b has nd_b = num_drafts[b] (K when
+// num_drafts is NULL) drafts and nd_b + 1 rows starting at sum_{c<b}(nd_c + 1);
+// blocks past the last row return.  Each thread recomputes its row's prefix
+// hash (at most K folds) and writes a strided share of the slice.
 template <typename T>
-__global__ void synth_target_kernel(int B, int K, const uint64_t* seq_hash, const int32_t* last_tok,
-                                    const int32_t* drafts, uint64_t thr, int V, int slice, T* logits,
-                                    int32_t* row_offsets) {
+__global__ void synth_target_kernel(int B, int K, const int32_t* num_drafts, const uint64_t* seq_hash,
+                                    const int32_t* last_tok, const int32_t* drafts, uint64_t thr, int V, int slice,
+                                    T* logits, int32_t* row_offsets) {
   const int r = blockIdx.y;
-  const int b = r / (K + 1), j = r - b * (K + 1);
-  if (row_offsets && blockIdx.x == 0 && blockIdx.y == 0)
-    for (int i = threadIdx.x; i <= B; i += blockDim.x) row_offsets[i] = i * (K + 1);
+  int b = 0, row0 = 0;
+  for (; b < B; ++b) {
+    const int nd = num_drafts ? min(max(num_drafts[b], 0), K) : K;
+    if (r < row0 + nd + 1) break;
+    row0 += nd + 1;
+  }
+  if (row_offsets && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    int o = 0;
+    for (int c = 0; c < B; ++c) {
+      row_offsets[c] = o;
+      o += (num_drafts ? min(max(num_drafts[c], 0), K) : K) + 1;
+    }
+    row_offsets[B] = o;
+  }
+  if (b >= B) return;
+  const int j = r - row0;
   uint64_t h = seq_hash[b];
   int32_t last = last_tok[b];
   for (int i = 0; i < j; ++i) {
@@ -60,6 +75,44 @@ __global__ void synth_target_kernel(int B, int K, const uint64_t* seq_hash, cons
   T* row = logits + (size_t)r * V;
   for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x)
     store_val<T>(row + v, v == tgt ? 8.0f : uhalf(h, (uint64_t)v + 1));
+}
+
+// Probability of the argmax under each draft step's logits: one block per
+// (request, step), max then sum of exp(z - max) over the vocabulary with a
+// fixed-order block reduction; conf = 1 / sum.
+__global__ void draft_conf_kernel(const float* logits, int V, float* conf) {
+  __shared__ float red[32];
+  const float* z = logits + (size_t)blockIdx.x * V;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float m = -INFINITY;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) m = fmaxf(m, z[v]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red[w] = m;
+  __syncthreads();
+  m = red[0];
+  for (int i = 1; i < nw; ++i) m = fmaxf(m, red[i]);
+  __syncthreads();
+  float sum = 0.0f;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) sum += expf(z[v] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) red[w] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.0f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    conf[blockIdx.x] = 1.0f / t;
+  }
+}
+
+// Leading run of draft steps whose confidence exceeds tau, per request.
+__global__ void leading_run_kernel(int B, int K, const float* conf, float tau, int32_t* num_drafts) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += gridDim.x * blockDim.x) {
+    int n = 0;
+    while (n < K && conf[(size_t)b * K + n] > tau) ++n;
+    num_drafts[b] = n;
+  }
 }
 
 template <typename T>
@@ -117,9 +170,9 @@ static mtp_status loop_status(cudaError_t e) {
   return MTP_ERR_CUDA;
 }
 
-extern "C" mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K, const uint64_t* seq_hash,
-                                       const int32_t* last_tok, const int32_t* drafts, uint64_t sticky_thr,
-                                       void* logits, int32_t* row_offsets) {
+extern "C" mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K, const int32_t* num_drafts,
+                                       const uint64_t* seq_hash, const int32_t* last_tok, const int32_t* drafts,
+                                       uint64_t sticky_thr, void* logits, int32_t* row_offsets) {
   if (!ctx || B < 1 || B > ctx->cfg.max_batch || K < 0 || K > ctx->cfg.max_k) return MTP_ERR_INVALID;
   if (!seq_hash || !last_tok || !logits || (K > 0 && !drafts)) return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
@@ -128,11 +181,11 @@ extern "C" mtp_status mtp_synth_target(mtp_ctx* ctx, void* stream, int B, int K,
   const dim3 grid(slices, B * (K + 1));
   cudaStream_t s = (cudaStream_t)stream;
   if (ctx->cfg.dtype == MTP_DTYPE_BF16)
-    synth_target_kernel<uint16_t><<<grid, 256, 0, s>>>(B, K, seq_hash, last_tok, drafts, sticky_thr, V, 4096,
-                                                        (uint16_t*)logits, row_offsets);
+    synth_target_kernel<uint16_t><<<grid, 256, 0, s>>>(B, K, num_drafts, seq_hash, last_tok, drafts, sticky_thr, V,
+                                                        4096, (uint16_t*)logits, row_offsets);
   else
-    synth_target_kernel<float><<<grid, 256, 0, s>>>(B, K, seq_hash, last_tok, drafts, sticky_thr, V, 4096,
-                                                     (float*)logits, row_offsets);
+    synth_target_kernel<float><<<grid, 256, 0, s>>>(B, K, num_drafts, seq_hash, last_tok, drafts, sticky_thr, V,
+                                                     4096, (float*)logits, row_offsets);
   ctx->launches++;
   return loop_status(cudaGetLastError());
 }
@@ -162,6 +215,26 @@ extern "C" mtp_status mtp_loop_advance(mtp_ctx* ctx, void* stream, int B, int K,
   return loop_status(cudaGetLastError());
 }
 
+extern "C" mtp_status mtp_draft_confidence(mtp_ctx* ctx, void* stream, int B, int K, const float* logits,
+                                           float tau, float* conf, int32_t* num_drafts) {
+  if (!ctx || B < 1 || B > ctx->cfg.max_batch || K < 1 || K > ctx->cfg.max_k || !logits || !conf)
+    return MTP_ERR_INVALID;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  draft_conf_kernel<<<B * K, 512, 0, s>>>(logits, ctx->cfg.vocab, conf);
+  ctx->launches++;
+  if (num_drafts) {
+    leading_run_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, K, conf, tau, num_drafts);
+    ctx->launches++;
+  }
+  return loop_status(cudaGetLastError());
+}
+
+extern "C" int mtp_adapt_k(int K, int accepted, int drafted, int k_min, int k_max) {
+  if (drafted > 0 && accepted == drafted) return K + 2 < k_max ? K + 2 : k_max;
+  return K - 1 > k_min ? K - 1 : k_min;
+}
+
 extern "C" mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* lp, int iters) {
   if (!ctx || !ctx->has_weights || !lp || iters < 0) return MTP_ERR_INVALID;
   const int B = lp->B, K = lp->K;
@@ -169,6 +242,8 @@ extern "C" mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv
   if (!lp->drafts || !lp->accepted || !lp->bonus || !lp->num_drafts || !lp->row_offsets || !lp->target_logits)
     return MTP_ERR_INVALID;
   if (K > 0 && !kv) return MTP_ERR_INVALID;
+  const bool conf_stop = lp->conf_threshold > 0.0f && K > 0;
+  if (conf_stop && (!lp->draft_logits || !lp->conf)) return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
   fill_i32_kernel<<<1, 128, 0, s>>>(lp->num_drafts, B, K);
@@ -177,11 +252,13 @@ extern "C" mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv
   const int stride = K > 0 ? K : 1;
   for (int it = 0; it < iters && st == MTP_OK; ++it) {
     if (K > 0)
-      st = mtp_draft(ctx, stream, B, lp->hidden, lp->embeds, lp->positions, kv, K, nullptr, lp->drafts, nullptr,
-                     nullptr);
+      st = mtp_draft(ctx, stream, B, lp->hidden, lp->embeds, lp->positions, kv, K, nullptr, lp->drafts,
+                     conf_stop ? lp->draft_logits : nullptr, nullptr);
+    if (st == MTP_OK && conf_stop)
+      st = mtp_draft_confidence(ctx, stream, B, K, lp->draft_logits, lp->conf_threshold, lp->conf, lp->num_drafts);
     if (st == MTP_OK)
-      st = mtp_synth_target(ctx, stream, B, K, lp->seq_hash, lp->last_tok, lp->drafts, lp->sticky_thr,
-                            lp->target_logits, lp->row_offsets);
+      st = mtp_synth_target(ctx, stream, B, K, lp->num_drafts, lp->seq_hash, lp->last_tok, lp->drafts,
+                            lp->sticky_thr, lp->target_logits, lp->row_offsets);
     if (st == MTP_OK)
       st = mtp_verify(ctx, stream, B, lp->target_logits, B * (K + 1), lp->row_offsets, lp->drafts, stride,
                       lp->num_drafts, lp->accepted, lp->bonus);

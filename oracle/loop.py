@@ -37,6 +37,7 @@ from typing import List
 
 import numpy as np
 
+from .dynamic import draft_confidence, num_drafts_from_confidence
 from .mtp_oracle import draft, kv_commit, round_to_bf16, verify
 
 M64 = (1 << 64) - 1
@@ -112,11 +113,13 @@ def greedy(h: int, last: int, thr: int, V: int, n: int) -> List[int]:
     return toks
 
 
-def spec_loop(W, kv, st: LoopState, K: int, thr: int, iters: int, dtype: str, embed_rows=None):
+def spec_loop(W, kv, st: LoopState, K: int, thr: int, iters: int, dtype: str, embed_rows=None, conf_tau=None):
     """`iters` speculative steps for every request, updating `st` and `kv`
     (the oracle's draft, verify and commit).  ``embed_rows`` gives the
     embedding the verifier hands to the first draft step (default: the
     head's own table; a quantized head's caller passes the dense table).
+    ``conf_tau``: propose only each request's leading drafts whose
+    probability exceeds it (the confidence stop of the dynamic module).
     Returns the accepted counts per step [iters, B]."""
     B = len(st.last)
     V = W.lm_rows
@@ -126,18 +129,21 @@ def spec_loop(W, kv, st: LoopState, K: int, thr: int, iters: int, dtype: str, em
         hidden = np.stack([target_hidden(st.seq_hash[b], H, dtype) for b in range(B)])
         embeds = (embed_rows or W.embed_rows)(np.array(st.last))
         res = draft(W, hidden, embeds, np.array(st.position, dtype=np.int32), kv, K)
+        nd = np.full(B, K, dtype=np.int32)
+        if conf_tau is not None:
+            nd = num_drafts_from_confidence(draft_confidence(res.logits), conf_tau)
         rows = []
         for b in range(B):
             h, l = st.seq_hash[b], st.last[b]
             rows.append(target_row(h, l, thr, V, dtype))
-            for j in range(K):
+            for j in range(int(nd[b])):
                 h = fold(h, int(res.ids[b, j]))
                 l = int(res.ids[b, j])
                 rows.append(target_row(h, l, thr, V, dtype))
         logits = np.stack(rows)
-        offs = np.arange(B + 1, dtype=np.int64) * (K + 1)
+        offs = np.concatenate([[0], np.cumsum(nd.astype(np.int64) + 1)])
         # the rows already hold the stored values (exact in float64)
-        a, bonus = verify(logits, offs, res.ids, np.full(B, K, dtype=np.int32), "f32")
+        a, bonus = verify(logits, offs, res.ids, nd, "f32")
         kv_commit(kv, np.minimum(a + 1, K).astype(np.int32), dtype)
         for b in range(B):
             emitted = [int(t) for t in res.ids[b, :a[b]]] + [int(bonus[b])]

@@ -96,3 +96,18 @@ def test_spec_loop_all_accepted_when_the_target_repeats():
 def test_spec_loop_equals_greedy_with_random_drafts():
     cfg, W, kv, st, h0, last0, lens = _loop_case(copy=False)
     _check_equivalence(W, kv, st, h0, last0, cfg.K, int(0.7 * 2 ** 53), 2)
+
+
+def test_spec_loop_with_confidence_stop_equals_greedy():
+    """The confidence stop changes how many drafts are proposed, never the
+    output: with a threshold at the median draft confidence some steps
+    propose fewer than K drafts and the tokens still equal greedy decoding."""
+    from oracle import dynamic as D
+    cfg, W, kv, st, h0, last0, lens = _loop_case(copy=False, B=2)
+    kv_probe = kv.copy()
+    res = O.draft(W, np.ones((2, cfg.H)), W.embed_rows(np.array(last0)), np.array(st.position, dtype=np.int32),
+                  kv_probe, cfg.K)
+    tau = float(np.median(D.draft_confidence(res.logits)))
+    acc = L.spec_loop(W, kv, st, cfg.K, int(0.7 * 2 ** 53), 6, "f32", conf_tau=tau)
+    for b in range(2):
+        assert st.out[b] == L.greedy(h0[b], last0[b], int(0.7 * 2 ** 53), W.lm_rows, len(st.out[b]))
