@@ -341,6 +341,73 @@ typedef struct {
  * The cache must have room for the committed entries of all steps. */
 mtp_status mtp_spec_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* loop, int iters);
 
+/* ------------------------------------------------------------------------
+ * Tree drafting ("Speculative Decoding", "Tree Drafting", "How Tree Drafting
+ * Works"), with the MTP head as the drafter.  Layer 1 is the MTP step from
+ * the verifier's hidden state and the last token; it proposes the
+ * `branching` most probable tokens.  At layer l >= 2 the `branching`
+ * candidates of layer l-1 with the highest cumulative log-probability (all
+ * of them at l = 2) are each expanded by one MTP step (input: the node's
+ * token and the output hidden state of the step that proposed it; position
+ * p + l - 1; attention over the committed cache plus the MTP entries of the
+ * node's ancestors) into their `branching` most probable children.  The
+ * `n_assist` candidates with the best cumulative score (ties: smaller depth,
+ * then earlier creation) form the packed tree, ordered by (depth, creation)
+ * so that parents come first.  The page's rules are enforced:
+ * branching^2 (depth-1) + branching >= n_assist >= depth.  Limits:
+ * branching <= 8, depth <= 16, n_assist <= 64, B * branching <= max_batch,
+ * max_k >= 2 when depth >= 2.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int B, branching, depth, n_assist;
+  int32_t* scratch_blocks;   /* [(depth-1) * B * branching * 2] ids of free blocks of the cache pool,
+                                used for the expansions' private copies (device) */
+  void* ws;                  /* workspace of at least mtp_tree_workspace_bytes(...) bytes (device) */
+  size_t ws_bytes;
+  int32_t* tokens;           /* [B, n_assist] packed nodes' tokens (device, written by mtp_draft_tree) */
+  int32_t* parents;          /* [B, n_assist] parent node index, -1 for a child of the root */
+  int32_t* depths;           /* [B, n_assist] 1..depth */
+} mtp_tree;
+
+/* Workspace bytes of one tree call for a cache whose block tables have
+ * `max_blocks` entries; 0 for a bad shape. */
+size_t mtp_tree_workspace_bytes(const mtp_ctx* ctx, int B, int branching, int depth, int n_assist, int max_blocks);
+
+/* Draft the trees of B requests (inputs as mtp_draft's).  The root step
+ * writes slot seq_len[b] of each request's cache (pending[b] = 1; pending
+ * must be 0 on entry); expansions write only the private scratch blocks.
+ * Every slot seq_len[b] .. seq_len[b] + depth must lie in the block table
+ * (device-checked: MTP_ERR_CAPACITY). */
+mtp_status mtp_draft_tree(mtp_ctx* ctx, void* stream, const void* hidden, const void* embeds,
+                          const int32_t* positions, const mtp_kv* kv, const mtp_tree* tree);
+
+/* The synthetic verifier's rows for the packed trees: request b's rows start
+ * at b * (1 + n_assist); row 0 follows the committed prefix, row 1 + i the
+ * prefix extended by node i's path.  row_offsets [B+1] optional. */
+mtp_status mtp_synth_target_tree(mtp_ctx* ctx, void* stream, const mtp_tree* tree, const uint64_t* seq_hash,
+                                 const int32_t* last_tok, uint64_t sticky_thr, void* logits, int32_t* row_offsets);
+
+/* Tree verification: starting at the root, follow the child whose token is
+ * the verifier's argmax (lowest id on ties) after the current prefix, while
+ * one exists.  accepted [B] nodes on that path, their tokens in
+ * path_tokens [B, depth], bonus [B] the last argmax.  target_logits
+ * [B * (1 + n_assist), V] in the context's dtype, rows as above. */
+mtp_status mtp_verify_tree(mtp_ctx* ctx, void* stream, const mtp_tree* tree, const void* target_logits,
+                           int32_t* accepted, int32_t* bonus, int32_t* path_tokens);
+
+/* Keep the root's entry and the entries of the accepted nodes that were
+ * expanded (in path order, slots seq_len[b] + 1, ...), then advance
+ * seq_len[b] by their count and clear pending[b]. */
+mtp_status mtp_tree_commit(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_tree* tree,
+                           const int32_t* accepted);
+
+/* `iters` steps of the speculative loop with tree drafting: mtp_draft_tree
+ * -> mtp_synth_target_tree -> mtp_verify_tree (path into loop->drafts
+ * [B, depth]) -> mtp_tree_commit -> mtp_loop_advance.  loop->target_logits
+ * holds B * (1 + n_assist) rows. */
+mtp_status mtp_tree_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* loop, const mtp_tree* tree,
+                         int iters);
+
 /* Synchronise the context's device, return the device error word as an
  * mtp_status (MTP_OK if none) and clear it. */
 mtp_status mtp_get_device_error(mtp_ctx* ctx);

@@ -21,7 +21,7 @@ from ._lib import (  # noqa: F401
     MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
     MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
     MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64, MTPConfig, MTPKV,
-    MTPLoop, MTPWeights, WEIGHT_FIELDS,
+    MTPLoop, MTPTree, MTPWeights, WEIGHT_FIELDS,
 )
 
 _clib = L.load()
@@ -251,6 +251,70 @@ def mtp_spec_loop(ctx: Context, kv: Optional[KVCache], loop: SpecLoop, iters: in
     kvs = kv.struct() if kv is not None else None
     _check(_clib.mtp_spec_loop(ctx.handle, _stream(stream), ctypes.byref(kvs) if kvs is not None else None,
                                ctypes.byref(st), int(iters)), "mtp_spec_loop")
+
+
+class TreeDraft:
+    """Buffers of tree drafting for B requests (branching, depth, n_assist);
+    ``scratch_blocks`` is an int32 device tensor of free block ids of the cache
+    pool ((depth-1) * B * branching * 2 of them)."""
+
+    def __init__(self, ctx: Context, B: int, branching: int, depth: int, n_assist: int, max_blocks: int,
+                 scratch_blocks: Optional[torch.Tensor], device="cuda"):
+        n = int(_clib.mtp_tree_workspace_bytes(ctx.handle, B, branching, depth, n_assist, max_blocks))
+        if n == 0:
+            raise MTPError(MTP_ERR_INVALID, "mtp_tree_workspace_bytes")
+        self.B, self.branching, self.depth, self.n_assist = B, branching, depth, n_assist
+        self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+        self.scratch_blocks = scratch_blocks
+        i32 = dict(dtype=torch.int32, device=device)
+        self.tokens = torch.zeros((B, n_assist), **i32)
+        self.parents = torch.zeros((B, n_assist), **i32)
+        self.depths = torch.zeros((B, n_assist), **i32)
+
+    def struct(self) -> MTPTree:
+        sb = self.scratch_blocks.data_ptr() if self.scratch_blocks is not None else None
+        return MTPTree(self.B, self.branching, self.depth, self.n_assist, sb, self.ws.data_ptr(),
+                       int(self.ws.numel()), self.tokens.data_ptr(), self.parents.data_ptr(), self.depths.data_ptr())
+
+
+def mtp_draft_tree(ctx: Context, hidden: torch.Tensor, embeds: torch.Tensor, positions: torch.Tensor, kv: KVCache,
+                   tree: TreeDraft, stream=None) -> None:
+    dt = torch_dtype(ctx.cfg.dtype)
+    kvs, ts = kv.struct(), tree.struct()
+    _check(_clib.mtp_draft_tree(ctx.handle, _stream(stream), _ptr(hidden, dt, "hidden"), _ptr(embeds, dt, "embeds"),
+                                _ptr(positions, torch.int32, "positions"), ctypes.byref(kvs), ctypes.byref(ts)),
+           "mtp_draft_tree")
+
+
+def mtp_synth_target_tree(ctx: Context, tree: TreeDraft, seq_hash: torch.Tensor, last_tok: torch.Tensor,
+                          sticky_thr: int, logits: torch.Tensor, row_offsets: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    ts = tree.struct()
+    _check(_clib.mtp_synth_target_tree(ctx.handle, _stream(stream), ctypes.byref(ts),
+                                       _ptr(seq_hash, torch.int64, "seq_hash"), _ptr(last_tok, torch.int32, "last_tok"),
+                                       ctypes.c_uint64(int(sticky_thr)), _ptr(logits, torch_dtype(ctx.cfg.dtype), "logits"),
+                                       _ptr(row_offsets, torch.int32, "row_offsets")), "mtp_synth_target_tree")
+
+
+def mtp_verify_tree(ctx: Context, tree: TreeDraft, target_logits: torch.Tensor, accepted: torch.Tensor,
+                    bonus: torch.Tensor, path_tokens: torch.Tensor, stream=None) -> None:
+    ts = tree.struct()
+    _check(_clib.mtp_verify_tree(ctx.handle, _stream(stream), ctypes.byref(ts),
+                                 _ptr(target_logits, torch_dtype(ctx.cfg.dtype), "target_logits"),
+                                 _ptr(accepted, torch.int32, "accepted"), _ptr(bonus, torch.int32, "bonus"),
+                                 _ptr(path_tokens, torch.int32, "path_tokens")), "mtp_verify_tree")
+
+
+def mtp_tree_commit(ctx: Context, kv: KVCache, tree: TreeDraft, accepted: torch.Tensor, stream=None) -> None:
+    kvs, ts = kv.struct(), tree.struct()
+    _check(_clib.mtp_tree_commit(ctx.handle, _stream(stream), ctypes.byref(kvs), ctypes.byref(ts),
+                                 _ptr(accepted, torch.int32, "accepted")), "mtp_tree_commit")
+
+
+def mtp_tree_loop(ctx: Context, kv: KVCache, loop: SpecLoop, tree: TreeDraft, iters: int, stream=None) -> None:
+    kvs, ls, ts = kv.struct(), loop.struct(), tree.struct()
+    _check(_clib.mtp_tree_loop(ctx.handle, _stream(stream), ctypes.byref(kvs), ctypes.byref(ls), ctypes.byref(ts),
+                               int(iters)), "mtp_tree_loop")
 
 
 def mtp_quantize_int4_g64(w: torch.Tensor, q: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor,

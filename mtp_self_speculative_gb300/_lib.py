@@ -53,6 +53,12 @@ class MTPLoop(ctypes.Structure):
                 ("conf", c_void_p)]
 
 
+class MTPTree(ctypes.Structure):
+    _fields_ = [("B", c_int), ("branching", c_int), ("depth", c_int), ("n_assist", c_int),
+                ("scratch_blocks", c_void_p), ("ws", c_void_p), ("ws_bytes", c_size_t), ("tokens", c_void_p),
+                ("parents", c_void_p), ("depths", c_void_p)]
+
+
 # name -> (restype, argtypes); every symbol declared in include/mtp.h
 SIGNATURES = {
     "mtp_init": (c_int, [ctypes.POINTER(MTPConfig), ctypes.POINTER(MTPWeights), c_int, ctypes.POINTER(c_void_p)]),
@@ -74,6 +80,15 @@ SIGNATURES = {
     "mtp_loop_advance": (c_int, [c_void_p, c_void_p, c_int, c_int, P_i32, P_i32, P_i32, c_void_p, P_i32, P_i32,
                                  c_void_p, c_void_p, P_i32, P_i32, c_int]),
     "mtp_spec_loop": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPLoop), c_int]),
+    "mtp_tree_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int, c_int, c_int, c_int]),
+    "mtp_draft_tree": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, P_i32, ctypes.POINTER(MTPKV),
+                               ctypes.POINTER(MTPTree)]),
+    "mtp_synth_target_tree": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPTree), c_void_p, P_i32, ctypes.c_uint64,
+                                      c_void_p, P_i32]),
+    "mtp_verify_tree": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPTree), c_void_p, P_i32, P_i32, P_i32]),
+    "mtp_tree_commit": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPTree), P_i32]),
+    "mtp_tree_loop": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPLoop),
+                              ctypes.POINTER(MTPTree), c_int]),
     "mtp_get_device_error": (c_int, [c_void_p]),
     "mtp_destroy": (None, [c_void_p]),
     "mtp_status_str": (ctypes.c_char_p, [c_int]),

@@ -45,6 +45,22 @@ cudaError_t ensure_smem(const void* func, size_t bytes) {
 
 using namespace mtp;
 
+// One draft step k of K for B requests on the per-step kernels (quantized,
+// tensor-core or streamed, as mtp_draft chooses).
+cudaError_t mtp::draft_one_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,
+                                const void* embeds, const int32_t* positions, const mtp_kv* kv,
+                                const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out) {
+  if (ctx->quantized)
+    return launch_draft_step_q(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids, logits,
+                               hidden_out);
+  if (tc_supported(ctx, B))
+    return launch_draft_step_tc(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids, logits,
+                                hidden_out);
+  return launch_draft_step(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids, logits,
+                           hidden_out);
+}
+
+
 extern "C" {
 
 const char* mtp_status_str(mtp_status s) {
@@ -317,12 +333,9 @@ mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, cons
   if (persistent_supported(ctx, B))
     return after_launch(launch_draft_persistent(ctx, s, B, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
                                                 logits, hidden_out));
-  const bool tc = tc_supported(ctx, B);
   for (int k = 1; k <= K; ++k) {
-    cudaError_t e = tc ? launch_draft_step_tc(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
-                                              logits, hidden_out)
-                       : launch_draft_step(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids,
-                                           logits, hidden_out);
+    cudaError_t e = draft_one_step(ctx, s, B, k, K, hidden, embeds, positions, kv, chain_ids, draft_ids, logits,
+                                   hidden_out);
     if (e != cudaSuccess) return after_launch(e);
   }
   return after_launch(cudaGetLastError());
