@@ -555,7 +555,18 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     w = synth.copy_head(cfg, synth.make_weights(cfg, norm="ones"))
     thr = int(args.loop_alpha * 2 ** 53)
     total = args.warmup + args.steps + 2 * max(5, args.steps // 4) + 8
-    kv0 = synth.make_kv(cfg, lens, extra_slots=K * total + K + 1)
+    tree_shape = tuple(int(x) for x in args.tree.split(",")) if args.tree else None
+    if tree_shape:
+        K = tree_shape[1]                      # an accepted path is at most tree_depth long
+    kv0 = synth.make_kv(cfg, lens, extra_slots=(K + 1) * total + K + 1)
+    scratch = None
+    if tree_shape:
+        bf_, td_, _ = tree_shape
+        n_extra = max(td_ - 1, 1) * B * bf_ * 2
+        zeros = np.zeros((n_extra,) + kv0.k_pool.shape[1:], dtype=kv0.k_pool.dtype)
+        scratch = np.arange(kv0.k_pool.shape[0], kv0.k_pool.shape[0] + n_extra, dtype=np.int32)
+        kv0 = synth.KVState(np.concatenate([kv0.k_pool, zeros]), np.concatenate([kv0.v_pool, zeros]),
+                            kv0.block_table, kv0.seq_len, kv0.pending, kv0.block_size)
 
     def dev(a):
         a = np.ascontiguousarray(a)
@@ -563,12 +574,25 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
         return torch.from_numpy(a).cuda()
     wdev = {k: dev(v) for k, v in w.items()}
+    max_batch = B * tree_shape[0] if tree_shape else B
     ctx = M.mtp_init(M.make_config(cfg.H, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.ffn, cfg.vocab, cfg.eps,
-                                   cfg.rope_theta, cfg.dtype, B, K, cfg.block_size,
+                                   cfg.rope_theta, cfg.dtype, max_batch, max(K, 2), cfg.block_size,
                                    int(lens.max()) + (K + 1) * total + 8,
                                    weight_format=args.weights), wdev)
     kv = M.KVCache(dev(kv0.k_pool), dev(kv0.v_pool), dev(kv0.block_table), dev(kv0.seq_len), dev(kv0.pending))
     lp = M.SpecLoop(ctx, B, K, thr, out_cap=(K + 1) * total, conf_threshold=args.conf_threshold)
+    tree = None
+    if tree_shape:
+        tree = M.TreeDraft(ctx, B, tree_shape[0], tree_shape[1], tree_shape[2], kv0.block_table.shape[1],
+                           dev(scratch))
+        lp.target_logits = torch.zeros((B * (1 + tree_shape[2]), cfg.vocab), dtype=lp.target_logits.dtype,
+                                       device="cuda")
+
+    def run_loop(n):
+        if tree is not None:
+            M.mtp_tree_loop(ctx, kv, lp, tree, n)
+        else:
+            M.mtp_spec_loop(ctx, kv, lp, n)
     h0 = synth.loop_start_hashes(cfg, B)
     last0 = synth.uniform_int(cfg.seed, 95, (B,), 0, cfg.vocab)
     lp.seq_hash.copy_(torch.from_numpy(h0.view(np.int64)).cuda())
@@ -579,7 +603,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     lp.hidden.copy_(dev(synth.make_draft_inputs(cfg, w, lens).hidden))
     stream = torch.cuda.current_stream()
 
-    M.mtp_spec_loop(ctx, kv, lp, args.warmup)
+    run_loop(args.warmup)
     torch.cuda.synchronize()
     assert M.mtp_get_device_error(ctx) == 0
     n0 = int(lp.out_len.sum().item())
@@ -591,7 +615,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    M.mtp_spec_loop(ctx, kv, lp, args.steps)
+    run_loop(args.steps)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -604,7 +628,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     # LM-head launches timed on the library's stream (separate pass)
     nprof = max(5, args.steps // 4)
     M.mtp_profile_begin(ctx, M.MTP_KERNEL_LM_HEAD, nprof * K)
-    M.mtp_spec_loop(ctx, kv, lp, nprof)
+    run_loop(nprof)
     torch.cuda.synchronize()
     lm_ms = M.mtp_profile_end(ctx, nprof * K)
 
@@ -614,7 +638,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     e0 = int(lp.out_len.sum().item())
     te = time.perf_counter()
     for _ in range(ne):
-        M.mtp_spec_loop(ctx, kv, lp, 1)
+        run_loop(1)
         h_len.copy_(lp.out_len, non_blocking=True)
         torch.cuda.synchronize()
     te = time.perf_counter() - te
@@ -624,7 +648,8 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
     peaks, peak_kind = measured_peaks()
     peak = float(peaks["hbm_gbs"])
     fmt = args.weights
-    lm_bytes = kernel_bytes(cfg, lens, K, with_logits=False, fmt=fmt)["lm_head"]
+    lm_bytes = kernel_bytes(cfg, lens, K, with_logits=bool(tree_shape or args.conf_threshold > 0),
+                            fmt=fmt)["lm_head"]
     lm_gbs = lm_bytes / (statistics.mean(lm_ms) * 1e-3) / 1e9
     value = world * emitted / (ms * 1e-3)
     line = {
@@ -634,6 +659,8 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
         "data": "synthetic (copy-head weights, deterministic synthetic verifier)",
         "config": {"workload": "spec_loop_" + cfg.name, "batch": B, "draft_steps_K": K,
                    "sticky_alpha": args.loop_alpha, "weights": fmt, "conf_threshold": args.conf_threshold,
+                   "tree": ({"branching_factor": tree_shape[0], "tree_depth": tree_shape[1],
+                             "num_assistant_tokens": tree_shape[2]} if tree_shape else None),
                    "mean_emitted_per_step": emitted / (B * args.steps),
                    "l2": "inputs larger than L2 (weights streamed every draft step)"},
         "roofline": {"kernel": "lm_head_argmax" if fmt == "dense" else "lm_head_argmax_int8", "bound": "hbm",
@@ -645,7 +672,7 @@ def run_loop_workload(args, cfg, rank, world, local_rank):
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and tree_shape is None:
         line["cpu_baseline"] = loop_cpu_baseline(cfg, w, lens, h0, last0, thr, fmt)
     print(json.dumps(line), flush=True)
 
@@ -901,6 +928,8 @@ def main(argv=None):
                     help="probability that the synthetic verifier repeats the last token (--loop)")
     ap.add_argument("--conf-threshold", type=float, default=0.0,
                     help="with --loop: propose only the leading drafts whose probability exceeds it (0: off)")
+    ap.add_argument("--tree", default=None,
+                    help="with --loop: tree drafting 'branching_factor,tree_depth,num_assistant_tokens'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")

@@ -34,8 +34,10 @@ struct TreeLayout {
   int nV, NL, NC, rows;
   size_t root_hid, hid_out, step_logits, step_ids, chain, vbt, vseq, vpend, vpos, topk_tok, topk_lp;
   size_t cand_tok, cand_par, cand_depth, cand_src, cand_exp, cand_score, cand_n, surv, sel, keys, path_nodes;
-  size_t copy_src, copy_dst, total;
+  size_t copy_src, copy_dst, part_ms, part_keys, total;
 };
+
+constexpr int kTopkSlices = 64;
 
 static size_t tl_align(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -75,6 +77,8 @@ static TreeLayout tree_layout(const mtp_ctx* ctx, int B, int bf, int td, int n_a
   t.path_nodes = take((size_t)B * td * 4);
   t.copy_src = take((size_t)t.nV * 2 * 4);
   t.copy_dst = take((size_t)t.nV * 2 * 4);
+  t.part_ms = take((size_t)t.rows * kTopkSlices * 2 * 4);
+  t.part_keys = take((size_t)t.rows * kTopkSlices * bf * 8);
   const size_t nl = (size_t)(t.NL > 0 ? t.NL : 1) * t.nV;
   t.vseq = take(nl * 4);
   t.vpend = take(nl * 4);
@@ -85,19 +89,23 @@ static TreeLayout tree_layout(const mtp_ctx* ctx, int B, int bf, int td, int n_a
 }
 
 // Top-bf tokens of a logits row (larger first, lower id on ties) and their
-// log-softmax values.  One block per row; each thread keeps its own top list
-// of the strided share, warp 0 merges the lists.
-__global__ void tree_topk_kernel(const float* logits, size_t row_stride, size_t row_off, int V, int bf,
-                                 int32_t* out_tok, float* out_lp) {
+// log-softmax values, in two kernels.  Partial: grid (slices, rows); each
+// block takes one vocabulary slice and writes its max, its sum of
+// exp(z - max) and its top-bf keys (orderable value, lowest id on ties).
+__global__ void tree_topk_partial_kernel(const float* logits, size_t row_stride, size_t row_off, int V, int bf,
+                                         float* part_ms, unsigned long long* part_keys) {
   __shared__ unsigned long long cand[256 * kTreeMaxBf];
   __shared__ float red[8];
-  const float* z = logits + (size_t)blockIdx.x * row_stride + row_off;
+  const int row = blockIdx.y, sl = blockIdx.x;
+  const float* z = logits + (size_t)row * row_stride + row_off;
+  const int per = (V + kTopkSlices - 1) / kTopkSlices;
+  const int v0 = sl * per, v1 = min(V, v0 + per);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   float m = -INFINITY;
   unsigned long long top[kTreeMaxBf];
 #pragma unroll
   for (int i = 0; i < kTreeMaxBf; ++i) top[i] = 0ull;
-  for (int v = threadIdx.x; v < V; v += 256) {
+  for (int v = v0 + threadIdx.x; v < v1; v += 256) {
     const float x = z[v];
     m = fmaxf(m, x);
     unsigned long long key = argmax_key(x, (uint32_t)v);
@@ -120,15 +128,14 @@ __global__ void tree_topk_kernel(const float* logits, size_t row_stride, size_t 
   for (int i = 1; i < 8; ++i) m = fmaxf(m, red[i]);
   __syncthreads();
   float sum = 0.0f;
-  for (int v = threadIdx.x; v < V; v += 256) sum += expf(z[v] - m);
+  if (m > -INFINITY)
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) sum += expf(z[v] - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane == 0) red[w] = sum;
   __syncthreads();
   if (w == 0) {
-    float tot = 0.0f;
-    for (int i = 0; i < 8; ++i) tot += red[i];
-    const float lse = m + logf(tot);
+    const size_t pk = ((size_t)row * kTopkSlices + sl) * bf;
     for (int r = 0; r < bf; ++r) {
       unsigned long long best = 0ull;
       for (int i = lane; i < 256 * kTreeMaxBf; i += 32) best = umax64(best, cand[i]);
@@ -136,11 +143,42 @@ __global__ void tree_topk_kernel(const float* logits, size_t row_stride, size_t 
       for (int i = lane; i < 256 * kTreeMaxBf; i += 32)
         if (cand[i] == best) cand[i] = 0ull;
       __syncwarp();
-      if (lane == 0) {
-        const int idx = best ? (int)key_index(best) : 0;
-        out_tok[(size_t)blockIdx.x * bf + r] = idx;
-        out_lp[(size_t)blockIdx.x * bf + r] = z[idx] - lse;
-      }
+      if (lane == 0) part_keys[pk + r] = best;
+    }
+    if (lane == 0) {
+      float tot = 0.0f;
+      for (int i = 0; i < 8; ++i) tot += red[i];
+      part_ms[((size_t)row * kTopkSlices + sl) * 2] = m;
+      part_ms[((size_t)row * kTopkSlices + sl) * 2 + 1] = tot;
+    }
+  }
+}
+
+// Merge: one warp per row; slices combined in order (deterministic).
+__global__ void tree_topk_merge_kernel(const float* logits, size_t row_stride, size_t row_off, int bf,
+                                       const float* part_ms, unsigned long long* part_keys, int32_t* out_tok,
+                                       float* out_lp) {
+  const int row = blockIdx.x, lane = threadIdx.x;
+  const float* z = logits + (size_t)row * row_stride + row_off;
+  const float* pm = part_ms + (size_t)row * kTopkSlices * 2;
+  float m = -INFINITY;
+  for (int i = 0; i < kTopkSlices; ++i) m = fmaxf(m, pm[2 * i]);
+  float sum = 0.0f;
+  for (int i = 0; i < kTopkSlices; ++i)
+    if (pm[2 * i] > -INFINITY) sum += pm[2 * i + 1] * expf(pm[2 * i] - m);
+  const float lse = m + logf(sum);
+  unsigned long long* pk = part_keys + (size_t)row * kTopkSlices * bf;
+  for (int r = 0; r < bf; ++r) {
+    unsigned long long best = 0ull;
+    for (int i = lane; i < kTopkSlices * bf; i += 32) best = umax64(best, pk[i]);
+    best = warp_max_u64(best);
+    for (int i = lane; i < kTopkSlices * bf; i += 32)
+      if (pk[i] == best) pk[i] = 0ull;
+    __syncwarp();
+    if (lane == 0) {
+      const int idx = best ? (int)key_index(best) : 0;
+      out_tok[(size_t)row * bf + r] = idx;
+      out_lp[(size_t)row * bf + r] = z[idx] - lse;
     }
   }
 }
@@ -239,7 +277,9 @@ __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
   const int L = a.real_seq[b];
   const int bL = L / 16;
   const bool fits = bL + 1 < a.max_blocks;
+  __shared__ int s_p0[kTreeMaxBf], s_p1[kTreeMaxBf], s_ok[kTreeMaxBf];
   if (!fits && threadIdx.x == 0) set_error(a.err, MTP_ERR_CAPACITY);
+  const int32_t* real = a.real_bt + (size_t)b * a.max_blocks;
   for (int i = threadIdx.x; i < bf; i += blockDim.x) {
     const int s = s_surv[i];
     const int v = b * bf + i;
@@ -249,16 +289,12 @@ __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
     a.vseq[v] = L + l - 2;
     a.vpend[v] = 1;
     a.vpos[v] = a.positions[b] + l - 2;
-    int32_t* row = a.vbt + (size_t)v * a.max_blocks;
-    const int32_t* real = a.real_bt + (size_t)b * a.max_blocks;
-    for (int j = 0; j < a.max_blocks; ++j) row[j] = real[j];
     const int32_t p0 = a.scratch[((size_t)e * a.nV + v) * 2], p1 = a.scratch[((size_t)e * a.nV + v) * 2 + 1];
     const bool ok = fits && p0 >= 0 && p0 < a.num_blocks && p1 >= 0 && p1 < a.num_blocks;
     if (!ok) set_error(a.err, MTP_ERR_DEVICE_ARGS);
-    if (fits) {
-      row[bL] = ok ? p0 : real[bL];
-      row[bL + 1] = ok ? p1 : real[bL + 1];
-    }
+    s_p0[i] = p0;
+    s_p1[i] = p1;
+    s_ok[i] = ok;
     // private blocks start as copies of the proposer's: the request's own
     // blocks for a layer-1 node, the proposing expansion's private blocks
     // otherwise; the second holds entries only once the path reaches it
@@ -269,6 +305,15 @@ __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
     const int last_slot = L + l - 2;   // the proposer's own entry
     a.copy_src[v * 2 + 1] = (ok && last_slot >= (bL + 1) * 16) ? from[bL + 1] : -1;
     a.copy_dst[v * 2 + 1] = (ok && last_slot >= (bL + 1) * 16) ? p1 : -1;
+  }
+  __syncthreads();
+  // block tables: the request's own, with the two private blocks in place
+  for (int t = threadIdx.x; t < bf * a.max_blocks; t += blockDim.x) {
+    const int i = t / a.max_blocks, j = t - i * a.max_blocks;
+    int32_t val = real[j];
+    if (s_ok[i] && j == bL) val = s_p0[i];
+    if (s_ok[i] && j == bL + 1) val = s_p1[i];
+    a.vbt[(size_t)(b * bf + i) * a.max_blocks + j] = val;
   }
   // hidden states of the survivors' proposers
   for (int t = threadIdx.x; t < bf * a.H; t += blockDim.x) {
@@ -541,9 +586,12 @@ extern "C" mtp_status mtp_draft_tree(mtp_ctx* ctx, void* stream, const void* hid
   if ((e = draft_one_step(ctx, s, B, 1, 1, hidden, embeds, positions, kv, nullptr, step_ids, step_logits,
                           (float*)(ws + Lo.root_hid))) != cudaSuccess)
     return tree_status(e);
-  tree_topk_kernel<<<B, 256, 0, s>>>(step_logits, V, 0, (int)V, bf, topk_tok, topk_lp);
+  float* part_ms = (float*)(ws + Lo.part_ms);
+  unsigned long long* part_keys = (unsigned long long*)(ws + Lo.part_keys);
+  tree_topk_partial_kernel<<<dim3(kTopkSlices, B), 256, 0, s>>>(step_logits, V, 0, (int)V, bf, part_ms, part_keys);
+  tree_topk_merge_kernel<<<B, 32, 0, s>>>(step_logits, V, 0, bf, part_ms, part_keys, topk_tok, topk_lp);
   tree_root_kernel<<<B, 32, 0, s>>>(B, bf, Lo.NC, topk_tok, topk_lp, c);
-  ctx->launches += 2;
+  ctx->launches += 3;
   const size_t block_elems = (size_t)ctx->cfg.n_kv_heads * 16 * ctx->cfg.head_dim;
   for (int l = 2; l <= td; ++l) {
     const int ei = l - 2;
@@ -578,9 +626,11 @@ extern "C" mtp_status mtp_draft_tree(mtp_ctx* ctx, void* stream, const void* hid
     if ((e = draft_one_step(ctx, s, Lo.nV, 2, 2, hidden, embeds, a.vpos, &vk, a.chain, step_ids, step_logits,
                             (float*)(ws + Lo.hid_out) + (size_t)ei * Lo.nV * H)) != cudaSuccess)
       return tree_status(e);
-    tree_topk_kernel<<<Lo.nV, 256, 0, s>>>(step_logits, 2 * V, V, (int)V, bf, topk_tok, topk_lp);
+    tree_topk_partial_kernel<<<dim3(kTopkSlices, Lo.nV), 256, 0, s>>>(step_logits, 2 * V, V, (int)V, bf, part_ms,
+                                                                         part_keys);
+    tree_topk_merge_kernel<<<Lo.nV, 32, 0, s>>>(step_logits, 2 * V, V, bf, part_ms, part_keys, topk_tok, topk_lp);
     tree_children_kernel<<<B, 64, 0, s>>>(bf, Lo.NC, l, a.surv, topk_tok, topk_lp, c);
-    ctx->launches += 2;
+    ctx->launches += 3;
   }
   tree_select_kernel<<<B, 256, 0, s>>>(t->n_assist, Lo.NC, c, (int32_t*)(ws + Lo.sel), t->tokens, t->parents,
                                        t->depths);
