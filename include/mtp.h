@@ -170,12 +170,16 @@ mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, cons
 /* Greedy verification ("Overview" of the speculative-decoding page).
  * For request b with K_b = num_drafts[b] (0..max_k) drafts, target rows
  * row_offsets[b] .. row_offsets[b] + K_b of target_logits [num_rows, V]
- * (dtype) give r_j = argmax of row j (lowest id on ties); accepted[b] = the
+ * (dtype) give r_j = argmax of row j (lowest id on ties, -0 equal to +0, NaN
+ * entries passed over; a row of NaN only gives r_j = -1); accepted[b] = the
  * largest a <= K_b with drafts[b*drafts_stride + j] == r_j for all j < a;
  * bonus[b] = r_a.  Device-checked per request: K_b <= min(max_k,
  * drafts_stride), row_offsets[b+1] - row_offsets[b] == K_b + 1, and the rows
- * lie inside [0, num_rows); on violation nothing of the request is read,
- * accepted[b] = bonus[b] = -1 and the error word is set. */
+ * lie inside [0, num_rows); on violation accepted[b] = bonus[b] = -1 and the
+ * error word is set.  Every one of the num_rows rows is read (the rows are
+ * scanned as one flat range split evenly over the grid), so num_rows must not
+ * exceed the rows target_logits holds; host-checked: 1 <= num_rows <=
+ * max_batch * (max_k + 1), else MTP_ERR_INVALID. */
 mtp_status mtp_verify(mtp_ctx* ctx, void* stream, int B, const void* target_logits, int num_rows,
                       const int32_t* row_offsets, const int32_t* drafts, int drafts_stride,
                       const int32_t* num_drafts, int32_t* accepted, int32_t* bonus);
@@ -189,10 +193,10 @@ mtp_status mtp_verify(mtp_ctx* ctx, void* stream, int B, const void* target_logi
  * caller cannot create a context there).  Same arguments and results as
  * mtp_verify, with the shape passed directly: vocab, dtype (mtp_dtype) and
  * max_k (0..100) in place of the context.
- *   Scratch: a fixed array of 65536 argmax keys and 4096 counters (about
- *   530 KB) that is part of the library's device image; every GPU that loads
- *   the library holds it until the process exits.  Requires B <= 4096 and
- *   B * (max_k + 1) <= 65536, else MTP_ERR_INVALID.
+ *   Scratch: a fixed array of 65536 argmax keys and one arrival counter
+ *   (about 512 KB) that is part of the library's device image; every GPU that
+ *   loads the library holds it until the process exits.  Requires B <= 4096,
+ *   B * (max_k + 1) <= 65536 and num_rows <= 65536, else MTP_ERR_INVALID.
  *   Set-up: the first call on a device looks up that array's device address
  *   (once per device, under a lock); make that first call before any stream
  *   capture on the device.

@@ -169,7 +169,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   const size_t o_part = take(part_rows * (c.head_dim + 4) * 4);
   const size_t o_acnt = take(maxB * c.n_kv_heads * 4);
   const size_t o_lmk = take(maxB * 8), o_lmc = take(4);
-  const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(maxB * 4);
+  const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(256);
   const size_t o_err = take(4);
   const size_t o_bad = take(maxB * 4);
   const size_t o_rope = take(rope_n * sizeof(float2));
@@ -344,7 +344,9 @@ mtp_status mtp_draft(mtp_ctx* ctx, void* stream, int B, const void* hidden, cons
 mtp_status mtp_verify(mtp_ctx* ctx, void* stream, int B, const void* target_logits, int num_rows,
                       const int32_t* row_offsets, const int32_t* drafts, int drafts_stride,
                       const int32_t* num_drafts, int32_t* accepted, int32_t* bonus) {
-  if (!ctx || B < 1 || B > ctx->cfg.max_batch || num_rows < 1) return MTP_ERR_INVALID;
+  if (!ctx || B < 1 || B > ctx->cfg.max_batch || num_rows < 1 ||
+      num_rows > ctx->cfg.max_batch * (ctx->cfg.max_k + 1))
+    return MTP_ERR_INVALID;
   if (!target_logits || !row_offsets || !drafts || !num_drafts || !accepted || !bonus || drafts_stride < 1)
     return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;

@@ -223,7 +223,7 @@ struct mtp_ctx {
   unsigned long long* lm_keys;  // [maxB] argmax keys
   int* lm_cnt;                  // [1]
   unsigned long long* ver_keys; // [maxB, max_k + 1]
-  int* ver_cnt;                 // [maxB]
+  int* ver_cnt;                 // [1]
   int* err;                     // [1]
   int* req_bad;                 // [maxB] 1: pending was not 0 when the draft call began
   float2* rope;                 // [max_pos, head_dim / 2] (cos, sin)

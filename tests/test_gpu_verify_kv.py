@@ -77,6 +77,86 @@ def test_verify_edges_unaligned_vocab_zero_drafts_and_ties(dtype):
     np.testing.assert_array_equal(bon, r[vi.row_offsets[1:] - 1])
 
 
+def _adversarial_rows(V, dtype, seed):
+    """Rows that stress the argmax scan: a constant row, a row of -inf, -0/+0
+    as the maximum in both orders, the maximum repeated at spread-out ids,
+    record-breaking values at every 1000th id, a maximum in the first and in
+    the last element, and plain normal rows.  Seeded numpy, float64 values
+    exact in the stored dtype."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    rows.append(np.full(V, 0.5))
+    rows.append(np.full(V, -np.inf))
+    r = -1.0 - rng.random(V); r[V // 2] = -0.0; r[3] = 0.0; rows.append(r)
+    r = -1.0 - rng.random(V); r[V - 7] = 0.0; r[101] = -0.0; rows.append(r)
+    r = rng.standard_normal(V); at = rng.choice(V, 9, replace=False); r[at] = 6.0; rows.append(r)
+    r = rng.standard_normal(V) - 10.0; r[::1000] = np.arange(len(r[::1000])) * 0.25; rows.append(r)
+    r = rng.standard_normal(V); r[0] = 9.0; rows.append(r)
+    r = rng.standard_normal(V); r[V - 1] = 9.0; rows.append(r)
+    while len(rows) < 24:
+        rows.append(rng.standard_normal(V))
+    z = np.stack(rows)
+    if dtype == "bf16":
+        return synth.f32_to_bf16_bits(z.astype(np.float32))
+    return z.astype(np.float32)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 151936), ("f32", 151936), ("bf16", 40009), ("f32", 1001)])
+def test_verify_adversarial_rows_all_accepted(dtype, V):
+    """Every row's argmax is observed: the drafts are the oracle's argmaxes,
+    so the GPU accepts all K_b drafts only if every row agrees.  The rows
+    ([24, V], odd V gives misaligned row starts) are cut by the flat split of
+    the scan at many points inside rows."""
+    import mtp_self_speculative_gb300 as M
+    lg = _adversarial_rows(V, dtype, seed=77 + V)
+    nd = np.array([4, 0, 7, 2, 6], dtype=np.int32)           # 24 rows
+    ro = np.concatenate([[0], np.cumsum(nd + 1)]).astype(np.int32)
+    r = O.argmax_lowest(O.widen(lg, dtype))
+    assert r[0] == 0 and r[1] == 0 and r[2] == 3 and r[3] == 101
+    drafts = np.full((len(nd), 8), -1, dtype=np.int32)
+    for b in range(len(nd)):
+        drafts[b, :nd[b]] = r[ro[b]:ro[b] + nd[b]]
+    cfg = synth.MTPShape("adv", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=V, batch=len(nd), K=8,
+                         dtype=dtype, ctx_lo=1, ctx_hi=1, seed_index=41)
+    ctx = make_context(cfg, None, max_batch=len(nd), max_k=8)
+    acc = torch.empty(len(nd), dtype=torch.int32, device="cuda")
+    bon = torch.empty(len(nd), dtype=torch.int32, device="cuda")
+    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc, bon)
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(ctx) == 0
+    acc_o, bon_o = O.verify(lg, ro, drafts, nd, dtype)
+    np.testing.assert_array_equal(acc_o, nd)
+    np.testing.assert_array_equal(host(acc), acc_o)
+    np.testing.assert_array_equal(host(bon), bon_o)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_nan_entries_are_passed_over(dtype):
+    """NaN logits are not candidates (the library's stated behaviour; the
+    pages never meet NaN): the argmax is that of the other entries, and a row
+    of NaN only gives r = -1."""
+    import mtp_self_speculative_gb300 as M
+    V = 3000
+    z = np.zeros((3, V))
+    z[0, :] = np.nan
+    z[1, :] = -1.0; z[1, 0] = np.nan; z[1, 2999] = np.nan; z[1, 1234] = 2.0; z[1, 1500:1600] = np.nan
+    z[2, :] = -2.0; z[2, 7] = np.nan; z[2, 2048] = 0.5
+    lg = synth.f32_to_bf16_bits(z.astype(np.float32)) if dtype == "bf16" else z.astype(np.float32)
+    nd = np.array([0, 1], dtype=np.int32)      # request 0: row 0; request 1: rows 1, 2
+    ro = np.array([0, 1, 3], dtype=np.int32)
+    drafts = np.array([[-1], [1234]], dtype=np.int32)
+    cfg = synth.MTPShape("nan", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=V, batch=2, K=1,
+                         dtype=dtype, ctx_lo=1, ctx_hi=1, seed_index=42)
+    ctx = make_context(cfg, None, max_batch=2, max_k=1)
+    acc = torch.empty(2, dtype=torch.int32, device="cuda")
+    bon = torch.empty(2, dtype=torch.int32, device="cuda")
+    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc, bon)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(acc), [0, 1])
+    np.testing.assert_array_equal(host(bon), [-1, 2048])
+    assert M.mtp_get_device_error(ctx) == 0
+
+
 def test_verify_inconsistent_offsets_sets_error():
     import mtp_self_speculative_gb300 as M
     cfg = synth.shrink(synth.VERIFY_B64, vocab=512, batch=4)
