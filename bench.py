@@ -43,8 +43,12 @@ METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM ro
 # dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch from an ncu capture of the
 # current kernel (profiles/lm_head_argmax_qwen3_8b_mtp_b1.md); other workloads report null.
 LM_TRAFFIC = {
-    "qwen3_8b_mtp_b1": 1244760000 + 3036928,
+    "qwen3_8b_mtp_b1": 1244862000 + 3273216,
     "qwen3_8b_mtp_b1:int4_g64": 622737408 + 3309056,
+}
+# The same for one verify launch (profiles/verify_rollback_b64.md).
+VERIFY_TRAFFIC = {
+    "verify_rollback_b64": 111302144 + 3310848,
 }
 # The same for one launch of the persistent draft kernel (all K steps); null until captured.
 PERSISTENT_TRAFFIC = {}
@@ -813,8 +817,8 @@ def run_verify_workload(args, cfg, rank, world, local_rank):
                          "%.1f MB of logits per call" % (ver_bytes / 1e6)},
         "verify_ms": tv, "commit_ms": statistics.median(t_com),
         "roofline": {"kernel": "verify", "bound": "hbm", "achieved": ver_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": ver_gbs / peak, "peak_source": peak_kind + " hbm_gbs", "traffic": None,
-                     "bytes_per_launch": ver_bytes},
+                     "frac": ver_gbs / peak, "peak_source": peak_kind + " hbm_gbs",
+                     "traffic": VERIFY_TRAFFIC.get(cfg.name), "bytes_per_launch": ver_bytes},
         "commit_bytes": com_bytes,
         "e2e": {"value": 1.0 / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": ver_bytes,
                 "d2h_bytes_per_step": 2 * B * 4},
