@@ -328,9 +328,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 #pragma unroll
       for (int j = 0; j < NB; ++j) {
         if (j < nb) {
-          const float* xp = xs + (size_t)j * C + (size_t)v * VPE;
-          acc0[j] += dot_vec<T>(wa, xp);
-          acc1[j] += dot_vec<T>(wb, xp);
+          const float* xr = xs + (size_t)j * C;
+          acc0[j] += dot_vec_xs<T>(wa, xr, v, C);
+          acc1[j] += dot_vec_xs<T>(wb, xr, v, C);
         }
       }
     }
@@ -404,15 +404,24 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
     const size_t budget = (size_t)ctx->gemv_budget_kb[KIND] * 1024;
     int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;
     if (max_stages > kMaxTmaStages) max_stages = kMaxTmaStages;
-    // stages = consumers * k: pick the consumer count (4..8) that keeps the most stages
+    // stages = consumers * k.  One row: pick the consumer count (4..8) that
+    // keeps the most stages.  Two or four rows: the consumers' arithmetic
+    // grows with the rows while the bytes do not, so keep all eight consumer
+    // warps whenever eight stages fit.
     int consumers = 0, stages = 0;
-    for (int cw = kTmaConsumers; cw >= 1; --cw) {
-      const int st = cw * (max_stages / cw);
-      if (st > stages || (st == stages && st > 0 && cw > consumers && cw <= max_stages)) {
-        stages = st;
-        consumers = cw;
+    if (nbt >= 2 && max_stages >= kTmaConsumers) {
+      consumers = kTmaConsumers;
+      stages = kTmaConsumers * (max_stages / kTmaConsumers);
+    }
+    if (stages == 0) {
+      for (int cw = kTmaConsumers; cw >= 1; --cw) {
+        const int st = cw * (max_stages / cw);
+        if (st > stages || (st == stages && st > 0 && cw > consumers && cw <= max_stages)) {
+          stages = st;
+          consumers = cw;
+        }
+        if (cw <= 4 && stages > 0) break;
       }
-      if (cw <= 4 && stages > 0) break;
     }
     if (((ctx->gemv_stream_mask >> KIND) & 1) && a.B <= 4 && stages >= 2 && consumers >= 2) {
       const size_t smem_t = stages * stage_stride + xs_bytes;

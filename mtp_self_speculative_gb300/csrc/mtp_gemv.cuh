@@ -204,13 +204,48 @@ __device__ __forceinline__ void load8_row(const S* p, float (&x)[8]) {
   }
 }
 
-// Copy n values (fp32 or T; n % 8 == 0) into dst (fp32) times the norm
-// weight w (if any); returns this thread's sum of squares of the raw
-// values.  Source and weight loads are independent and vectorised, so a
-// 4096-wide row costs each consumer thread two groups: about one L2 round
-// trip.
+// Layout of a staged input row (fp32, C values) in shared memory.  A
+// consumer lane takes 16-byte weight vectors v = lane, lane + 32, ... and
+// needs the vector's activations: 8 floats for bf16 weights.  Stored plainly
+// they sit 32 bytes apart from lane to lane, so each 16-byte load of a warp
+// touches every bank twice.  bf16 rows are therefore split in two planes:
+// floats 0..3 of vector v at [4v], floats 4..7 at [C/2 + 4v], and each load
+// of a warp reads 512 contiguous bytes.  fp32 weights (4 per vector) keep
+// the plain layout.
+template <typename T>
+__device__ __forceinline__ int xs_index(int i, int C) {
+  if constexpr (sizeof(T) == 2) return ((i & 7) >> 2) * (C >> 1) + ((i >> 3) << 2) + (i & 3);
+  else return i;
+}
+
+// Dot product of one weight vector with its staged activations (same
+// operation order as dot_vec).
+template <typename T>
+__device__ __forceinline__ float dot_vec_xs(const uint4& w, const float* row, int v, int C) {
+  if constexpr (sizeof(T) == 2) {
+    const float4 a = *reinterpret_cast<const float4*>(row + 4 * v);
+    const float4 b = *reinterpret_cast<const float4*>(row + (C >> 1) + 4 * v);
+    float s = bf16_lo(w.x) * a.x;
+    s = fmaf(bf16_hi(w.x), a.y, s);
+    s = fmaf(bf16_lo(w.y), a.z, s);
+    s = fmaf(bf16_hi(w.y), a.w, s);
+    s = fmaf(bf16_lo(w.z), b.x, s);
+    s = fmaf(bf16_hi(w.z), b.y, s);
+    s = fmaf(bf16_lo(w.w), b.z, s);
+    s = fmaf(bf16_hi(w.w), b.w, s);
+    return s;
+  } else {
+    return dot_vec<T>(w, row + 4 * v);
+  }
+}
+
+// Copy n values (fp32 or T; n % 8 == 0) into elements [e0, e0 + n) of the
+// staged row `row` (C values, layout above) times the norm weight w (if
+// any); returns this thread's sum of squares of the raw values.  Source and
+// weight loads are independent and vectorised, so a 4096-wide row costs each
+// consumer thread two groups: about one L2 round trip.
 template <typename T, typename S>
-__device__ __forceinline__ float cons_stage_raw(float* dst, const S* src, int n, const T* w) {
+__device__ __forceinline__ float cons_stage_raw(float* row, int C, int e0, const S* src, int n, const T* w) {
   const int ct = threadIdx.x - 32;
   float ss = 0.0f;
 #pragma unroll 2
@@ -223,16 +258,18 @@ __device__ __forceinline__ float cons_stage_raw(float* dst, const S* src, int n,
       ss = fmaf(x[e], x[e], ss);
       if (w) x[e] *= wv[e];
     }
-    float4* d = reinterpret_cast<float4*>(dst + (size_t)i8 * 8);
-    d[0] = make_float4(x[0], x[1], x[2], x[3]);
-    d[1] = make_float4(x[4], x[5], x[6], x[7]);
+    const int e = e0 + i8 * 8;
+    float4* d0 = reinterpret_cast<float4*>(row + xs_index<T>(e, C));
+    float4* d1 = reinterpret_cast<float4*>(row + xs_index<T>(e + 4, C));
+    *d0 = make_float4(x[0], x[1], x[2], x[3]);
+    *d1 = make_float4(x[4], x[5], x[6], x[7]);
   }
   return ss;
 }
 
-// Stage the normalised input row(s) of all nb requests: one pass that stores
-// x * w and sums x^2 for every vector, one block reduction for all of them,
-// then the scalar RMS factors applied in shared memory.
+// Stage the normalised input row(s) of all nb requests (layout above): one
+// pass that stores x * w and sums x^2 for every vector, one block reduction
+// for all of them, then the scalar RMS factors applied in shared memory.
 template <typename T, int KIND>
 __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
   constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
@@ -244,28 +281,28 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
     float s0 = 0.0f, s1 = 0.0f;
     if constexpr (KIND == EH_PROJ) {
       if (a.k == 1) {
-        s0 = cons_stage_raw<T, T>(dst, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h);
-        s1 = cons_stage_raw<T, T>(dst + a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e);
+        s0 = cons_stage_raw<T, T>(dst, C, 0, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h);
+        s1 = cons_stage_raw<T, T>(dst, C, a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e);
       } else {
         int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
                              : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
-        s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_h);
+        s0 = cons_stage_raw<T, float>(dst, C, 0, a.hid + (size_t)b * a.H, a.H, a.w_norm_h);
         if (id < 0 || id >= a.V) {
           if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
           id = 0;
         }
-        s1 = cons_stage_raw<T, T>(dst + a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
+        s1 = cons_stage_raw<T, T>(dst, C, a.H, a.embed + (size_t)id * a.H, a.H, a.w_norm_e);
       }
     } else if constexpr (KIND == QKV_ROPE) {
-      s0 = cons_stage_raw<T, float>(dst, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
+      s0 = cons_stage_raw<T, float>(dst, C, 0, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
     } else if constexpr (KIND == O_PROJ) {
-      cons_stage_raw<T, float>(dst, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr);
+      cons_stage_raw<T, float>(dst, C, 0, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr);
     } else if constexpr (KIND == GATE_UP) {
-      s0 = cons_stage_raw<T, float>(dst, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post);
+      s0 = cons_stage_raw<T, float>(dst, C, 0, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post);
     } else if constexpr (KIND == DOWN) {
-      cons_stage_raw<T, float>(dst, a.act + (size_t)b * a.F, a.F, (const T*)nullptr);
+      cons_stage_raw<T, float>(dst, C, 0, a.act + (size_t)b * a.F, a.F, (const T*)nullptr);
     } else {
-      s0 = cons_stage_raw<T, float>(dst, a.hid + (size_t)b * a.H, a.H, a.w_norm_f);
+      s0 = cons_stage_raw<T, float>(dst, C, 0, a.hid + (size_t)b * a.H, a.H, a.w_norm_f);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -289,8 +326,8 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
         float t = 0.0f;
         for (int w = 0; w < kTmaConsumers; ++w) t += red[w * 8 + 2 * b + v];
         const float sc = rsqrtf(t / (float)a.H + a.eps);
-        float* dst = xs + (size_t)b * C + (size_t)v * a.H;
-        for (int i = ct; i < a.H; i += 256) dst[i] *= sc;
+        float* dst = xs + (size_t)b * C;
+        for (int i = ct; i < a.H; i += 256) dst[xs_index<T>(v * a.H + i, C)] *= sc;
       }
   }
   cons_bar();
