@@ -253,6 +253,8 @@ struct TreeSetupArgs {
 
 __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
   __shared__ int s_surv[kTreeMaxBf];
+  __shared__ float s_score[kTreeMaxBf * kTreeMaxBf];
+  __shared__ int s_depth[kTreeMaxBf * kTreeMaxBf];
   const int b = blockIdx.x;
   const int bf = a.bf, l = a.l, e = l - 2;
   const int n = c.n[b];
@@ -264,13 +266,15 @@ __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
     // them (higher score, then earlier creation) and keep the first bf
     const int c0 = n - bf * bf;
     for (int t = threadIdx.x; t < bf * bf; t += blockDim.x) {
-      const int i = c0 + t;
+      s_score[t] = c.score[cb + c0 + t];
+      s_depth[t] = c.depth[cb + c0 + t];
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < bf * bf; t += blockDim.x) {
       int rank = 0;
-      for (int u = 0; u < bf * bf; ++u) {
-        const int j = c0 + u;
-        if (j != i && cand_better(c.score[cb + j], c.depth[cb + j], j, c.score[cb + i], c.depth[cb + i], i)) ++rank;
-      }
-      if (rank < bf) s_surv[rank] = i;
+      for (int u = 0; u < bf * bf; ++u)
+        if (u != t && cand_better(s_score[u], s_depth[u], c0 + u, s_score[t], s_depth[t], c0 + t)) ++rank;
+      if (rank < bf) s_surv[rank] = c0 + t;
     }
   }
   __syncthreads();
@@ -315,14 +319,34 @@ __global__ void tree_setup_kernel(TreeSetupArgs a, TreeCand c) {
     if (s_ok[i] && j == bL + 1) val = s_p1[i];
     a.vbt[(size_t)(b * bf + i) * a.max_blocks + j] = val;
   }
-  // hidden states of the survivors' proposers
-  for (int t = threadIdx.x; t < bf * a.H; t += blockDim.x) {
-    const int i = t / a.H, h = t - i * a.H;
-    const int s = s_surv[i];
-    const int src = c.src[cb + s];
+  // hidden states of the survivors' proposers: 16-byte copies, four loads
+  // issued before their stores (the rows are 16-byte aligned when H % 4 == 0)
+  for (int i = 0; i < bf; ++i) {
+    const int src = c.src[cb + s_surv[i]];
     const float* from = (src < 0) ? a.root_hid + (size_t)b * a.H
                                   : a.hid_out + ((size_t)(e - 1) * a.nV + src) * a.H;
-    a.hid[(size_t)(b * bf + i) * a.H + h] = from[h];
+    float* to = a.hid + (size_t)(b * bf + i) * a.H;
+    const bool vec = (a.H & 3) == 0 && ((uintptr_t)from & 15) == 0 && ((uintptr_t)to & 15) == 0;
+    if (vec) {
+      const int n4 = a.H >> 2;
+      const float4* f4 = reinterpret_cast<const float4*>(from);
+      float4* t4 = reinterpret_cast<float4*>(to);
+      for (int h0 = threadIdx.x; h0 < n4; h0 += 4 * blockDim.x) {
+        float4 v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int h = h0 + q * blockDim.x;
+          if (h < n4) v[q] = __ldcg(f4 + h);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int h = h0 + q * blockDim.x;
+          if (h < n4) t4[h] = v[q];
+        }
+      }
+    } else {
+      for (int h = threadIdx.x; h < a.H; h += blockDim.x) to[h] = __ldcg(from + h);
+    }
   }
 }
 
