@@ -220,9 +220,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
 // ------------------------------------------------- TMA-streamed variant
 //
 // Same work split and epilogues as gemv_kernel, for batches of at most 4:
-// one CTA per SM; warp 0 is a producer that streams this CTA's row pairs
-// into a ring of shared-memory stages with one-dimensional bulk (TMA) copies
-// (one copy per contiguous pair, two for rotary or gate/up pairs), completing
+// one CTA per SM; warp 0 is a producer that streams this CTA's units (row
+// pairs, or single rows for eh_proj and down) into a ring of shared-memory
+// stages with one-dimensional bulk (TMA) copies (one copy per contiguous
+// unit, two for rotary or gate/up pairs), completing
 // on per-stage mbarriers; it starts before the dependency wait, so the ring
 // (about 200 KB per SM) fills while the previous kernel drains.  Warps 1..8
 // stage the normalised input, then consume pairs round-robin from shared
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
   const int p_end = (int)(((long long)(blockIdx.x + 1) * P) / G);
   const int n = p_end - p_begin;
   const uint32_t row_bytes = (uint32_t)C * sizeof(T);
-  const uint32_t stage_stride = (2 * row_bytes + 127) & ~127u;
+  const uint32_t stage_stride = (gemv_unit_rows(KIND) * row_bytes + 127) & ~127u;
   float* xs = reinterpret_cast<float*>(gsm + (size_t)stages * stage_stride);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int VPE = Elem<T>::kPerVec;
@@ -324,13 +325,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 #pragma unroll 4
     for (int v = lane; v < nvec; v += 32) {
       const uint4 wa = *reinterpret_cast<const uint4*>(s0 + (size_t)v * VPE);
-      const uint4 wb = two ? *reinterpret_cast<const uint4*>(s1 + (size_t)v * VPE) : make_uint4(0, 0, 0, 0);
+      if constexpr (gemv_unit_rows(KIND) == 1) {
 #pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        if (j < nb) {
-          const float* xr = xs + (size_t)j * C;
-          acc0[j] += dot_vec_xs<T>(wa, xr, v, C);
-          acc1[j] += dot_vec_xs<T>(wb, xr, v, C);
+        for (int j = 0; j < NB; ++j)
+          if (j < nb) acc0[j] += dot_vec_xs<T>(wa, xs + (size_t)j * C, v, C);
+      } else {
+        const uint4 wb = two ? *reinterpret_cast<const uint4*>(s1 + (size_t)v * VPE) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          if (j < nb) {
+            const float* xr = xs + (size_t)j * C;
+            acc0[j] += dot_vec_xs<T>(wa, xr, v, C);
+            acc1[j] += dot_vec_xs<T>(wb, xr, v, C);
+          }
         }
       }
     }
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       acc0[j] = warp_sum(acc0[j]);
-      acc1[j] = warp_sum(acc1[j]);
+      if constexpr (gemv_unit_rows(KIND) == 2) acc1[j] = warp_sum(acc1[j]);
     }
     if (lane == 0) {
 #pragma unroll
@@ -381,7 +388,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
 template <typename T, int KIND>
 static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& a) {
   const int C = (KIND == EH_PROJ) ? 2 * a.H : (KIND == O_PROJ) ? a.q_dim : (KIND == DOWN) ? a.F : a.H;
-  const int P = (KIND == EH_PROJ || KIND == O_PROJ || KIND == DOWN) ? a.H / 2
+  const int P = (KIND == EH_PROJ || KIND == DOWN) ? a.H
+                : (KIND == O_PROJ) ? a.H / 2
                 : (KIND == QKV_ROPE) ? (a.q_dim + 2 * a.kv_dim) / 2
                 : (KIND == GATE_UP) ? a.F
                                     : (a.V + 1) / 2;
@@ -399,7 +407,7 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
   // TMA-streamed variant for B <= 4
   {
     const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;
-    const size_t stage_stride = ((size_t)2 * C * sizeof(T) + 127) & ~(size_t)127;
+    const size_t stage_stride = ((size_t)gemv_unit_rows(KIND) * C * sizeof(T) + 127) & ~(size_t)127;
     const size_t xs_bytes = (size_t)nbt * C * sizeof(float);
     const size_t budget = (size_t)ctx->gemv_budget_kb[KIND] * 1024;
     int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;

@@ -64,19 +64,25 @@ __device__ __forceinline__ int gemv_cols(const StepArgs<T>& a, int kind) {
   }
 }
 
+// Rows per streamed unit: one for the wide-row kinds (eh_proj reads 2H
+// columns, down F), so that a unit stays at 16-24 KB and the ring keeps
+// enough stages; two (a "pair") otherwise.
+__host__ __device__ constexpr int gemv_unit_rows(int kind) { return (kind == EH_PROJ || kind == DOWN) ? 1 : 2; }
+
+// Number of units of a kind.
 template <typename T>
 __device__ __forceinline__ int gemv_pairs(const StepArgs<T>& a, int kind) {
   switch (kind) {
-    case EH_PROJ: return a.H / 2;
+    case EH_PROJ: return a.H;
     case QKV_ROPE: return (a.q_dim + 2 * a.kv_dim) / 2;
     case O_PROJ: return a.H / 2;
     case GATE_UP: return a.F;
-    case DOWN: return a.H / 2;
+    case DOWN: return a.H;
     default: return (a.V + 1) / 2;
   }
 }
 
-// Rows (r0, r1) of pair p and their weight pointers.  r1 < 0: no second row.
+// Rows (r0, r1) of unit p and their weight pointers.  r1 < 0: no second row.
 template <typename T, int KIND>
 __device__ __forceinline__ void pair_rows(const StepArgs<T>& a, int p, int C, int& r0, int& r1,
                                           const T*& w0, const T*& w1) {
@@ -97,8 +103,13 @@ __device__ __forceinline__ void pair_rows(const StepArgs<T>& a, int p, int C, in
     r1 = p;
     w0 = a.w_gate + (size_t)p * C;
     w1 = a.w_up + (size_t)p * C;
+  } else if constexpr (gemv_unit_rows(KIND) == 1) {
+    r0 = p;
+    r1 = -1;
+    w0 = ((KIND == EH_PROJ) ? a.w_eh : a.w_down) + (size_t)p * C;
+    w1 = nullptr;
   } else {
-    const T* W = (KIND == EH_PROJ) ? a.w_eh : (KIND == O_PROJ) ? a.w_o : (KIND == DOWN) ? a.w_down : a.lm_head;
+    const T* W = (KIND == O_PROJ) ? a.w_o : a.lm_head;
     const int R = (KIND == LM_HEAD) ? a.V : a.H;
     r0 = 2 * p;
     r1 = (2 * p + 1 < R) ? 2 * p + 1 : -1;
