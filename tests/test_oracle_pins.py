@@ -266,7 +266,7 @@ def test_verify_brute_force_against_sequential_statement():
                 assert len(emitted) == acc[0] + 1
 
 
-def test_verify_north_star_invariants_and_ragged_rows():
+def test_verify_accept_invariants_and_ragged_rows():
     cfg = synth.shrink(synth.VERIFY_B64, vocab=512, batch=12)
     vi = synth.make_verify_inputs(cfg)
     acc, bon = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "bf16")
