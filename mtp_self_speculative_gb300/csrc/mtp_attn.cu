@@ -422,13 +422,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int blk1 = min(nblk, blk0 + a.bps);
   const int nsplit = (nblk + a.bps - 1) / a.bps;
 
-  uint32_t qa[8][4];
-  load_q_frags(qa, a.q + (size_t)b * a.n_q * HD + (size_t)(g * G) * HD, a.qscale, lane, G);
-  float o[16][4];
-#pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-  float m_run = -INFINITY, l_run = 0.0f;
-
   unsigned char* my_stage = smem_raw + (size_t)warp * kStages * 2 * TILE_BYTES;
   auto tile_row = [&](int bi) -> int {
     int blk = (bi < a.max_blocks) ? s_bt[bi - blk0] : -1;
@@ -448,6 +441,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   if (lane == 0)
     for (int it = 0; it < count && it < kStages; ++it) issue(it, first + it * kAttnWarps);
   __syncwarp();
+
+  // the query fragments load while the first tiles are in flight
+  uint32_t qa[8][4];
+  load_q_frags(qa, a.q + (size_t)b * a.n_q * HD + (size_t)(g * G) * HD, a.qscale, lane, G);
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f;
 
   int stop_at = -1;
   for (int it = 0; it < count; ++it) {
