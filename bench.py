@@ -861,15 +861,131 @@ def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1, fmt: str = "dense")
                       (sample_steps, cfg.K, len(lens))}
 
 
+def reference_budget_s() -> float:
+    return float(os.environ.get("MTP_REFERENCE_BUDGET_S", "150"))
+
+
+def run_reference_verify(args, cfg, world):
+    """Reference arm of the verify workload: the oracle's verify + commit of
+    the same inputs, one call per step, on this arm's metric and config."""
+    import oracle as O
+    vi = synth.make_verify_inputs(cfg)
+    lens = synth.context_lengths(cfg)
+    kv0 = synth.make_kv(cfg, lens, extra_slots=int(vi.num_drafts.max()) + 1, prefill_slots=lens + vi.num_drafts)
+    kv0.pending = vi.num_drafts.astype(np.int32).copy()
+    B = len(lens)
+    ver_bytes = int(vi.row_offsets[-1]) * cfg.vocab * cfg.elem_bytes
+
+    def call():
+        kv_c = kv0.copy()
+        t = time.perf_counter()
+        acc, _ = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, cfg.dtype)
+        O.kv_commit(kv_c, np.minimum(acc + 1, vi.num_drafts), cfg.dtype)
+        return time.perf_counter() - t
+
+    t_start = time.perf_counter()
+    for _ in range(min(args.warmup, 1)):
+        call()
+    times = []
+    for _ in range(args.steps):
+        times.append(call())
+        if time.perf_counter() - t_start > reference_budget_s():
+            break
+    per_call = statistics.mean(times)
+    value = 1.0 / per_call
+    line = {"impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": "calls/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_call * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) logits with planted spikes)",
+            "config": {"workload": cfg.name, "batch": B, "k_range": [int(vi.num_drafts.min()), int(vi.num_drafts.max())],
+                       "vocab": cfg.vocab, "verify_rows": int(vi.row_offsets[-1]), "context": int(lens[0]),
+                       "l2": "L2 flushed between calls (256 MB write, outside the timed events); "
+                             "%.1f MB of logits per call" % (ver_bytes / 1e6)},
+            "cpu_baseline": {"value": value, "unit": "calls/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": "%d full call(s): float64 numpy verify + commit of the same inputs%s" %
+                                       (len(times), "; capped by the time budget" if len(times) < args.steps else "")},
+            "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "samples_run": len(times)}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_loop(args, cfg, world):
+    """Reference arm of the speculative loop: the oracle's loop (chain,
+    confidence stop or tree drafting, as selected) on the same copy-head
+    weights and synthetic verifier, one loop iteration per step."""
+    import oracle as O
+    import oracle.loop as OL
+    import oracle.tree as OT
+    B, K = cfg.batch, cfg.K
+    lens = synth.context_lengths(cfg)
+    w = synth.copy_head(cfg, synth.make_weights(cfg, norm="ones"))
+    thr = int(args.loop_alpha * 2 ** 53)
+    tree_shape = tuple(int(x) for x in args.tree.split(",")) if args.tree else None
+    if tree_shape:
+        K = tree_shape[1]
+    W = oracle_head(cfg, w, args.weights)
+    total = args.steps + 2
+    kv = synth.make_kv(cfg, lens, extra_slots=(K + 1) * total + K + 1)
+    st = OL.LoopState([int(x) for x in synth.loop_start_hashes(cfg, B)],
+                      [int(x) for x in synth.uniform_int(cfg.seed, 95, (B,), 0, cfg.vocab)], [int(x) for x in lens],
+                      [[] for _ in range(B)])
+    dense = None if args.weights == "dense" else (lambda ids: O.widen(w["embed"][np.asarray(ids)], cfg.dtype))
+    conf = args.conf_threshold if args.conf_threshold > 0 else None
+
+    def one():
+        n0 = sum(len(o) for o in st.out)
+        t = time.perf_counter()
+        if tree_shape:
+            OT.tree_spec_loop(W, kv, st, tree_shape[0], tree_shape[1], tree_shape[2], thr, 1, cfg.dtype,
+                              embed_rows=dense)
+        else:
+            OL.spec_loop(W, kv, st, K, thr, 1, cfg.dtype, embed_rows=dense, conf_tau=conf)
+        return time.perf_counter() - t, sum(len(o) for o in st.out) - n0
+
+    t_start = time.perf_counter()
+    for _ in range(min(args.warmup, 1)):
+        one()
+    dts, toks = [], 0
+    for _ in range(args.steps):
+        dt, n = one()
+        dts.append(dt)
+        toks += n
+        if time.perf_counter() - t_start > reference_budget_s():
+            break
+    value = toks / sum(dts)
+    line = {"impl": "reference", "metric": LOOP_METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(dts) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (copy-head weights, deterministic synthetic verifier)",
+            "config": {"workload": "spec_loop_" + cfg.name, "batch": B, "draft_steps_K": K,
+                       "sticky_alpha": args.loop_alpha, "weights": args.weights,
+                       "conf_threshold": args.conf_threshold,
+                       "tree": ({"branching_factor": tree_shape[0], "tree_depth": tree_shape[1],
+                                 "num_assistant_tokens": tree_shape[2]} if tree_shape else None),
+                       "mean_emitted_per_step": toks / (B * len(dts)),
+                       "l2": "inputs larger than L2 (weights streamed every draft step)"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": "%d loop iteration(s) of the float64 numpy oracle%s" %
+                                       (len(dts), "; capped by the time budget" if len(dts) < args.steps else "")},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "samples_run": len(dts)}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, world):
     """The oracle timed as the reference arm.  A step is sampled as one of
     the K draft steps (the decoder layer, LM head and argmax for the whole
     batch) plus one K-th of the verify rows; the full step is K such samples.
-    The number of samples is capped so the run stays within a few minutes."""
+    The number of samples is capped so the run stays within a few minutes.
+    The verify workload and the speculative loop have arms of their own."""
     if rank != 0:
         return
     import oracle as O
     cfg = WORKLOADS[args.workload]
+    if cfg.H == 0:
+        return run_reference_verify(args, cfg, world)
+    if args.loop:
+        return run_reference_loop(args, cfg, world)
     w = synth.make_weights(cfg, norm="ones")
     lens = synth.context_lengths(cfg)
     kv = synth.make_kv(cfg, lens, extra_slots=cfg.K + 1)
@@ -883,7 +999,7 @@ def run_reference(args, rank, world):
         O.kv_rollback(kv, cfg.dtype)
         O.verify(vi.logits, vi.row_offsets, np.repeat(res.ids, cfg.K, axis=1), vi.num_drafts, cfg.dtype)
 
-    budget = float(os.environ.get("MTP_REFERENCE_BUDGET_S", "150"))
+    budget = reference_budget_s()
     t_start = time.perf_counter()
     for _ in range(min(args.warmup, 1)):
         sample()

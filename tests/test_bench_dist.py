@@ -60,3 +60,32 @@ def test_step_bytes_of_the_bench_workload():
          + 5 * 4096) * 2
     assert sb["weights"] == w
     assert abs(sb["draft"] / 5 / 1e6 - 1715.09) < 0.5
+
+
+def _reference_line(argv, capsys):
+    import json
+    import bench
+    bench.main(argv)
+    out = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(out) == 1
+    return json.loads(out[0])
+
+
+def test_reference_arm_follows_the_workload(capsys, monkeypatch):
+    """The reference arm reports the metric, unit and config of the arm it
+    stands beside: draft steps/s, loop tok/s (chain and tree)."""
+    import bench
+    monkeypatch.setenv("MTP_REFERENCE_BUDGET_S", "2")
+    d = _reference_line(["--impl", "reference", "--workload", "tiny_f32_h256", "--steps", "1", "--warmup", "3"],
+                        capsys)
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "steps/s"
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    d = _reference_line(["--impl", "reference", "--workload", "tiny_f32_h256", "--loop", "--steps", "2",
+                         "--warmup", "3"], capsys)
+    assert d["metric"] == bench.LOOP_METRIC and d["unit"] == "tok/s"
+    assert d["config"]["workload"] == "spec_loop_tiny_f32_h256" and d["config"]["tree"] is None
+    assert d["value"] > 0 and d["config"]["mean_emitted_per_step"] >= 1.0
+    d = _reference_line(["--impl", "reference", "--workload", "tiny_f32_h256", "--loop", "--tree", "2,3,4",
+                         "--steps", "1", "--warmup", "3"], capsys)
+    assert d["config"]["tree"] == {"branching_factor": 2, "tree_depth": 3, "num_assistant_tokens": 4}
+    assert d["value"] > 0
