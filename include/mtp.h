@@ -412,6 +412,18 @@ mtp_status mtp_tree_commit(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const m
 mtp_status mtp_tree_loop(mtp_ctx* ctx, void* stream, const mtp_kv* kv, const mtp_loop* loop, const mtp_tree* tree,
                          int iters);
 
+/* Failure-detection diagnostic.  Runs one of the library's bounded waits on
+ * a condition that never becomes true, so that the wait runs out as it would
+ * for a lost arrival in a real launch: which = 0, the shared-memory barrier
+ * phase wait of the streamed kernels (a barrier nobody arrives at, 4096
+ * polls); which = 1, the persistent kernel's grid-barrier counter wait (a
+ * private counter nobody increments, 2 s of the GPU's global timer).  The
+ * kernel records MTP_ERR_TIMEOUT in the context's error word and returns; it
+ * touches nothing else, so the context stays usable.  Returns MTP_ERR_INVALID
+ * for a null context or another `which`; asynchronous on `stream` otherwise.
+ * mtp_get_device_error then reads (and clears) MTP_ERR_TIMEOUT. */
+mtp_status mtp_selftest_wait_timeout(mtp_ctx* ctx, void* stream, int which);
+
 /* Synchronise the context's device, return the device error word as an
  * mtp_status (MTP_OK if none) and clear it. */
 mtp_status mtp_get_device_error(mtp_ctx* ctx);

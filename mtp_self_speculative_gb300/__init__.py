@@ -360,6 +360,10 @@ def mtp_kv_truncate(ctx: Context, kv: KVCache, new_len: torch.Tensor, stream=Non
                                 _ptr(new_len, torch.int32, "new_len")), "mtp_kv_truncate")
 
 
+def mtp_selftest_wait_timeout(ctx: Context, which: int, stream=None) -> None:
+    _check(_clib.mtp_selftest_wait_timeout(ctx.handle, _stream(stream), int(which)), "mtp_selftest_wait_timeout")
+
+
 def mtp_get_device_error(ctx: Context) -> int:
     return int(_clib.mtp_get_device_error(ctx.handle))
 

@@ -89,6 +89,7 @@ SIGNATURES = {
     "mtp_tree_commit": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPTree), P_i32]),
     "mtp_tree_loop": (c_int, [c_void_p, c_void_p, ctypes.POINTER(MTPKV), ctypes.POINTER(MTPLoop),
                               ctypes.POINTER(MTPTree), c_int]),
+    "mtp_selftest_wait_timeout": (c_int, [c_void_p, c_void_p, c_int]),
     "mtp_get_device_error": (c_int, [c_void_p]),
     "mtp_destroy": (None, [c_void_p]),
     "mtp_status_str": (ctypes.c_char_p, [c_int]),

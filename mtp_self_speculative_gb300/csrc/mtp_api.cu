@@ -380,6 +380,12 @@ mtp_status mtp_kv_truncate(mtp_ctx* ctx, void* stream, int B, const mtp_kv* kv, 
   return kv_edit(ctx, stream, B, kv, KV_TRUNCATE, new_len, 0);
 }
 
+mtp_status mtp_selftest_wait_timeout(mtp_ctx* ctx, void* stream, int which) {
+  if (!ctx || (which != 0 && which != 1)) return MTP_ERR_INVALID;
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
+  return after_launch(launch_selftest_wait(ctx, (cudaStream_t)stream, which));
+}
+
 mtp_status mtp_get_device_error(mtp_ctx* ctx) {
   if (!ctx) return MTP_ERR_INVALID;
   if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;

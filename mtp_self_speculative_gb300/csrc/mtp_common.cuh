@@ -311,6 +311,7 @@ cudaError_t draft_one_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, co
                            float* logits, float* hidden_out);
 bool tc_supported(const mtp_ctx* ctx, int B);
 bool persistent_supported(const mtp_ctx* ctx, int B);
+cudaError_t launch_selftest_wait(mtp_ctx* ctx, cudaStream_t s, int which);
 cudaError_t launch_draft_persistent(mtp_ctx* ctx, cudaStream_t s, int B, int K, const void* hidden,
                                     const void* embeds, const int32_t* positions, const mtp_kv* kv,
                                     const int32_t* chain_ids, int32_t* draft_ids, float* logits,

@@ -1105,4 +1105,47 @@ cudaError_t launch_draft_persistent(mtp_ctx* ctx, cudaStream_t s, int B, int K, 
   return e;
 }
 
+// ------------------------------------------------------------ diagnostics
+//
+// Runs one of the library's bounded waits on a condition that never becomes
+// true, so that it runs out the way a lost arrival or a missing CTA would make
+// it run out in a real launch: which = 0, the mbarrier phase wait of the
+// streamed kernels (an mbarrier nobody arrives at, kSelftestPolls polls);
+// which = 1, the persistent kernel's grid-barrier counter wait (a private
+// counter nobody increments; 2 s of %globaltimer).  No copy is ever in flight,
+// so the CTA may exit as soon as the wait gives up.
+constexpr uint32_t kSelftestPolls = 1u << 12;
+static __device__ unsigned long long g_selftest_counter[64];
+
+__global__ void selftest_wait_kernel(int which, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    s_abort = 0;
+  }
+  fence_mbar_init();
+  __syncthreads();
+  if (which == 0) {
+    const bool ok = mbar_wait_bounded(&bar, 0u, kSelftestPolls);
+    if (!ok && threadIdx.x == 0) set_error(err, MTP_ERR_TIMEOUT);
+  } else if (threadIdx.x == 0) {
+    PArgs a;
+    memset(&a, 0, sizeof(a));
+    a.gbar = g_selftest_counter;
+    a.err = err;
+    p_wait_count(a, 1ull, &s_abort);
+  }
+}
+
+cudaError_t launch_selftest_wait(mtp_ctx* ctx, cudaStream_t s, int which) {
+  void* counter = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&counter, g_selftest_counter);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(counter, 0, sizeof(g_selftest_counter), s)) != cudaSuccess) return e;
+  selftest_wait_kernel<<<1, 64, 0, s>>>(which, ctx->err);
+  ctx->launches++;
+  return cudaGetLastError();
+}
+
 }  // namespace mtp

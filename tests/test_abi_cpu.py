@@ -80,6 +80,7 @@ def test_calls_without_context_are_rejected(lib):
     assert lib.mtp_kv_rollback(None, None, 1, ctypes.byref(kv)) == _lib.MTP_ERR_INVALID
     assert lib.mtp_kv_truncate(None, None, 1, ctypes.byref(kv), 1) == _lib.MTP_ERR_INVALID
     assert lib.mtp_get_device_error(None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_selftest_wait_timeout(None, None, 0) == _lib.MTP_ERR_INVALID
     assert lib.mtp_profile_begin(None, 0, 1) == _lib.MTP_ERR_INVALID
     assert lib.mtp_launch_count(None) == 0
     lib.mtp_destroy(None)

@@ -287,3 +287,24 @@ def test_qwen3_32b_b128_sampled():
     case = Case(synth.QWEN3_32B_B128)
     subset = sorted(set(synth.uniform_int(case.cfg.seed, 88, (8,), 0, 128).tolist()))
     check_forced(case, subset, LOGIT_TOL, inplace=True)
+
+
+@pytest.mark.parametrize("which", [0, 1])
+def test_bounded_wait_runs_out_and_reports_timeout(which):
+    """A bounded wait whose condition never comes true (a shared-memory
+    barrier nobody arrives at; a grid-barrier counter nobody increments)
+    gives up, reports MTP_ERR_TIMEOUT through the error word, and leaves the
+    context usable: the error reads once, then the head drafts correctly."""
+    import time
+    import mtp_self_speculative_gb300 as M
+    case = Case(synth.TINY_F32)
+    t = time.perf_counter()
+    M.mtp_selftest_wait_timeout(case.ctx, which)
+    assert M.mtp_get_device_error(case.ctx) == M.MTP_ERR_TIMEOUT
+    elapsed = time.perf_counter() - t
+    assert elapsed < 30.0
+    if which == 1:
+        assert elapsed >= 1.9          # the counter wait is bounded by 2 s of the GPU timer
+    assert M.mtp_get_device_error(case.ctx) == 0
+    check_forced(case, [0], F32_LOGIT_TOL)
+
