@@ -15,9 +15,12 @@
 // ("MTP (Multi-Token Prediction)", "Architecture": dual norm, concat,
 // projection, one standard decoder layer, shared LM head.)
 //
-// Layout of the work: the grid is two CTAs per SM; CTA i owns a contiguous,
-// balanced range of row pairs; its 8 warps take pairs round-robin.  A warp
-// streams both rows of a pair with 16-byte non-allocating loads, U vectors
+// Layout of the work (register-streaming variant below; the bulk-copy
+// variant further down is the default for batches of at most 4): the grid
+// is two CTAs per SM; CTA i owns a contiguous, balanced range of units (row
+// pairs, single rows for eh_proj and down); its 8 warps take units
+// round-robin.  A warp streams the rows of a unit with 16-byte
+// non-allocating loads, U vectors
 // per lane in flight per row, against the normalised input vector(s) staged
 // once per CTA in shared memory as fp32.  Before waiting on the previous
 // kernel (programmatic dependent launch) each warp prefetches the head of
@@ -226,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
 // unit, two for rotary or gate/up pairs), completing
 // on per-stage mbarriers; it starts before the dependency wait, so the ring
 // (about 200 KB per SM) fills while the previous kernel drains.  Warps 1..8
-// stage the normalised input, then consume pairs round-robin from shared
+// stage the normalised input, then consume units round-robin from shared
 // memory and release each stage as soon as its values are in registers.
-// The stage count is a multiple of the number of consuming warps, and pair
+// The stage count is a multiple of the number of consuming warps, and unit
 // it goes to stage it % stages and warp it % consumers (see below).
 
 template <typename T, int KIND, int NB>
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs
   const int cw = warp - 1;
   // Full-barrier waits are by phase parity, so a warp may wait on a stage
   // only after the stage's previous fill has landed.  `stages` is a multiple
-  // of the number of consuming warps A: pair it uses stage it % stages and
+  // of the number of consuming warps A: unit it uses stage it % stages and
   // warp it % A, so consecutive uses of a stage belong to the same warp,
   // which consumed (hence saw land) the previous fill itself.
   const int active = consumers;
