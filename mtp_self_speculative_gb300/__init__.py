@@ -136,10 +136,36 @@ def mtp_draft(ctx: Context, hidden: torch.Tensor, embeds: torch.Tensor, position
            "mtp_draft")
 
 
+def _check_verify_shapes(target_logits: torch.Tensor, row_offsets: torch.Tensor, drafts: torch.Tensor,
+                         num_drafts: torch.Tensor, accepted: torch.Tensor, bonus: torch.Tensor, vocab: int,
+                         where: str) -> int:
+    """Shape checks the C entry points cannot make (they receive plain
+    pointers): the kernel reads num_rows x vocab logits and B + 1 offsets and
+    writes B results, so a mismatch here would read or write past a buffer.
+    Returns B."""
+    if target_logits.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("%s: target_logits must be float32 or bfloat16, got %s" % (where, target_logits.dtype))
+    if target_logits.dim() != 2 or int(target_logits.shape[1]) != int(vocab) or int(target_logits.shape[0]) < 1:
+        raise ValueError("%s: target_logits must be [num_rows >= 1, vocab=%d], got %s"
+                         % (where, vocab, tuple(target_logits.shape)))
+    if num_drafts.dim() != 1:
+        raise ValueError("%s: num_drafts must be 1-D [B]" % where)
+    B = int(num_drafts.shape[0])
+    if row_offsets.dim() != 1 or int(row_offsets.shape[0]) != B + 1:
+        raise ValueError("%s: row_offsets must be [B + 1] = [%d], got %s" % (where, B + 1, tuple(row_offsets.shape)))
+    if drafts.dim() != 2 or int(drafts.shape[0]) != B:
+        raise ValueError("%s: drafts must be [B=%d, stride], got %s" % (where, B, tuple(drafts.shape)))
+    for t, name in ((accepted, "accepted"), (bonus, "bonus")):
+        if t.numel() != B:
+            raise ValueError("%s: %s must hold B=%d entries, got %d" % (where, name, B, t.numel()))
+    return B
+
+
 def mtp_verify(ctx: Context, target_logits: torch.Tensor, row_offsets: torch.Tensor, drafts: torch.Tensor,
                num_drafts: torch.Tensor, accepted: torch.Tensor, bonus: torch.Tensor, stream=None) -> None:
     dt = torch_dtype(ctx.cfg.dtype)
-    B = int(num_drafts.shape[0])
+    B = _check_verify_shapes(target_logits, row_offsets, drafts, num_drafts, accepted, bonus, ctx.cfg.vocab,
+                             "mtp_verify")
     _check(_clib.mtp_verify(ctx.handle, _stream(stream), B, _ptr(target_logits, dt, "target_logits"),
                            int(target_logits.shape[0]), _ptr(row_offsets, torch.int32, "row_offsets"), _ptr(drafts, torch.int32, "drafts"),
                            int(drafts.shape[1]), _ptr(num_drafts, torch.int32, "num_drafts"),
@@ -152,9 +178,12 @@ def mtp_verify_noalloc(target_logits: torch.Tensor, row_offsets: torch.Tensor, d
     """mtp_verify without a context and without any device allocation (for
     callers whose device memory is owned by a fixed plan or another pool, or
     who cannot take cudaMalloc's device-wide synchronisation); the shape is
-    passed directly and the scratch is the library's fixed device array."""
+    passed directly and the scratch is the library's fixed device array.
+    target_logits must be float32 or bfloat16 [num_rows, vocab]; the shape
+    checks run before anything reaches the library."""
+    B = _check_verify_shapes(target_logits, row_offsets, drafts, num_drafts, accepted, bonus, vocab,
+                             "mtp_verify_noalloc")
     code = MTP_DTYPE_BF16 if target_logits.dtype == torch.bfloat16 else MTP_DTYPE_F32
-    B = int(num_drafts.shape[0])
     _check(_clib.mtp_verify_noalloc(_stream(stream), B, int(vocab), code, int(max_k),
                                     _ptr(target_logits, name="target_logits"), int(target_logits.shape[0]),
                                     _ptr(row_offsets, torch.int32, "row_offsets"), _ptr(drafts, torch.int32, "drafts"),

@@ -101,7 +101,7 @@ __device__ void stage_inputs(const StepArgs<T>& a, float* xs, int C, int b0, int
 }
 
 template <typename T, int KIND, int NB>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) {
+__global__ void __launch_bounds__(kThreads, 2) mtp_regs_proj_kernel(const StepArgs<T> a) {
   extern __shared__ __align__(16) float xs[];
   __shared__ float red[kWarps];
   __shared__ unsigned long long cta_best[kWarps][NB];
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
 
 // ------------------------------------------------- TMA-streamed variant
 //
-// Same work split and epilogues as gemv_kernel, for batches of at most 4:
+// Same work split and epilogues as mtp_regs_proj_kernel, for batches of at most 4:
 // one CTA per SM; warp 0 is a producer that streams this CTA's units (row
 // pairs, or single rows for eh_proj and down) into a ring of shared-memory
 // stages with one-dimensional bulk (TMA) copies (one copy per contiguous
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const StepArgs<T> a) 
 // it goes to stage it % stages and warp it % consumers (see below).
 
 template <typename T, int KIND, int NB>
-__global__ void __launch_bounds__(kTmaThreads, 1) gemv_tma_kernel(const StepArgs<T> a, int stages, int consumers) {
+__global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const StepArgs<T> a, int stages, int consumers) {
   extern __shared__ __align__(128) unsigned char gsm[];
   __shared__ __align__(8) uint64_t full_bar[kMaxTmaStages], empty_bar[kMaxTmaStages];
   __shared__ float red[kTmaConsumers * 8];
@@ -438,15 +438,15 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
       const size_t smem_t = stages * stage_stride + xs_bytes;
       const int gridt = min(ctx->num_sms, P);
       if (nbt == 1) {
-        auto kern = gemv_tma_kernel<T, KIND, 1>;
+        auto kern = mtp_stream_proj_kernel<T, KIND, 1>;
         ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       } else if (nbt == 2) {
-        auto kern = gemv_tma_kernel<T, KIND, 2>;
+        auto kern = mtp_stream_proj_kernel<T, KIND, 2>;
         ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       } else {
-        auto kern = gemv_tma_kernel<T, KIND, 4>;
+        auto kern = mtp_stream_proj_kernel<T, KIND, 4>;
         ensure_smem((const void*)kern, smem_t);
         e = launch_pdl(kern, dim3(gridt), dim3(kTmaThreads), smem_t, s, a, stages, consumers);
       }
@@ -456,15 +456,15 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
     }
   }
   if (nb == 4) {
-    auto kern = gemv_kernel<T, KIND, 4>;
+    auto kern = mtp_regs_proj_kernel<T, KIND, 4>;
     ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   } else if (nb == 2) {
-    auto kern = gemv_kernel<T, KIND, 2>;
+    auto kern = mtp_regs_proj_kernel<T, KIND, 2>;
     ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   } else {
-    auto kern = gemv_kernel<T, KIND, 1>;
+    auto kern = mtp_regs_proj_kernel<T, KIND, 1>;
     ensure_smem((const void*)kern, smem);
     e = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, a);
   }

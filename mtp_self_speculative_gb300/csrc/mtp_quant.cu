@@ -548,7 +548,7 @@ __device__ void stage_q_inputs(const StepArgs<uint16_t>& a, unsigned char* xf, f
 // epilogue while the others go on.
 template <int KIND, int NB>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-    gemv_q4_mma_kernel(const StepArgs<uint16_t> a, int stages, int gpc) {
+    mtp_q4_proj_kernel(const StepArgs<uint16_t> a, int stages, int gpc) {
   extern __shared__ __align__(128) unsigned char gsm[];
   __shared__ __align__(8) uint64_t full_bar[kQStages], empty_bar[kQStages];
   __shared__ float red[kTmaConsumers * 8];
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 // running argmax.  The cross-CTA argmax is that of the dense kernel.
 template <int NB>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-    gemv_q8_mma_kernel(const StepArgs<uint16_t> a, int stages, int consumers, int gpc) {
+    mtp_q8_lm_kernel(const StepArgs<uint16_t> a, int stages, int consumers, int gpc) {
   extern __shared__ __align__(128) unsigned char gsm[];
   __shared__ __align__(8) uint64_t full_bar[kQStages], empty_bar[kQStages];
   __shared__ float red[kTmaConsumers * 8];
@@ -965,8 +965,8 @@ static cudaError_t launch_q4_nb(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uin
   int stages = (int)((kQSmemBudget - fixed) / ((size_t)gpc * kQ4Tile));
   if (stages > kQStages) stages = kQStages;
   const size_t smem = (size_t)stages * gpc * kQ4Tile + fixed;
-  ensure_smem((const void*)gemv_q4_mma_kernel<KIND, NB>, smem);
-  return launch_pdl(gemv_q4_mma_kernel<KIND, NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, gpc);
+  ensure_smem((const void*)mtp_q4_proj_kernel<KIND, NB>, smem);
+  return launch_pdl(mtp_q4_proj_kernel<KIND, NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, gpc);
 }
 
 template <int KIND>
@@ -991,8 +991,8 @@ static cudaError_t launch_q8_nb(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uin
   int stages, consumers;
   if (!q_plan((size_t)gpc * kQ8Tile, fixed, 0, &stages, &consumers)) return cudaErrorInvalidConfiguration;
   const size_t smem = (size_t)stages * gpc * kQ8Tile + fixed;
-  ensure_smem((const void*)gemv_q8_mma_kernel<NB>, smem);
-  return launch_pdl(gemv_q8_mma_kernel<NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, consumers, gpc);
+  ensure_smem((const void*)mtp_q8_lm_kernel<NB>, smem);
+  return launch_pdl(mtp_q8_lm_kernel<NB>, dim3(grid), dim3(kTmaThreads), smem, s, a, stages, consumers, gpc);
 }
 
 static cudaError_t launch_q8_lm(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uint16_t>& a) {

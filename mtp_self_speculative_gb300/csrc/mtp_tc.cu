@@ -428,7 +428,7 @@ __device__ __forceinline__ SegList seg_list(const TcArgs& a) {
   return L;
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[8], empty_bar[8], accf_bar[2], acce_bar[2];
   __shared__ uint32_t tmem_base;
@@ -908,7 +908,7 @@ static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
   if (cl_stages > 8) cl_stages = 8;
   const size_t cl_smem = 1024 + (size_t)cl_stages * stage_bytes;
   size_t smem = 1024 + (size_t)stages * stage_bytes;
-  if (ensure_smem((const void*)tc_gemm_kernel, cl_smem > smem ? cl_smem : smem) != cudaSuccess) return nullptr;
+  if (ensure_smem((const void*)mtp_tc_proj_kernel, cl_smem > smem ? cl_smem : smem) != cudaSuccess) return nullptr;
   int S = 1;
   if (kind != TC_LM && n_tiles < slots && (size_t)cl_stages * stage_bytes >= (size_t)NT * 128 * 4) {
     // the LM head keeps whole tiles (argmax epilogue).  Largest cluster size
@@ -930,7 +930,7 @@ static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
       q.attrs = qa;
       q.numAttrs = 1;
       int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)tc_gemm_kernel, &q) != cudaSuccess) {
+      if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)mtp_tc_proj_kernel, &q) != cudaSuccess) {
         cudaGetLastError();
         continue;
       }
@@ -1003,7 +1003,7 @@ static cudaError_t tc_launch(mtp_ctx* ctx, cudaStream_t s, int kind, int B, int 
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = (pl->S > 1) ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&lc, tc_gemm_kernel, pl->maps, a);
+  cudaError_t e = cudaLaunchKernelEx(&lc, mtp_tc_proj_kernel, pl->maps, a);
   prof_after(ctx, kid, s);
   ctx->launches++;
   return e;

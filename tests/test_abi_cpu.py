@@ -91,3 +91,39 @@ def test_stream_copy_rejects_unaligned_or_overlapping(lib):
     assert lib.mtp_stream_copy(None, 16, 4096, 15) == _lib.MTP_ERR_INVALID
     assert lib.mtp_stream_copy(None, 17, 4096, 16) == _lib.MTP_ERR_INVALID
     assert lib.mtp_stream_copy(None, 4096, 4096 + 16, 64) == _lib.MTP_ERR_INVALID
+
+
+def test_verify_wrappers_check_shapes_before_any_call():
+    """The C entry points receive plain pointers, so the binding checks what
+    they cannot: logits dtype (float32 or bfloat16), a 2-D [rows, vocab]
+    logits tensor, B + 1 row offsets, B draft rows, B outputs.  Every bad
+    case raises before anything reaches the library; the well-formed case
+    (CPU tensors here) stops at the device-pointer check."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    V, B = 100, 3
+    i32 = dict(dtype=torch.int32)
+    good = dict(target_logits=torch.zeros((8, V), dtype=torch.bfloat16), row_offsets=torch.zeros(B + 1, **i32),
+                drafts=torch.zeros((B, 4), **i32), num_drafts=torch.zeros(B, **i32),
+                accepted=torch.zeros(B, **i32), bonus=torch.zeros(B, **i32))
+    bad = [("target_logits", torch.zeros((8, V), dtype=torch.float16), "float32 or bfloat16"),
+           ("target_logits", torch.zeros((2, 4, V), dtype=torch.bfloat16), "vocab"),
+           ("target_logits", torch.zeros((8, V + 1), dtype=torch.bfloat16), "vocab"),
+           ("row_offsets", torch.zeros(B, **i32), "row_offsets"),
+           ("drafts", torch.zeros((B + 1, 4), **i32), "drafts"),
+           ("drafts", torch.zeros(B * 4, **i32), "drafts"),
+           ("accepted", torch.zeros(B - 1, **i32), "accepted"),
+           ("bonus", torch.zeros(B + 1, **i32), "bonus")]
+    ctx = M.Context(0, M.make_config(256, 4, 2, 64, 1024, V, dtype="bf16", max_batch=B, max_k=4), None)
+    calls = [lambda kw: M.mtp_verify_noalloc(vocab=V, max_k=4, **kw), lambda kw: M.mtp_verify(ctx, **kw)]
+    for call in calls:
+        for name, t, msg in bad:
+            with pytest.raises(ValueError, match=msg):
+                call(dict(good, **{name: t}))
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call(dict(good, stream=_NullStream()))
+
+
+class _NullStream:
+    """Stands in for a torch stream on a machine without a GPU (handle 0)."""
+    cuda_stream = 0

@@ -12,8 +12,9 @@ import torch
 
 import oracle as O
 import synth
-from gpu_util import (F32_LOGIT_TOL, LOGIT_TOL, check_ids, check_logits, dev, download_kv, host, kv_slots,
-                      make_context, oracle_weights, upload_kv, upload_weights)
+from gpu_util import (F32_LOGIT_TOL, LOGIT_TOL, Guarded, check_ids, check_ids_are_argmax_of_own_logits,
+                      check_logits, dev, download_kv, exact_floor, host, kv_slots, make_context, oracle_weights,
+                      upload_kv, upload_weights)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,14 +42,18 @@ class Case:
         import mtp_self_speculative_gb300 as M
         cfg, B, K = self.cfg, self.B, self.K
         kvd = upload_kv(self.kv0) if kvd is None else kvd
-        ids = torch.full((B, K), -7, dtype=torch.int32, device="cuda")
-        logits = torch.empty((B, K, cfg.vocab), dtype=torch.float32, device="cuda")
-        hout = torch.empty((B, cfg.H), dtype=torch.float32, device="cuda")
+        ids = Guarded((B, K), torch.int32, fill=-7)
+        logits = Guarded((B, K, cfg.vocab), torch.float32)
+        hout = Guarded((B, cfg.H), torch.float32)
         chain = dev(self.chain[:, :K - 1].copy()) if (forced and K > 1) else None
-        M.mtp_draft(self.ctx, *self.inputs, kvd, K, ids, logits, hout, chain_ids=chain)
+        M.mtp_draft(self.ctx, *self.inputs, kvd, K, ids.t, logits.t, hout.t, chain_ids=chain)
         torch.cuda.synchronize()
         assert M.mtp_get_device_error(self.ctx) == 0
-        return host(ids), host(logits), host(hout), kvd
+        for g, name in ((ids, "draft_ids"), (logits, "logits"), (hout, "hidden_out")):
+            g.check(name)
+        ids_h, logits_h = host(ids.t), host(logits.t)
+        check_ids_are_argmax_of_own_logits(ids_h, logits_h)
+        return ids_h, logits_h, host(hout.t), kvd
 
     def oracle(self, subset, forced=True, kv=None):
         """Oracle draft on ``subset``; appends into ``kv`` (default: a copy of
@@ -76,6 +81,8 @@ def check_forced(case, subset, tol, inplace=False):
     res, view = case.oracle(subset, forced=True, kv=case.kv0 if inplace else None)
     worst = check_logits(logits[subset], res.logits, tol)
     exact = check_ids(ids[subset], res.logits)
+    n_steps = len(subset) * K
+    assert exact >= (n_steps if tol <= F32_LOGIT_TOL else exact_floor(n_steps)), (exact, n_steps)
     e_h = np.max(np.abs(hout[subset] - res.hidden_out), axis=-1) / np.max(np.abs(res.hidden_out), axis=-1)
     assert np.max(e_h) <= tol
     got = download_kv(kvd)

@@ -6,19 +6,21 @@ import torch
 
 import oracle as O
 import synth
-from gpu_util import dev, download_kv, host, make_context, upload_kv
+from gpu_util import Guarded, dev, download_kv, host, make_context, upload_kv
 
 pytestmark = pytest.mark.gpu
 
 
 def _verify_gpu(ctx, vi, B):
     import mtp_self_speculative_gb300 as M
-    acc = torch.empty(B, dtype=torch.int32, device="cuda")
-    bon = torch.empty(B, dtype=torch.int32, device="cuda")
-    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+    acc = Guarded((B,), torch.int32, fill=-9)
+    bon = Guarded((B,), torch.int32, fill=-9)
+    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc.t, bon.t)
     torch.cuda.synchronize()
     assert M.mtp_get_device_error(ctx) == 0
-    return host(acc), host(bon)
+    acc.check("accepted")
+    bon.check("bonus")
+    return host(acc.t), host(bon.t)
 
 
 def test_verify_rollback_b64_bit_exact():
@@ -119,15 +121,17 @@ def test_verify_adversarial_rows_all_accepted(dtype, V):
     cfg = synth.MTPShape("adv", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=V, batch=len(nd), K=8,
                          dtype=dtype, ctx_lo=1, ctx_hi=1, seed_index=41)
     ctx = make_context(cfg, None, max_batch=len(nd), max_k=8)
-    acc = torch.empty(len(nd), dtype=torch.int32, device="cuda")
-    bon = torch.empty(len(nd), dtype=torch.int32, device="cuda")
-    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc, bon)
+    acc = Guarded((len(nd),), torch.int32, fill=-9)
+    bon = Guarded((len(nd),), torch.int32, fill=-9)
+    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc.t, bon.t)
     torch.cuda.synchronize()
     assert M.mtp_get_device_error(ctx) == 0
+    acc.check("accepted")
+    bon.check("bonus")
     acc_o, bon_o = O.verify(lg, ro, drafts, nd, dtype)
     np.testing.assert_array_equal(acc_o, nd)
-    np.testing.assert_array_equal(host(acc), acc_o)
-    np.testing.assert_array_equal(host(bon), bon_o)
+    np.testing.assert_array_equal(host(acc.t), acc_o)
+    np.testing.assert_array_equal(host(bon.t), bon_o)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -148,12 +152,14 @@ def test_verify_nan_entries_are_passed_over(dtype):
     cfg = synth.MTPShape("nan", H=0, n_q=2, n_kv=2, head_dim=64, ffn=0, vocab=V, batch=2, K=1,
                          dtype=dtype, ctx_lo=1, ctx_hi=1, seed_index=42)
     ctx = make_context(cfg, None, max_batch=2, max_k=1)
-    acc = torch.empty(2, dtype=torch.int32, device="cuda")
-    bon = torch.empty(2, dtype=torch.int32, device="cuda")
-    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc, bon)
+    acc = Guarded((2,), torch.int32, fill=-9)
+    bon = Guarded((2,), torch.int32, fill=-9)
+    M.mtp_verify(ctx, dev(lg), dev(ro), dev(drafts), dev(nd), acc.t, bon.t)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(host(acc), [0, 1])
-    np.testing.assert_array_equal(host(bon), [-1, 2048])
+    acc.check("accepted")
+    bon.check("bonus")
+    np.testing.assert_array_equal(host(acc.t), [0, 1])
+    np.testing.assert_array_equal(host(bon.t), [-1, 2048])
     assert M.mtp_get_device_error(ctx) == 0
 
 
@@ -164,11 +170,13 @@ def test_verify_inconsistent_offsets_sets_error():
     ro = vi.row_offsets.copy()
     ro[2] += 1                          # request 1 claims one row too many
     ctx = make_context(cfg, None, max_batch=4, max_k=vi.max_k)
-    acc = torch.empty(4, dtype=torch.int32, device="cuda")
-    bon = torch.empty(4, dtype=torch.int32, device="cuda")
-    M.mtp_verify(ctx, dev(vi.logits), dev(ro), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+    acc = Guarded((4,), torch.int32, fill=-9)
+    bon = Guarded((4,), torch.int32, fill=-9)
+    M.mtp_verify(ctx, dev(vi.logits), dev(ro), dev(vi.drafts), dev(vi.num_drafts), acc.t, bon.t)
     assert M.mtp_get_device_error(ctx) == M.MTP_ERR_DEVICE_ARGS
-    assert host(acc)[1] == -1 and host(bon)[1] == -1
+    assert host(acc.t)[1] == -1 and host(bon.t)[1] == -1
+    acc.check("accepted")
+    bon.check("bonus")
     assert M.mtp_get_device_error(ctx) == 0     # cleared
 
 
@@ -187,12 +195,14 @@ def test_commit_after_verify_b64_bit_exact():
     kv0 = _drafted_kv(cfg, vi.num_drafts)
     kvd = upload_kv(kv0)
     ctx = make_context(cfg, None, max_batch=cfg.batch, max_k=vi.max_k)
-    acc = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
-    bon = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
-    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
-    M.mtp_kv_commit_accepted(ctx, kvd, acc, extra=1)
+    acc = Guarded((cfg.batch,), torch.int32, fill=-9)
+    bon = Guarded((cfg.batch,), torch.int32, fill=-9)
+    M.mtp_verify(ctx, dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc.t, bon.t)
+    M.mtp_kv_commit_accepted(ctx, kvd, acc.t, extra=1)
     torch.cuda.synchronize()
     assert M.mtp_get_device_error(ctx) == 0
+    acc.check("accepted")
+    bon.check("bonus")
     got = download_kv(kvd)
     acc_o, _ = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "bf16")
     kv_o = kv0.copy()

@@ -29,16 +29,19 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
 def _both(cfg, vi, ctx, M, torch, dev, host):
     B = len(vi.num_drafts)
     outs = []
+    from gpu_util import Guarded
     for fn in ("ctx", "noalloc"):
-        acc = torch.full((B,), -9, dtype=torch.int32, device="cuda")
-        bon = torch.full((B,), -9, dtype=torch.int32, device="cuda")
-        args = (dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc, bon)
+        acc = Guarded((B,), torch.int32, fill=-9)
+        bon = Guarded((B,), torch.int32, fill=-9)
+        args = (dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts), acc.t, bon.t)
         if fn == "ctx":
             M.mtp_verify(ctx, *args)
         else:
             M.mtp_verify_noalloc(*args, vocab=cfg.vocab, max_k=vi.max_k)
         torch.cuda.synchronize()
-        outs.append((host(acc), host(bon)))
+        acc.check("accepted")
+        bon.check("bonus")
+        outs.append((host(acc.t), host(bon.t)))
     return outs
 
 
@@ -67,3 +70,36 @@ def test_noalloc_verify_matches_context_verify_twice():
         (a_ctx, b_ctx), (a_na, b_na) = _both(cfg2, vi2, ctx2, M, torch, dev, host)
         np.testing.assert_array_equal(a_na, a_ctx)
         np.testing.assert_array_equal(b_na, b_ctx)
+
+
+@pytest.mark.gpu
+def test_noalloc_malformed_rows_give_minus_one_for_those_requests_only():
+    """Request 1 claims one row too many, so request 2 is left one short:
+    both get accepted = bonus = -1 (the documented device-side result, there
+    being no error word without a context); requests 0 and 3 still get the
+    oracle's results.  A second, well-formed call right after it is exact
+    again."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    import oracle as O
+    from gpu_util import Guarded, dev, host
+
+    cfg = synth.shrink(synth.VERIFY_B64, vocab=3001, batch=4)
+    vi = synth.make_verify_inputs(cfg)
+    ro = vi.row_offsets.copy()
+    ro[2] += 1
+    acc_o, bon_o = O.verify(vi.logits, vi.row_offsets, vi.drafts, vi.num_drafts, "bf16")
+    for offsets, bad in ((ro, {1, 2}), (vi.row_offsets, set())):
+        acc = Guarded((4,), torch.int32, fill=-9)
+        bon = Guarded((4,), torch.int32, fill=-9)
+        M.mtp_verify_noalloc(dev(vi.logits), dev(offsets), dev(vi.drafts), dev(vi.num_drafts), acc.t, bon.t,
+                             vocab=cfg.vocab, max_k=vi.max_k)
+        torch.cuda.synchronize()
+        acc.check("accepted")
+        bon.check("bonus")
+        a, b_ = host(acc.t), host(bon.t)
+        for r in range(4):
+            if r in bad:
+                assert (a[r], b_[r]) == (-1, -1), r
+            else:
+                assert (a[r], b_[r]) == (acc_o[r], bon_o[r]), r
