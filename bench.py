@@ -434,6 +434,19 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_e2e:
         e2e = run_e2e(wl, max(5, min(args.steps // 4, 200)))
 
+    # the first draft's ids and logits (the workload is deterministic: every
+    # draft from the starting state gives them), for the exact-id report
+    wl.draft()
+    M.mtp_kv_rollback(wl.ctx, wl.kv)
+    torch.cuda.synchronize()
+    first_ids, first_logits = wl.ids.cpu().numpy(), wl.logits.cpu().numpy()
+
+    # the other configurations, measured in the same process (N = 1 only)
+    others = None
+    if world == 1 and not args.no_workloads and args.workload == DEFAULT_WORKLOAD and args.weights == "dense" \
+            and args.persistent_max_batch == 0 and args.ctx is None:
+        others = measure_other_workloads(args, local_rank)
+
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -493,9 +506,137 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e:
         line["e2e"] = e2e
+    if others:
+        line["workloads"] = others
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, fmt=args.weights)
+        cb, parity = cpu_baseline(cfg, fmt=args.weights, gpu_ids=first_ids, gpu_logits=first_logits)
+        line["cpu_baseline"] = cb
+        line["draft_parity"] = parity
     print(json.dumps(line), flush=True)
+
+
+def timed_steps(fn, n: int, stream) -> float:
+    """Mean milliseconds of n calls of fn, CUDA events on the launching
+    stream, synchronised on both sides."""
+    import torch
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(n):
+        fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n
+
+
+def measure_draft_workload(cfg: synth.MTPShape, local_rank: int, steps: int, warmup: int, peak: float) -> dict:
+    """Full steps (draft K + verify + commit + truncate) and draft-only calls
+    of one draft configuration, with its per-kernel breakdown and the clocks
+    seen while its steps ran."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    wl = Workload(cfg, cfg.K)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    assert M.mtp_get_device_error(wl.ctx) == 0
+    sampler = ClockSampler(gpu_id_for_smi(local_rank))
+    sampler.start()
+    ms_step = timed_steps(wl.step, steps, stream)
+
+    def draft_only():
+        wl.draft()
+        M.mtp_kv_rollback(wl.ctx, wl.kv)
+    ms_draft = timed_steps(draft_only, steps, stream)
+    clocks = sampler.stop()
+    kernels = kernel_breakdown(wl, max(3, steps // 2))
+    assert M.mtp_get_device_error(wl.ctx) == 0
+    sb = step_bytes(cfg, wl.lens, cfg.K)
+    acc = wl.acc.cpu().numpy()
+    out = {
+        "batch": wl.B, "draft_steps_K": cfg.K, "hidden": cfg.H, "ffn": cfg.ffn, "q_heads": cfg.n_q,
+        "mtp_context": [int(wl.lens.min()), int(wl.lens.max())], "dtype": cfg.dtype,
+        "steps_s": 1e3 / ms_step, "ms_per_step": ms_step,
+        "accepted_tok_s": {"emitted": float(np.sum(acc + 1)) * 1e3 / ms_step,
+                           "accepted_drafts": float(np.sum(acc)) * 1e3 / ms_step},
+        "draft": {"ms_per_draft_step": ms_draft / cfg.K, "bytes_per_draft_step": sb["draft"] / cfg.K,
+                  "hbm_frac_of_measured": sb["draft"] / (ms_draft * 1e-3) / 1e9 / peak},
+        "step_hbm_frac_of_measured": sb["total"] / (ms_step * 1e-3) / 1e9 / peak,
+        "kernels": kernels, "clocks": clocks, "timed_steps": steps,
+    }
+    M.mtp_destroy(wl.ctx)
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_verify_workload(cfg: synth.MTPShape, local_rank: int, calls: int, peak: float) -> dict:
+    """mtp_verify + mtp_kv_commit_accepted on the 64-request verify inputs,
+    each call timed with CUDA events, L2 flushed between calls."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    vi = synth.make_verify_inputs(cfg)
+    lens = synth.context_lengths(cfg)
+    kv0 = synth.make_kv(cfg, lens, extra_slots=int(vi.num_drafts.max()) + 1, prefill_slots=lens + vi.num_drafts)
+    kv0.pending = vi.num_drafts.astype(np.int32).copy()
+    B = len(lens)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a).cuda()
+    ctx = M.mtp_init(M.make_config(1, cfg.n_q, cfg.n_kv, cfg.head_dim, 8, cfg.vocab, dtype=cfg.dtype, max_batch=B,
+                                   max_k=vi.max_k, block_size=cfg.block_size))
+    kv = M.KVCache(dev(kv0.k_pool), dev(kv0.v_pool), dev(kv0.block_table), dev(kv0.seq_len), dev(kv0.pending))
+    seq0, pend0 = dev(kv0.seq_len), dev(kv0.pending)
+    logits, ro, drafts, nd = dev(vi.logits), dev(vi.row_offsets), dev(vi.drafts), dev(vi.num_drafts)
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    bon = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(calls)]
+    for i in range(3 + calls):
+        e = ev[i - 3] if i >= 3 else None
+        if e:
+            e[0].record(stream)
+        M.mtp_verify(ctx, logits, ro, drafts, nd, acc, bon)
+        if e:
+            e[1].record(stream)
+        M.mtp_kv_commit_accepted(ctx, kv, acc, extra=1)
+        if e:
+            e[2].record(stream)
+        kv.seq_len.copy_(seq0)
+        kv.pending.copy_(pend0)
+        flush.fill_(1)
+        if i == 2:
+            torch.cuda.synchronize()
+            sampler = ClockSampler(gpu_id_for_smi(local_rank))
+            sampler.start()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert M.mtp_get_device_error(ctx) == 0
+    t_ver = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    t_com = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    ver_bytes = int(vi.row_offsets[-1]) * cfg.vocab * cfg.elem_bytes
+    gbs = ver_bytes / (t_ver * 1e-3) / 1e9
+    M.mtp_destroy(ctx)
+    return {"batch": B, "k_range": [int(vi.num_drafts.min()), int(vi.num_drafts.max())],
+            "verify_rows": int(vi.row_offsets[-1]), "calls_s": 1e3 / (t_ver + t_com), "verify_ms": t_ver,
+            "commit_ms": t_com, "verify_bytes": ver_bytes, "verify_gbs": gbs, "verify_hbm_frac_of_measured": gbs / peak,
+            "l2": "flushed between calls (256 MB write outside the events)", "timed_calls": calls, "clocks": clocks}
+
+
+def measure_other_workloads(args, local_rank: int) -> dict:
+    """The continuous-batching, large-batch and verify configurations, each
+    set up, measured at a few steps and freed in turn."""
+    peak = float(measured_peaks()[0]["hbm_gbs"])
+    out = {}
+    for cfg, steps in ((synth.QWEN3_8B_CB32, 20), (synth.QWEN3_32B_B128, 6)):
+        out[cfg.name] = measure_draft_workload(cfg, local_rank, steps, 3, peak)
+    out[synth.VERIFY_B64.name] = measure_verify_workload(synth.VERIFY_B64, local_rank, 50, peak)
+    return out
 
 
 def run_e2e(wl: Workload, n: int) -> dict:
@@ -839,9 +980,13 @@ def oracle_head(cfg: synth.MTPShape, w, fmt: str):
     return O.MTPWeights64.from_stored(w, cfg.dtype, cfg.n_q, cfg.n_kv, cfg.head_dim, cfg.eps, cfg.rope_theta)
 
 
-def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1, fmt: str = "dense") -> dict:
+def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1, fmt: str = "dense", gpu_ids=None, gpu_logits=None):
     """The float64 oracle as it stands, one full step (K draft steps, verify,
-    commit) for the same workload on the host cores."""
+    commit) for the same workload on the host cores.  With the GPU's first
+    draft (ids [B, K], logits [B, K, V]) of the same inputs, also returns the
+    draft parity of that call: exact-id matches step by step while the two
+    free-running chains agree, the near-ties among them, and the worst
+    normwise logit error."""
     import oracle as O
     w = synth.make_weights(cfg, norm="ones")
     lens = synth.context_lengths(cfg)
@@ -856,9 +1001,29 @@ def cpu_baseline(cfg: synth.MTPShape, sample_steps: int = 1, fmt: str = "dense")
         O.kv_commit(kv, np.minimum(acc + 1, cfg.K), cfg.dtype)
         O.kv_truncate(kv, lens, cfg.dtype)
     dt = (time.perf_counter() - t) / sample_steps
-    return {"value": 1.0 / dt, "unit": "steps/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": "%d full step(s): %d draft steps + verify + commit, B=%d, float64 numpy" %
-                      (sample_steps, cfg.K, len(lens))}
+    cb = {"value": 1.0 / dt, "unit": "steps/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
+          "sample": "%d full step(s): %d draft steps + verify + commit, B=%d, float64 numpy" %
+                    (sample_steps, cfg.K, len(lens))}
+    if gpu_ids is None:
+        return cb
+    z = res.logits
+    compared = exact = near = 0
+    worst = 0.0
+    for b in range(len(lens)):
+        for k in range(cfg.K):
+            zo = z[b, k]
+            scale = float(np.max(np.abs(zo)))
+            worst = max(worst, float(np.max(np.abs(gpu_logits[b, k].astype(np.float64) - zo))) / scale)
+            compared += 1
+            exact += int(gpu_ids[b, k] == res.ids[b, k])
+            near += int(O.top2_gap(zo[None])[0] < 2e-2 * scale)
+            if gpu_ids[b, k] != res.ids[b, k]:
+                break            # the chains now follow different tokens
+    parity = {"compared_steps": compared, "exact_ids": exact, "oracle_near_ties": near,
+              "max_logit_rel_err": worst, "tolerance": 2e-2,
+              "note": "GPU free-running draft vs the float64 oracle on the same inputs; steps compared "
+                      "until the first id difference"}
+    return cb, parity
 
 
 def reference_budget_s() -> float:
@@ -1051,6 +1216,8 @@ def main(argv=None):
     ap.add_argument("--tree", default=None,
                     help="with --loop: tree drafting 'branching_factor,tree_depth,num_assistant_tokens'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations measured after the headline workload")
     ap.add_argument("--ctx", type=int, default=None,
                     help="override the committed MTP context length (smaller cases for profiling)")
     ap.add_argument("--lm-traffic", type=float, default=None,
