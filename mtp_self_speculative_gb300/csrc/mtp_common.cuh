@@ -35,6 +35,7 @@ template <typename T> struct Elem;
 template <> struct Elem<float> {
   static constexpr int kPerVec = 4;  // elements per 16-byte vector
   __device__ static __forceinline__ float load1(const float* p) { return __ldg(p); }
+  __device__ static __forceinline__ float loads(const float* p) { return *p; }  // any state space
   __device__ static __forceinline__ void store1(float* p, float v) { *p = v; }
 };
 template <> struct Elem<uint16_t> {
@@ -42,6 +43,7 @@ template <> struct Elem<uint16_t> {
   __device__ static __forceinline__ float load1(const uint16_t* p) {
     return __uint_as_float(((uint32_t)__ldg(p)) << 16);
   }
+  __device__ static __forceinline__ float loads(const uint16_t* p) { return __uint_as_float(((uint32_t)*p) << 16); }
   __device__ static __forceinline__ void store1(uint16_t* p, float v) { *p = f32_to_bf16_rne(v); }
 };
 

@@ -24,7 +24,16 @@
 
 namespace mtp {
 
-constexpr int kVerifyThreads = 256;
+// One CTA per SM: warp 0 streams the CTA's chunks of the flat logit range
+// into a ring of shared-memory stages with one-dimensional bulk copies;
+// warps 1..8 each own every 8th chunk (and, the stage count being the warp
+// count, always the same stage) and reduce it from shared memory.
+constexpr int kVerifyConsumers = 8;
+constexpr int kVerifyThreads = 32 * (1 + kVerifyConsumers);
+constexpr int kVerifyStages = kVerifyConsumers;
+constexpr uint32_t kVerifyStageBytes = 24576;
+constexpr uint32_t kVerifyMinChunk = 2048;
+constexpr uint32_t kVerifyWaitLimit = 1u << 24;
 
 template <typename T>
 struct VerifyArgs {
@@ -35,37 +44,27 @@ struct VerifyArgs {
   const int32_t* num_drafts;
   int32_t* accepted;
   int32_t* bonus;
-  unsigned long long* keys;  // [num_rows]
-  int* cnt;                  // [1]
+  unsigned long long* keys;  // [num_rows], zero on entry, zero again on exit
+  int* cnt;                  // [1], zero on entry and on exit
   int* err;
   int V, max_k, B, num_rows;
+  uint32_t chunk;            // bytes per chunk (multiple of 16, <= kVerifyStageBytes)
 };
 
-// Batch helpers of the vector scan.  A thread loads kVerifyBatch 16-byte
-// vectors and takes their maximum with packed max instructions (about one
-// instruction per two bf16 logits); it keeps only its running maximum and
-// the vector where that maximum first appeared (the lowest vector of the
-// batch holding it, looked up only when the running maximum moves).  The
-// position inside the vector is found once per row segment: the lanes whose
-// maximum equals their warp's take the first element equal to it in the
-// vector they kept in registers.  Ids visited by a thread increase with
-// q and within a vector, and the running maximum moves only on a strictly
-// larger batch maximum, so that element is the thread's lowest id holding
-// its maximum.  Vectors past the end are filled with -inf
-// and never searched.  -0 equals +0 in every comparison; NaN logits are
-// passed over (the packed max returns the other operand, a batch whose
-// maximum is NaN is skipped, no search matches NaN), in the scalar head and
-// tail as well.
 template <typename T> struct VecOps;
 template <> struct VecOps<uint16_t> {
-  static constexpr uint32_t kFill = 0xFF80FF80u;  // -inf, -inf
   __device__ static __forceinline__ uint32_t max2(uint32_t x, uint32_t y) {
     uint32_t r;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
     return r;
   }
-  __device__ static __forceinline__ uint32_t vmax(const uint4& u) { return max2(max2(u.x, u.y), max2(u.z, u.w)); }
-  __device__ static __forceinline__ float finish(uint32_t m) { return fmaxf(bf16_lo(m), bf16_hi(m)); }
+  // maximum of the eight values (NaN entries are passed over by max.bf16x2;
+  // NaN only if all eight are NaN)
+  __device__ static __forceinline__ float vmax(const uint4& u) {
+    const uint32_t m = max2(max2(u.x, u.y), max2(u.z, u.w));
+    return fmaxf(bf16_lo(m), bf16_hi(m));
+  }
+  // lowest position in the vector holding a value equal to m (-0 == +0)
   __device__ static __forceinline__ int find(const uint4& u, float m) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     int at = -1;
@@ -78,12 +77,9 @@ template <> struct VecOps<uint16_t> {
   }
 };
 template <> struct VecOps<float> {
-  static constexpr uint32_t kFill = 0xFF800000u;  // -inf
-  __device__ static __forceinline__ uint32_t max2(uint32_t x, uint32_t y) {
-    return __float_as_uint(fmaxf(__uint_as_float(x), __uint_as_float(y)));
+  __device__ static __forceinline__ float vmax(const uint4& u) {
+    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)), fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
   }
-  __device__ static __forceinline__ uint32_t vmax(const uint4& u) { return max2(max2(u.x, u.y), max2(u.z, u.w)); }
-  __device__ static __forceinline__ float finish(uint32_t m) { return __uint_as_float(m); }
   __device__ static __forceinline__ int find(const uint4& u, float m) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     int at = -1;
@@ -94,192 +90,175 @@ template <> struct VecOps<float> {
   }
 };
 
-constexpr int kVerifyBatch = 8;
-
-// One thread's view of a row segment row[c0, c1): the (value, id) key of its
-// scalar head and tail elements, and its running maximum over the vector
-// body with the batch where that maximum first appeared.
+// (value, lowest id) key of the row segment seg[0, len) held in shared
+// memory, whose first element is column col0 of its row.  Warp-collective;
+// every lane returns the warp's key (0 when every entry is NaN).  Scalar head
+// up to 16-byte alignment, 16-byte vector body, scalar tail.  Each lane keeps
+// its running maximum and the first vector where it appeared (lanes visit
+// their vectors in increasing order and move only on a strictly larger
+// value); after the body, the lanes holding the warp's maximum look up its
+// first position in that vector.
 template <typename T>
-struct ScanState {
-  const T* vbase;              // first 16-byte aligned element of the body
-  int c;                       // its column
-  int nvec;                    // vectors in the body
-  float bv;
-  int bat;                     // the vector where bv first appeared, -1 = none
-  uint4 bu;                    // that vector's contents
-  unsigned long long scalar;   // key of the head and tail elements
-};
-
-// Streams row[c0, c1): scalar head to 16-byte alignment, vector body with
-// kVerifyBatch loads in flight per thread, scalar tail.
-template <typename T>
-__device__ __forceinline__ ScanState<T> scan_body(const T* row, int c0, int c1) {
+__device__ __forceinline__ unsigned long long segment_key(const T* seg, int len, int col0, int lane) {
   using Ops = VecOps<T>;
   constexpr int VPE = Elem<T>::kPerVec;
-  constexpr int kStride = kVerifyThreads * kVerifyBatch;
-  ScanState<T> st;
-  st.scalar = 0ull;
-  int c = c0;
-  const int misalign = (int)(((uintptr_t)(row + c) & 15) / sizeof(T));
-  const int head_end = misalign ? min(c1, c + (VPE - misalign)) : c;
-  for (int i = c + threadIdx.x; i < head_end; i += kVerifyThreads) {
-    const float x = Elem<T>::load1(row + i);
-    if (x == x) st.scalar = umax64(st.scalar, argmax_key(x, (uint32_t)i));
+  unsigned long long key = 0ull;
+  const int mis = (int)((smem_addr(seg) & 15u) / sizeof(T));
+  const int head = mis ? min(len, VPE - mis) : 0;
+  if (lane < head) {
+    const float x = Elem<T>::loads(seg + lane);
+    if (x == x) key = argmax_key(x, (uint32_t)(col0 + lane));
   }
-  c = head_end;
-  st.c = c;
-  st.nvec = max(0, (c1 - c) / VPE);
-  st.vbase = row + c;
-  st.bv = -INFINITY;
-  st.bat = -1;
-  st.bu = make_uint4(Ops::kFill, Ops::kFill, Ops::kFill, Ops::kFill);
-  for (int v0 = threadIdx.x; v0 < st.nvec; v0 += kStride) {
-    uint4 u[kVerifyBatch];
-#pragma unroll
-    for (int q = 0; q < kVerifyBatch; ++q) {
-      const int v = v0 + q * kVerifyThreads;
-      u[q] = v < st.nvec ? ld_stream(st.vbase + (size_t)v * VPE)
-                         : make_uint4(Ops::kFill, Ops::kFill, Ops::kFill, Ops::kFill);
-    }
-    uint32_t vm[kVerifyBatch], m[kVerifyBatch];
-#pragma unroll
-    for (int q = 0; q < kVerifyBatch; ++q) m[q] = vm[q] = Ops::vmax(u[q]);
-#pragma unroll
-    for (int w = 1; w < kVerifyBatch; w *= 2)
-#pragma unroll
-      for (int q = 0; q + w < kVerifyBatch; q += 2 * w) m[q] = Ops::max2(m[q], m[q + w]);
-    const float mf = Ops::finish(m[0]);
-    if (mf > st.bv || (st.bat < 0 && mf == mf)) {
-      // the lowest vector of the batch holding mf (filled vectors come last)
-      int qi = 0;
-      uint4 bu = u[0];
-#pragma unroll
-      for (int q = kVerifyBatch - 1; q >= 0; --q)
-        if (Ops::finish(vm[q]) == mf) {
-          qi = q;
-          bu = u[q];
-        }
-      st.bv = mf;
-      st.bat = v0 + qi * kVerifyThreads;
-      st.bu = bu;
+  const T* body = seg + head;
+  const int nvec = (len - head) / VPE;
+  float bv = -INFINITY;
+  int bat = -1;
+#pragma unroll 4
+  for (int v = lane; v < nvec; v += 32) {
+    const uint4 u = *reinterpret_cast<const uint4*>(body + (size_t)v * VPE);
+    const float m = Ops::vmax(u);
+    if (m > bv || (bat < 0 && m == m)) {
+      bv = m;
+      bat = v;
     }
   }
-  for (int i = c + st.nvec * VPE + threadIdx.x; i < c1; i += kVerifyThreads) {
-    const float x = Elem<T>::load1(row + i);
-    if (x == x) st.scalar = umax64(st.scalar, argmax_key(x, (uint32_t)i));
+  const int tail0 = head + nvec * VPE;
+  if (tail0 + lane < len) {
+    const float x = Elem<T>::loads(seg + tail0 + lane);
+    if (x == x) key = umax64(key, argmax_key(x, (uint32_t)(col0 + tail0 + lane)));
   }
-  return st;
+  const float wm = warp_max(bv);
+  if (bat >= 0 && bv == wm) {
+    const int f = Ops::find(*reinterpret_cast<const uint4*>(body + (size_t)bat * VPE), bv);
+    if (f >= 0) key = umax64(key, argmax_key(bv, (uint32_t)(col0 + head + bat * VPE + f)));
+  }
+  return warp_max_u64(key);
 }
 
-// This thread's keys for up to two segments: the lanes holding their warp's
-// maximum of a segment take the first element equal to it in the vector they
-// kept.  Warp-collective; has_b is block-uniform.
-template <typename T>
-__device__ __forceinline__ void scan_locate2(const ScanState<T>& sa, const ScanState<T>& sb, bool has_b,
-                                             unsigned long long& ka, unsigned long long& kb) {
-  using Ops = VecOps<T>;
-  constexpr int VPE = Elem<T>::kPerVec;
-  float wa = sa.bv, wb = has_b ? sb.bv : -INFINITY;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    wa = fmaxf(wa, __shfl_xor_sync(0xffffffffu, wa, o));
-    wb = fmaxf(wb, __shfl_xor_sync(0xffffffffu, wb, o));
-  }
-  ka = sa.scalar;
-  kb = has_b ? sb.scalar : 0ull;
-  if (sa.bat >= 0 && sa.bat < sa.nvec && sa.bv == wa) {
-    const int f = Ops::find(sa.bu, sa.bv);
-    if (f >= 0) ka = umax64(ka, argmax_key(sa.bv, (uint32_t)(sa.c + sa.bat * VPE + f)));
-  }
-  if (has_b && sb.bat >= 0 && sb.bat < sb.nvec && sb.bv == wb) {
-    const int f = Ops::find(sb.bu, sb.bv);
-    if (f >= 0) kb = umax64(kb, argmax_key(sb.bv, (uint32_t)(sb.c + sb.bat * VPE + f)));
-  }
-}
-
-// Block-wide maximum of two keys (all threads call; result valid in thread 0).
-__device__ __forceinline__ void block_max2(unsigned long long& k0, unsigned long long& k1,
-                                           unsigned long long (*red)[kVerifyThreads / 32]) {
-  k0 = warp_max_u64(k0);
-  k1 = warp_max_u64(k1);
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = k0;
-    red[1][threadIdx.x >> 5] = k1;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kVerifyThreads / 32; ++w) {
-      k0 = umax64(k0, red[0][w]);
-      k1 = umax64(k1, red[1][w]);
-    }
-  }
-  __syncthreads();
+__device__ __forceinline__ void verify_cons_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(32 * kVerifyConsumers) : "memory");
 }
 
 constexpr int kWalkChunk = 9;  // K_b <= 8 in one round trip
 
 template <typename T>
-__global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(const VerifyArgs<T> a) {
-  __shared__ unsigned long long red[2][kVerifyThreads / 32];
+__global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const VerifyArgs<T> a) {
+  extern __shared__ __align__(128) unsigned char vsm[];
+  __shared__ __align__(8) uint64_t full_bar[kVerifyStages], empty_bar[kVerifyStages];
   __shared__ int am_last;
   pdl_trigger();
-  pdl_wait();
-  // Request metadata for the accept walk, fetched while the scan runs in
-  // case this CTA is the last (thread b holds request b, b < block size).
-  int pk = 0, pr0 = 0, pr1 = 0;
-  if (threadIdx.x < a.B) {
-    pk = a.num_drafts[threadIdx.x];
-    pr0 = a.row_offsets[threadIdx.x];
-    pr1 = a.row_offsets[threadIdx.x + 1];
-  }
-  const long long total = (long long)a.num_rows * a.V;
-  const long long per = (total + gridDim.x - 1) / gridDim.x;
-  const long long e0 = (long long)blockIdx.x * per;
-  const long long e1 = min(total, e0 + per);
-  if (e0 < e1 && per <= a.V) {
-    // The share lies in at most two rows: stream both parts back to back and
-    // reduce once.
-    const int rA = (int)(e0 / a.V);
-    const int cA = (int)(e0 - (long long)rA * a.V);
-    const int cA1 = (int)min((long long)a.V, (long long)cA + (e1 - e0));
-    const int lenB = (int)((e1 - e0) - (cA1 - cA));
-    const ScanState<T> sA = scan_body<T>(a.logits + (size_t)rA * a.V, cA, cA1);
-    ScanState<T> sB = sA;
-    if (lenB > 0) sB = scan_body<T>(a.logits + (size_t)(rA + 1) * a.V, 0, lenB);
-    unsigned long long kA, kB;
-    scan_locate2<T>(sA, sB, lenB > 0, kA, kB);
-    block_max2(kA, kB, red);
-    if (threadIdx.x == 0) {
-      if (kA) atomicMax(a.keys + rA, kA);
-      if (kB) atomicMax(a.keys + rA + 1, kB);
-    }
-  } else {
-    for (long long e = e0; e < e1;) {
-      const int r = (int)(e / a.V);
-      const int c0 = (int)(e - (long long)r * a.V);
-      const int c1 = (int)min((long long)a.V, (long long)c0 + (e1 - e));
-      const ScanState<T> st = scan_body<T>(a.logits + (size_t)r * a.V, c0, c1);
-      unsigned long long k, unused;
-      scan_locate2<T>(st, st, false, k, unused);
-      block_max2(k, unused, red);
-      if (threadIdx.x == 0 && k) atomicMax(a.keys + r, k);
-      e += c1 - c0;
-    }
-  }
-  // Arrival: a release-acquire add orders this CTA's key updates (all made
-  // by thread 0) before it, and the last CTA's reads after it (the barrier
-  // carries the acquire to the other threads).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The flat range [0, num_rows * V) of elements: its 16-byte aligned body
+  // is cut into chunks of a.chunk bytes; the few elements before and after
+  // the body are read directly by one warp.
+  const long long n_elem = (long long)a.num_rows * a.V;
+  const uintptr_t base = (uintptr_t)a.logits;
+  const uintptr_t lo = (base + 15) & ~(uintptr_t)15;
+  const uintptr_t hi = (base + (uintptr_t)n_elem * sizeof(T)) & ~(uintptr_t)15;
+  const bool has_body = hi > lo;
+  const long long body_bytes = has_body ? (long long)(hi - lo) : 0;
+  const long long head_elems = has_body ? (long long)((lo - base) / sizeof(T)) : n_elem;
+  const long long tail_elem0 = has_body ? (long long)((hi - base) / sizeof(T)) : n_elem;
+  const long long nch = (body_bytes + a.chunk - 1) / a.chunk;
+  const long long c0 = (long long)blockIdx.x * nch / gridDim.x;
+  const int n = (int)((long long)(blockIdx.x + 1) * nch / gridDim.x - c0);
+
   if (threadIdx.x == 0) {
+    for (int s = 0; s < kVerifyStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // the logits may come from the kernel just before this one
+    pdl_wait();
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // each logit is read once
+      for (int it = 0; it < n; ++it) {
+        const int s = it % kVerifyStages;
+        if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)(((it / kVerifyStages) & 1) ^ 1), kVerifyWaitLimit)) {
+          set_error(a.err, MTP_ERR_TIMEOUT);
+          break;
+        }
+        const long long off = (c0 + it) * (long long)a.chunk;
+        const uint32_t bytes = (uint32_t)min((long long)a.chunk, body_bytes - off);
+        mbar_expect_tx(&full_bar[s], bytes);
+        bulk_g2s_hint(vsm + (size_t)s * kVerifyStageBytes, (const void*)(lo + off), bytes, &full_bar[s], pol);
+      }
+    }
+    return;
+  }
+
+  pdl_wait();
+  const int ct = threadIdx.x - 32;   // 0 .. 255
+  // request metadata for the accept walk, in case this CTA is the last
+  int pk = 0, pr0 = 0, pr1 = 0;
+  if (ct < a.B) {
+    pk = a.num_drafts[ct];
+    pr0 = a.row_offsets[ct];
+    pr1 = a.row_offsets[ct + 1];
+  }
+  // elements outside the aligned body (fewer than 16 bytes at each end)
+  if (blockIdx.x == 0 && warp == 1) {
+    const long long n_out = head_elems + (n_elem - tail_elem0);
+    for (long long i = lane; i < n_out; i += 32) {
+      const long long e = i < head_elems ? i : tail_elem0 + (i - head_elems);
+      const float x = Elem<T>::load1(a.logits + e);
+      const int r = (int)(e / a.V);
+      if (x == x) atomicMax(a.keys + r, argmax_key(x, (uint32_t)(e - (long long)r * a.V)));
+    }
+  }
+  const int cw = warp - 1;
+  bool timed_out = false;
+  int it = cw;
+  for (; it < n; it += kVerifyConsumers) {
+    const int s = it % kVerifyStages;
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], (uint32_t)((it / kVerifyStages) & 1),
+                                                   kVerifyWaitLimit))) {
+      timed_out = true;
+      break;
+    }
+    const long long off = (c0 + it) * (long long)a.chunk;
+    const long long cnt = min((long long)a.chunk, body_bytes - off) / (long long)sizeof(T);
+    const long long e0 = head_elems + off / (long long)sizeof(T);
+    const T* sp = reinterpret_cast<const T*>(vsm + (size_t)s * kVerifyStageBytes);
+    for (long long e = e0; e < e0 + cnt;) {
+      const int r = (int)(e / a.V);
+      const long long r_end = min(e0 + cnt, (long long)(r + 1) * a.V);
+      const unsigned long long key =
+          segment_key<T>(sp + (e - e0), (int)(r_end - e), (int)(e - (long long)r * a.V), lane);
+      if (lane == 0 && key) atomicMax(a.keys + r, key);
+      e = r_end;
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[s])) : "memory");
+  }
+  if (timed_out) {
+    if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+    // copies still in flight into this warp's stage get a bounded chance to land
+    mbar_wait_bounded(&full_bar[it % kVerifyStages], (uint32_t)((it / kVerifyStages) & 1), kVerifyWaitLimit);
+  }
+  // Arrival: every lane fences its key updates, the consumer barrier
+  // collects them, and a release-acquire add publishes the CTA's work; the
+  // last CTA's reads come after its acquire (the barrier carries it to the
+  // other consumer threads).
+  __threadfence();
+  verify_cons_bar();
+  if (ct == 0) {
     int prev;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.cnt) : "memory");
     am_last = (prev == (int)gridDim.x - 1);
   }
-  __syncthreads();
+  verify_cons_bar();
   if (!am_last) return;
-  for (int b = threadIdx.x; b < a.B; b += kVerifyThreads) {
-    const int K_b = b < kVerifyThreads ? pk : a.num_drafts[b];
-    const int r0 = b < kVerifyThreads ? pr0 : a.row_offsets[b];
-    const int r1 = b < kVerifyThreads ? pr1 : a.row_offsets[b + 1];
+  constexpr int kWalkThreads = 32 * kVerifyConsumers;
+  for (int b = ct; b < a.B; b += kWalkThreads) {
+    const int K_b = b < kWalkThreads ? pk : a.num_drafts[b];
+    const int r0 = b < kWalkThreads ? pr0 : a.row_offsets[b];
+    const int r1 = b < kWalkThreads ? pr1 : a.row_offsets[b + 1];
     const bool bad = K_b < 0 || K_b > a.max_k || K_b > a.drafts_stride || r1 - r0 != K_b + 1 || r0 < 0 ||
                      r0 + K_b + 1 > a.num_rows;
     if (bad) {
@@ -297,7 +276,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(const VerifyA
 #pragma unroll
       for (int q = 0; q < kWalkChunk; ++q) {
         const int jj = j0 + q;
-        r[q] = jj <= K_b ? (int)key_index(__ldcg(a.keys + r0 + jj)) : -1;
+        const unsigned long long k = jj <= K_b ? __ldcg(a.keys + r0 + jj) : 0ull;
+        r[q] = k ? (int)key_index(k) : -1;
         d[q] = jj < K_b ? a.drafts[(size_t)b * a.drafts_stride + jj] : -1;
       }
 #pragma unroll
@@ -315,17 +295,34 @@ __global__ void __launch_bounds__(kVerifyThreads, 4) verify_kernel(const VerifyA
     a.accepted[b] = acc;
     a.bonus[b] = bonus;
   }
-  __syncthreads();
-  for (int r = threadIdx.x; r < a.num_rows; r += kVerifyThreads) a.keys[r] = 0ull;
-  if (threadIdx.x == 0) *a.cnt = 0;
+  verify_cons_bar();
+  for (int r = ct; r < a.num_rows; r += kWalkThreads) a.keys[r] = 0ull;
+  if (ct == 0) *a.cnt = 0;
 }
 
-// Grid of the verify kernel: a few CTAs per SM, at least 16K elements each.
-static int verify_grid(int sms, int num_rows, int V) {
-  const long long total = (long long)num_rows * V;
-  long long g = (total + 16383) / 16384;
-  if (g > 4LL * sms) g = 4LL * sms;
-  return g < 1 ? 1 : (int)g;
+// Chunk size and grid of the verify kernel for a flat range of `bytes`:
+// about eight chunks per CTA (one per consumer warp) when the range is
+// small, chunks of a whole stage when it is large; at most one CTA per SM.
+static void verify_plan(int sms, long long bytes, uint32_t* chunk, int* grid) {
+  long long c = (bytes + 8LL * sms - 1) / (8LL * sms);
+  c = (c + 15) & ~15LL;
+  if (c < (long long)kVerifyMinChunk) c = kVerifyMinChunk;
+  if (c > (long long)kVerifyStageBytes) c = kVerifyStageBytes;
+  const long long nch = (bytes + c - 1) / c;
+  *chunk = (uint32_t)c;
+  *grid = (int)(nch < 1 ? 1 : (nch < sms ? nch : sms));
+}
+
+constexpr size_t kVerifySmem = (size_t)kVerifyStages * kVerifyStageBytes;
+
+// Launch of the verify kernel (shared by mtp_verify and the context-free
+// variant): keys and cnt must be zero on entry, and the kernel's shared-
+// memory limit raised to kVerifySmem on this device beforehand.
+template <typename T>
+static cudaError_t launch_verify_kernel(cudaStream_t s, int sms, VerifyArgs<T> a) {
+  int grid = 1;
+  verify_plan(sms, (long long)a.num_rows * a.V * (long long)sizeof(T), &a.chunk, &grid);
+  return launch_pdl(verify_kernel<T>, dim3(grid), dim3(kVerifyThreads), kVerifySmem, s, a);
 }
 
 template <typename T>
@@ -409,17 +406,18 @@ cudaError_t launch_verify(mtp_ctx* ctx, cudaStream_t s, int B, const void* logit
                           int32_t* accepted, int32_t* bonus) {
   const mtp_config& c = ctx->cfg;
   if (num_rows > c.max_batch * (c.max_k + 1)) return cudaErrorInvalidValue;
-  const dim3 grid(verify_grid(ctx->num_sms, num_rows, c.vocab));
-  cudaError_t e;
+  cudaError_t e = ensure_smem(c.dtype == MTP_DTYPE_BF16 ? (const void*)verify_kernel<uint16_t>
+                                                         : (const void*)verify_kernel<float>, kVerifySmem);
+  if (e != cudaSuccess) return e;
   prof_before(ctx, MTP_KERNEL_VERIFY, s);
   if (c.dtype == MTP_DTYPE_BF16) {
     VerifyArgs<uint16_t> a{(const uint16_t*)logits, row_offsets, drafts, drafts_stride, num_drafts, accepted, bonus,
-                           ctx->ver_keys, ctx->ver_cnt, ctx->err, c.vocab, c.max_k, B, num_rows};
-    e = launch_pdl(verify_kernel<uint16_t>, grid, dim3(kVerifyThreads), 0, s, a);
+                           ctx->ver_keys, ctx->ver_cnt, ctx->err, c.vocab, c.max_k, B, num_rows, 0u};
+    e = launch_verify_kernel(s, ctx->num_sms, a);
   } else {
     VerifyArgs<float> a{(const float*)logits, row_offsets, drafts, drafts_stride, num_drafts, accepted, bonus,
-                        ctx->ver_keys, ctx->ver_cnt, ctx->err, c.vocab, c.max_k, B, num_rows};
-    e = launch_pdl(verify_kernel<float>, grid, dim3(kVerifyThreads), 0, s, a);
+                        ctx->ver_keys, ctx->ver_cnt, ctx->err, c.vocab, c.max_k, B, num_rows, 0u};
+    e = launch_verify_kernel(s, ctx->num_sms, a);
   }
   prof_after(ctx, MTP_KERNEL_VERIFY, s);
   ctx->launches++;
@@ -511,6 +509,13 @@ static cudaError_t noalloc_setup(int dev, NoAllocScratch** out, int* sms) {
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    // the verify kernel's shared-memory limit, once per device
+    e = cudaFuncSetAttribute((const void*)verify_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kVerifySmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute((const void*)verify_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kVerifySmem);
+    if (e != cudaSuccess) return e;
     g_noalloc_sms[dev] = n;
     g_noalloc_ptr[dev] = (NoAllocScratch*)p;
   }
@@ -550,16 +555,15 @@ extern "C" mtp_status mtp_verify_noalloc(void* stream, int B, int vocab, int dty
     cudaGetLastError();
     return MTP_ERR_CUDA;
   }
-  const dim3 grid(verify_grid(sms, num_rows, vocab));
   cudaError_t e;
   if (dtype == MTP_DTYPE_BF16) {
     VerifyArgs<uint16_t> a{(const uint16_t*)target_logits, row_offsets, drafts, drafts_stride, num_drafts, accepted,
-                           bonus, sc->keys, sc->cnt, &sc->err, vocab, max_k, B, num_rows};
-    e = launch_pdl(verify_kernel<uint16_t>, grid, dim3(kVerifyThreads), 0, s, a);
+                           bonus, sc->keys, sc->cnt, &sc->err, vocab, max_k, B, num_rows, 0u};
+    e = launch_verify_kernel(s, sms, a);
   } else {
     VerifyArgs<float> a{(const float*)target_logits, row_offsets, drafts, drafts_stride, num_drafts, accepted, bonus,
-                        sc->keys, sc->cnt, &sc->err, vocab, max_k, B, num_rows};
-    e = launch_pdl(verify_kernel<float>, grid, dim3(kVerifyThreads), 0, s, a);
+                        sc->keys, sc->cnt, &sc->err, vocab, max_k, B, num_rows, 0u};
+    e = launch_verify_kernel(s, sms, a);
   }
   if (e != cudaSuccess) {
     cudaGetLastError();
