@@ -369,6 +369,9 @@ def run_ours(args, rank, world, local_rank):
         copies.append(e0.elapsed_time(e1))
     copy_gbs = 2 * nbytes / (min(copies) * 1e-3) / 1e9
     del src, dst
+    kb0 = kernel_bytes(cfg, wl.lens, K, fmt=args.weights)
+    read_floor = read_floor_us({"attention": kb0["attention"], "verify": kb0["verify"],
+                                "lm_head": kb0["lm_head"]}, stream)
 
     for _ in range(args.warmup):
         wl.step()
@@ -500,6 +503,7 @@ def run_ours(args, rank, world, local_rank):
                      "launches_timed": len(lm_ms), "bytes_per_launch": roof_bytes},
         "kernels": kernels,
         "stream_copy_gbs": copy_gbs,
+        "read_floor": read_floor,
         "gpu_launches": int(launches),
         "deterministic_ids": deterministic,
         "clocks": clocks,
@@ -521,6 +525,37 @@ def l2_flush(buf) -> None:
     the whole L2 of dirty lines as it misses, which is not that kernel's
     traffic."""
     buf.sum()
+
+
+def read_floor_us(sizes: dict, stream, reps: int = 10) -> dict:
+    """Best time of the read-only yardstick (mtp_stream_read: the bytes
+    streamed once into shared memory, nothing computed) for each named byte
+    count, L2 flushed by a read before every timed call: the least a kernel
+    that only reads that many bytes takes, launch and tail included."""
+    import torch
+    import mtp_self_speculative_gb300 as M
+    biggest = max(int(v) for v in sizes.values())
+    buf = torch.empty((biggest + 4095) // 4096 * 4096, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda").fill_(1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    for name, n in sizes.items():
+        n = int(n) // 16 * 16
+        best = float("inf")
+        for r in range(reps + 2):
+            l2_flush(flush)
+            e0.record(stream)
+            M.mtp_stream_read(buf, n, err)
+            e1.record(stream)
+            e1.synchronize()
+            if r >= 2:
+                best = min(best, e0.elapsed_time(e1))
+        out[name] = {"bytes": n, "us": round(best * 1e3, 2), "gbs": round(n / (best * 1e-3) / 1e9, 1)}
+    assert int(err.item()) == 0
+    del buf, flush
+    return out
 
 
 def timed_steps(fn, n: int, stream) -> float:

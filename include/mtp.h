@@ -440,6 +440,17 @@ const char* mtp_status_str(mtp_status s);
  * bytes a multiple of 16. */
 mtp_status mtp_stream_copy(void* stream, void* dst, const void* src, size_t bytes);
 
+/* Read-only yardstick: `bytes` bytes at src (device memory, 16-byte aligned,
+ * bytes a multiple of 16) are streamed once into shared memory with bulk
+ * copies -- one CTA per SM, a contiguous share each, the mechanism of the
+ * streamed kernels -- and nothing is computed or written.  Its duration is
+ * the floor of a kernel that only has to read that many bytes (launch,
+ * first-byte latency and tail included).  err_word: optional caller-owned
+ * device int that receives MTP_ERR_TIMEOUT if a bounded wait ran out (NULL:
+ * not reported).  Asynchronous on `stream`; MTP_ERR_INVALID for bad
+ * arguments. */
+mtp_status mtp_stream_read(void* stream, const void* src, size_t bytes, int* err_word);
+
 /* Kernel timing.  Kernel ids for mtp_profile_begin. */
 typedef enum {
   MTP_KERNEL_EH_PROJ = 0,

@@ -411,6 +411,13 @@ def mtp_stream_copy(dst: torch.Tensor, src: torch.Tensor, nbytes: Optional[int] 
            "mtp_stream_copy")
 
 
+def mtp_stream_read(src: torch.Tensor, nbytes: Optional[int] = None, err_word: Optional[torch.Tensor] = None,
+                    stream=None) -> None:
+    n = src.numel() * src.element_size() if nbytes is None else nbytes
+    _check(_clib.mtp_stream_read(_stream(stream), _ptr(src, name="src"), n, _ptr(err_word, torch.int32, "err_word")),
+           "mtp_stream_read")
+
+
 def mtp_profile_begin(ctx: Context, kernel: int, capacity: int) -> None:
     _check(_clib.mtp_profile_begin(ctx.handle, int(kernel), int(capacity)), "mtp_profile_begin")
 

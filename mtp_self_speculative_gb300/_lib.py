@@ -94,6 +94,7 @@ SIGNATURES = {
     "mtp_destroy": (None, [c_void_p]),
     "mtp_status_str": (ctypes.c_char_p, [c_int]),
     "mtp_stream_copy": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t]),
+    "mtp_stream_read": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
     "mtp_profile_begin": (c_int, [c_void_p, c_int, c_int]),
     "mtp_profile_end": (c_int, [c_void_p, ctypes.POINTER(c_float), c_int, ctypes.POINTER(c_int)]),
     "mtp_launch_count": (c_int64, [c_void_p]),

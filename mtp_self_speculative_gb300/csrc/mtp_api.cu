@@ -411,6 +411,14 @@ mtp_status mtp_stream_copy(void* stream, void* dst, const void* src, size_t byte
   return after_launch(launch_stream_copy((cudaStream_t)stream, dst, src, bytes, sms));
 }
 
+mtp_status mtp_stream_read(void* stream, const void* src, size_t bytes, int* err_word) {
+  if (!src || bytes == 0 || bytes % 16 || ((uintptr_t)src & 15)) return MTP_ERR_INVALID;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MTP_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
+  return after_launch(launch_stream_read((cudaStream_t)stream, src, bytes, sms, err_word));
+}
+
 mtp_status mtp_profile_begin(mtp_ctx* ctx, int kernel, int capacity) {
   if (!ctx || kernel < 0 || kernel >= MTP_KERNEL_COUNT || capacity < 1 || capacity > (1 << 20))
     return MTP_ERR_INVALID;

@@ -334,6 +334,7 @@ cudaError_t launch_verify(mtp_ctx* ctx, cudaStream_t s, int B, const void* logit
 cudaError_t launch_kv_edit(mtp_ctx* ctx, cudaStream_t s, int B, const mtp_kv* kv, int mode,
                            const int32_t* arg, int extra);
 cudaError_t launch_stream_copy(cudaStream_t s, void* dst, const void* src, size_t bytes, int num_sms);
+cudaError_t launch_stream_read(cudaStream_t s, const void* src, size_t bytes, int num_sms, int* err);
 
 enum KvEditMode { KV_COMMIT = 0, KV_COMMIT_ACCEPTED = 1, KV_ROLLBACK = 2, KV_TRUNCATE = 3 };
 

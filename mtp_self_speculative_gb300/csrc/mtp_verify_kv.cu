@@ -467,6 +467,70 @@ cudaError_t launch_stream_copy(cudaStream_t s, void* dst, const void* src, size_
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ stream read
+// Read-only yardstick: the bytes are streamed once into a ring of shared-
+// memory stages with one-dimensional bulk copies (the same mechanism as the
+// streamed projections and verify), one CTA per SM, a contiguous share per
+// CTA, and nothing is computed; its duration is the floor of a kernel that
+// only has to read those bytes.
+constexpr int kReadStages = 8;
+constexpr uint32_t kReadChunk = 16384;
+constexpr uint32_t kReadWaitLimit = 1u << 24;
+
+__global__ void __launch_bounds__(64, 1) stream_read_kernel(const unsigned char* __restrict__ src, size_t bytes,
+                                                            int* err) {
+  extern __shared__ __align__(128) unsigned char rsm[];
+  __shared__ __align__(8) uint64_t full_bar[kReadStages], empty_bar[kReadStages];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long nch = (long long)((bytes + kReadChunk - 1) / kReadChunk);
+  const long long c0 = (long long)blockIdx.x * nch / gridDim.x;
+  const int n = (int)((long long)(blockIdx.x + 1) * nch / gridDim.x - c0);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kReadStages; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (lane != 0) return;
+  if (warp == 0) {
+    const uint64_t pol = l2_evict_first_policy();
+    for (int it = 0; it < n; ++it) {
+      const int st = it % kReadStages;
+      if (!mbar_wait_bounded(&empty_bar[st], (uint32_t)(((it / kReadStages) & 1) ^ 1), kReadWaitLimit)) {
+        if (err) set_error(err, MTP_ERR_TIMEOUT);
+        return;
+      }
+      const size_t off = (size_t)(c0 + it) * kReadChunk;
+      const uint32_t nb = (uint32_t)(bytes - off < kReadChunk ? bytes - off : kReadChunk);
+      mbar_expect_tx(&full_bar[st], nb);
+      bulk_g2s_hint(rsm + (size_t)st * kReadChunk, src + off, nb, &full_bar[st], pol);
+    }
+  } else {
+    for (int it = 0; it < n; ++it) {
+      const int st = it % kReadStages;
+      if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((it / kReadStages) & 1), kReadWaitLimit)) {
+        if (err) set_error(err, MTP_ERR_TIMEOUT);
+        // a copy still in flight gets a bounded chance to land
+        mbar_wait_bounded(&full_bar[st], (uint32_t)((it / kReadStages) & 1), kReadWaitLimit);
+        return;
+      }
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[st])) : "memory");
+    }
+  }
+}
+
+cudaError_t launch_stream_read(cudaStream_t s, const void* src, size_t bytes, int num_sms, int* err) {
+  const size_t smem = (size_t)kReadStages * kReadChunk;
+  cudaError_t e = ensure_smem((const void*)stream_read_kernel, smem);
+  if (e != cudaSuccess) return e;
+  const long long nch = (long long)((bytes + kReadChunk - 1) / kReadChunk);
+  const int grid = (int)(nch < num_sms ? nch : num_sms);
+  stream_read_kernel<<<grid, 64, smem, s>>>((const unsigned char*)src, bytes, err);
+  return cudaGetLastError();
+}
+
 }  // namespace mtp
 
 // ------------------------------------------- allocation-free verification

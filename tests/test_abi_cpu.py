@@ -127,3 +127,11 @@ def test_verify_wrappers_check_shapes_before_any_call():
 class _NullStream:
     """Stands in for a torch stream on a machine without a GPU (handle 0)."""
     cuda_stream = 0
+
+
+def test_stream_read_rejects_bad_arguments(lib):
+    from mtp_self_speculative_gb300 import _lib
+    assert lib.mtp_stream_read(None, None, 4096, None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_stream_read(None, 16, 0, None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_stream_read(None, 16, 4008, None) == _lib.MTP_ERR_INVALID
+    assert lib.mtp_stream_read(None, 24, 4096, None) == _lib.MTP_ERR_INVALID

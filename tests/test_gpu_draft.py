@@ -315,3 +315,16 @@ def test_bounded_wait_runs_out_and_reports_timeout(which):
     assert M.mtp_get_device_error(case.ctx) == 0
     check_forced(case, [0], F32_LOGIT_TOL)
 
+
+
+@pytest.mark.parametrize("n_q", [8, 16, 32])
+def test_long_context_small_batch_split_combine_bf16(n_q):
+    """Contexts of 2500 and 3001 tokens at B = 2 with 2, 4 and 8 query heads
+    per kv head: the tensor-core attention splits each (request, kv head)
+    over many CTAs and merges the splits (several lanes per output item for
+    2 and 4 heads per kv head), on both small-batch paths' step kernels."""
+    cfg = synth.MTPShape("long_ctx_bf16", H=1024, n_q=n_q, n_kv=4, head_dim=128, ffn=2048, vocab=5003, batch=2,
+                         K=3, dtype="bf16", ctx_lo=2500, ctx_hi=3001, paged_shuffle=True, seed_index=56)
+    case = Case(cfg, norm="random", lens=[3001, 2500], persistent_max_batch=-1)
+    _, _, ids, logits = check_forced(case, [0, 1], LOGIT_TOL)
+    check_free(case, [0, 1], ids, logits, LOGIT_TOL)
