@@ -121,20 +121,42 @@ __device__ __forceinline__ void attn_store_out(const AttnArgs<T>& a, int b, int 
 
 constexpr int kCombineBatch = 16;
 
-template <typename T, int HD, int G>
+// Online-softmax merge of (M, L, O) with another state (base-2 exponents).
+__device__ __forceinline__ void merge_state(float& M, float& L, float4& O, float m2, float l2, float4 o2) {
+  if (m2 == -INFINITY) return;
+  const float Mn = fmaxf(M, m2);
+  const float co = (M == -INFINITY) ? 0.0f : exp2f(M - Mn), cn = exp2f(m2 - Mn);
+  L = L * co + l2 * cn;
+  O.x = O.x * co + o2.x * cn;
+  O.y = O.y * co + o2.y * cn;
+  O.z = O.z * co + o2.z * cn;
+  O.w = O.w * co + o2.w * cn;
+  M = Mn;
+}
+
+// W warps per CTA.  Merge the per-warp online-softmax states of this CTA,
+// then either write the output (one split) or a partial (M, L, O) and, in
+// the last CTA of the (request, kv head), combine all splits: an item
+// (head, 4 dims) is served by P = threads / items consecutive lanes (at
+// least 1), lane p merging splits p, p + P, ... online (sixteen partials'
+// loads in flight at a time); the P states then merge by shuffles.
+template <typename T, int HD, int G, int W = kAttnWarps>
 __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, float (*wm)[G], float (*wl)[G], int s,
                                    int g, int b, int nsplit) {
   constexpr int RS = HD + 4;  // partial row stride (16-byte aligned rows)
+  constexpr int NT = W * 32;
+  constexpr int ITEMS = G * (HD / 4);
+  constexpr int P = (NT / ITEMS) >= 8 ? 8 : (NT / ITEMS) >= 4 ? 4 : (NT / ITEMS) >= 2 ? 2 : 1;
   __shared__ int am_last;
   float* part_base = a.part + ((size_t)b * a.n_q + (size_t)g * G) * a.max_splits * RS;
-  for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+  for (int idx = threadIdx.x; idx < G * HD; idx += NT) {
     const int h = idx / HD, d = idx - h * HD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w][h]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w][h]);
     float L = 0.0f, O = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
+    for (int w = 0; w < W; ++w) {
       const float f = (wm[w][h] == -INFINITY) ? 0.0f : exp2f(wm[w][h] - M);
       L += wl[w][h] * f;
       O += wacc[((size_t)w * G + h) * HD + d] * f;
@@ -156,44 +178,51 @@ __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, floa
   }
   __syncthreads();
   if (!am_last) return;
-  for (int it = threadIdx.x; it < G * (HD / 4); it += kAttnThreads) {
-    const int h = it / (HD / 4), d4 = it - h * (HD / 4);
+  for (int it = threadIdx.x; it < ITEMS * P; it += NT) {
+    const int item = it / P, p = it - item * P;
+    const int h = item / (HD / 4), d4 = item - h * (HD / 4);
     const float* ph = part_base + (size_t)h * a.max_splits * RS;
     float Mr = -INFINITY, Lr = 0.0f;
     float4 Or = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int j0 = 0; j0 < nsplit; j0 += kCombineBatch) {
+    for (int j0 = p; j0 < nsplit; j0 += P * kCombineBatch) {
       float mj[kCombineBatch], lj[kCombineBatch];
       float4 oj[kCombineBatch];
 #pragma unroll
       for (int q = 0; q < kCombineBatch; ++q) {
+        const int j = j0 + q * P;
         mj[q] = -INFINITY;
         lj[q] = 0.0f;
         oj[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (j0 + q < nsplit) {
-          const float* r = ph + (size_t)(j0 + q) * RS;
+        if (j < nsplit) {
+          const float* r = ph + (size_t)j * RS;
           mj[q] = __ldcg(r);
           lj[q] = __ldcg(r + 1);
           oj[q] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
         }
       }
 #pragma unroll
-      for (int q = 0; q < kCombineBatch; ++q) {
-        if (mj[q] == -INFINITY) continue;
-        const float Mn = fmaxf(Mr, mj[q]);
-        const float co = (Mr == -INFINITY) ? 0.0f : exp2f(Mr - Mn), cn = exp2f(mj[q] - Mn);
-        Lr = Lr * co + lj[q] * cn;
-        Or.x = Or.x * co + oj[q].x * cn;
-        Or.y = Or.y * co + oj[q].y * cn;
-        Or.z = Or.z * co + oj[q].z * cn;
-        Or.w = Or.w * co + oj[q].w * cn;
-        Mr = Mn;
+      for (int q = 0; q < kCombineBatch; ++q) merge_state(Mr, Lr, Or, mj[q], lj[q], oj[q]);
+    }
+    if constexpr (P > 1) {
+      // all threads take part (ITEMS * P == NT): merge the P lanes of an item
+#pragma unroll
+      for (int o = 1; o < P; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, Mr, o), l2 = __shfl_xor_sync(0xffffffffu, Lr, o);
+        float4 o2;
+        o2.x = __shfl_xor_sync(0xffffffffu, Or.x, o);
+        o2.y = __shfl_xor_sync(0xffffffffu, Or.y, o);
+        o2.z = __shfl_xor_sync(0xffffffffu, Or.z, o);
+        o2.w = __shfl_xor_sync(0xffffffffu, Or.w, o);
+        merge_state(Mr, Lr, Or, m2, l2, o2);
       }
     }
-    const float inv = 1.0f / Lr;
-    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 0, Or.x * inv);
-    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 1, Or.y * inv);
-    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 2, Or.z * inv);
-    attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 3, Or.w * inv);
+    if (p == 0) {
+      const float inv = 1.0f / Lr;
+      attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 0, Or.x * inv);
+      attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 1, Or.y * inv);
+      attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 2, Or.z * inv);
+      attn_store_out<T, HD, G>(a, b, g, h, 4 * d4 + 3, Or.w * inv);
+    }
   }
   if (threadIdx.x == 0) a.cnt[(size_t)b * a.n_kv + g] = 0;
 }
@@ -221,10 +250,11 @@ __device__ __forceinline__ void attn_finish(const AttnArgs<T>& a, unsigned char*
 // pass.  No kernel writes the block table, so this runs before the
 // dependency wait; the tiles' copies then need no dependent L2 read each.
 template <typename T>
-__device__ __forceinline__ void load_block_slice(const AttnArgs<T>& a, int* s_bt, int s, int b) {
+__device__ __forceinline__ void load_block_slice(const AttnArgs<T>& a, int* s_bt, int s, int b,
+                                                 int nthreads = kAttnThreads) {
   const int blk0 = s * a.bps;
   const int n = min(a.bps, a.max_blocks - blk0);
-  for (int i = threadIdx.x; i < n; i += kAttnThreads) s_bt[i] = a.block_table[(size_t)b * a.max_blocks + blk0 + i];
+  for (int i = threadIdx.x; i < n; i += nthreads) s_bt[i] = a.block_table[(size_t)b * a.max_blocks + blk0 + i];
 }
 
 // Shared-memory bytes of the block-table slice (16-byte multiple).
@@ -392,26 +422,26 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
 // the group's query heads on M, P kept in registers) on K/V tiles staged by
 // swizzled 2-D tensor-map loads.
 
-template <int G>
-__global__ void __launch_bounds__(kAttnThreads, 2)
+template <int G, int W, int NSTG>
+__global__ void __launch_bounds__(W * 32, (W <= 4) ? 2 : 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const AttnArgs<uint16_t> a) {
   constexpr int HD = 128;
   constexpr uint32_t TILE_BYTES = 16 * HD * 2;  // 4 KB per K or V tile
   extern __shared__ __align__(1024) unsigned char smem_raw_in[];
   unsigned char* smem_raw = (unsigned char*)(((uintptr_t)smem_raw_in + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t bars[kAttnWarps][kStages];
-  __shared__ float wm[kAttnWarps][G], wl[kAttnWarps][G];
+  __shared__ __align__(8) uint64_t bars[W][NSTG];
+  __shared__ float wm[W][G], wl[W][G];
 
-  int* s_bt = reinterpret_cast<int*>(smem_raw + (size_t)kAttnWarps * kStages * 2 * TILE_BYTES);
+  int* s_bt = reinterpret_cast<int*>(smem_raw + (size_t)W * NSTG * 2 * TILE_BYTES);
 
   pdl_trigger();
   const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;
-  if (threadIdx.x < kAttnWarps * kStages) mbar_init(&bars[threadIdx.x / kStages][threadIdx.x % kStages], 1);
+  if (threadIdx.x < W * NSTG) mbar_init(&bars[threadIdx.x / NSTG][threadIdx.x % NSTG], 1);
   fence_mbar_init();
-  load_block_slice(a, s_bt, s, b);
+  load_block_slice(a, s_bt, s, b, W * 32);
   __syncthreads();
   pdl_wait();
 
@@ -422,7 +452,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
   const int blk1 = min(nblk, blk0 + a.bps);
   const int nsplit = (nblk + a.bps - 1) / a.bps;
 
-  unsigned char* my_stage = smem_raw + (size_t)warp * kStages * 2 * TILE_BYTES;
+  unsigned char* my_stage = smem_raw + (size_t)warp * NSTG * 2 * TILE_BYTES;
   auto tile_row = [&](int bi) -> int {
     int blk = (bi < a.max_blocks) ? s_bt[bi - blk0] : -1;
     if (blk < 0 || blk >= a.num_blocks) {
@@ -432,14 +462,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     return (blk * a.n_kv + g) * 16;
   };
   auto issue = [&](int it, int bi) {
-    const int st = it % kStages;
+    const int st = it % NSTG;
     tma_kv_tile(my_stage + (size_t)st * 2 * TILE_BYTES, &kmap, &vmap, tile_row(bi), &bars[warp][st]);
   };
 
   const int first = blk0 + warp;
-  const int count = (first < blk1) ? (blk1 - first + kAttnWarps - 1) / kAttnWarps : 0;
+  const int count = (first < blk1) ? (blk1 - first + W - 1) / W : 0;
   if (lane == 0)
-    for (int it = 0; it < count && it < kStages; ++it) issue(it, first + it * kAttnWarps);
+    for (int it = 0; it < count && it < NSTG; ++it) issue(it, first + it * W);
   __syncwarp();
 
   // the query fragments load while the first tiles are in flight
@@ -452,8 +482,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
   int stop_at = -1;
   for (int it = 0; it < count; ++it) {
-    const int st = it % kStages;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], (uint32_t)((it / kStages) & 1),
+    const int st = it % NSTG;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[warp][st], (uint32_t)((it / NSTG) & 1),
                                                               kWaitLimit));
     if (!ok) {
       stop_at = it;
@@ -461,17 +491,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
     const uint32_t kt = smem_addr(my_stage + (size_t)st * 2 * TILE_BYTES);
     const uint32_t vt = kt + TILE_BYTES;
-    const int tok0 = (first + it * kAttnWarps) * 16;
+    const int tok0 = (first + it * W) * 16;
 
     attn_tile_mma(kt, vt, qa, o, m_run, l_run, tok0, T_len, lane);
     __syncwarp();
-    if (lane == 0 && it + kStages < count) issue(it + kStages, first + (it + kStages) * kAttnWarps);
+    if (lane == 0 && it + NSTG < count) issue(it + NSTG, first + (it + NSTG) * W);
     __syncwarp();
   }
   if (stop_at >= 0) {
     if (lane == 0) set_error(a.err, MTP_ERR_TIMEOUT);
-    for (int it = stop_at; it < count && it < stop_at + kStages; ++it)
-      mbar_wait_bounded(&bars[warp][it % kStages], (uint32_t)((it / kStages) & 1), kWaitLimit);
+    for (int it = stop_at; it < count && it < stop_at + NSTG; ++it)
+      mbar_wait_bounded(&bars[warp][it % NSTG], (uint32_t)((it / NSTG) & 1), kWaitLimit);
   }
 
   // per-warp state -> shared memory, then the common merge/combine
@@ -489,7 +519,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     }
   }
   __syncthreads();
-  attn_finish_merged<uint16_t, HD, G>(a, wacc, wm, wl, s, g, b, nsplit);
+  attn_finish_merged<uint16_t, HD, G, W>(a, wacc, wm, wl, s, g, b, nsplit);
+}
+
+template <int G, int W, int NSTG>
+static cudaError_t attn_mma_launch(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap& km,
+                                   const CUtensorMap& vm, const AttnArgs<uint16_t>& ab) {
+  auto kern = attn_mma_kernel<G, W, NSTG>;
+  const cudaError_t e = ensure_smem((const void*)kern, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, grid, dim3(W * 32), smem, s, km, vm, ab);
 }
 
 template <typename T, int HD, int G>
@@ -558,9 +597,12 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
   const int G = c.n_q_heads / c.n_kv_heads;
   const int HD = c.head_dim;
   const bool use_mma = sizeof(T) == 2 && HD == 128;
-  // the tensor-core kernel keeps at least 4 blocks per warp to amortise its
-  // set-up and the split combine
+  // the tensor-core kernel keeps at least 16 blocks per split to amortise
+  // its set-up and the split combine; when its grid is short of two CTAs per
+  // SM it runs eight warps per CTA (two blocks each at 16 blocks per split)
   a.bps = attn_bps(ctx, B, kv->max_blocks, use_mma ? 16 : 2);
+  const long long mma_ctas = (long long)((kv->max_blocks + a.bps - 1) / a.bps) * c.n_kv_heads * B;
+  const bool wide = use_mma && mma_ctas <= 2LL * ctx->num_sms;
   const int splits = (kv->max_blocks + a.bps - 1) / a.bps;
   a.max_splits = splits;  // partial-buffer stride of this call
   a.qscale = 1.4426950408889634f / sqrtf((float)c.head_dim);
@@ -570,17 +612,25 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
     const CUtensorMap& km = *kmp;
     const CUtensorMap& vm = *vmp;
     const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
-    const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096 + block_slice_bytes(a.bps);
     dim3 grid(splits, c.n_kv_heads, B);
+    if (wide) {
+      // few CTAs: 8 warps of 2 stages each, every tile of a 16-block split
+      // requested at once
+      const size_t smem = 1024 + (size_t)8 * 2 * 2 * 4096 + block_slice_bytes(a.bps);
+      switch (G) {
+        case 1: return attn_mma_launch<1, 8, 2>(grid, smem, s, km, vm, ab);
+        case 2: return attn_mma_launch<2, 8, 2>(grid, smem, s, km, vm, ab);
+        case 4: return attn_mma_launch<4, 8, 2>(grid, smem, s, km, vm, ab);
+        case 8: return attn_mma_launch<8, 8, 2>(grid, smem, s, km, vm, ab);
+      }
+      return cudaErrorInvalidValue;
+    }
+    const size_t smem = 1024 + (size_t)kAttnWarps * kStages * 2 * 4096 + block_slice_bytes(a.bps);
     switch (G) {
-      case 1: ensure_smem((const void*)attn_mma_kernel<1>, smem);
-              return launch_pdl(attn_mma_kernel<1>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 2: ensure_smem((const void*)attn_mma_kernel<2>, smem);
-              return launch_pdl(attn_mma_kernel<2>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 4: ensure_smem((const void*)attn_mma_kernel<4>, smem);
-              return launch_pdl(attn_mma_kernel<4>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
-      case 8: ensure_smem((const void*)attn_mma_kernel<8>, smem);
-              return launch_pdl(attn_mma_kernel<8>, grid, dim3(kAttnThreads), smem, s, km, vm, ab);
+      case 1: return attn_mma_launch<1, kAttnWarps, kStages>(grid, smem, s, km, vm, ab);
+      case 2: return attn_mma_launch<2, kAttnWarps, kStages>(grid, smem, s, km, vm, ab);
+      case 4: return attn_mma_launch<4, kAttnWarps, kStages>(grid, smem, s, km, vm, ab);
+      case 8: return attn_mma_launch<8, kAttnWarps, kStages>(grid, smem, s, km, vm, ab);
     }
     return cudaErrorInvalidValue;
   }

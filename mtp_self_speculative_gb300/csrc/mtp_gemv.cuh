@@ -278,6 +278,36 @@ __device__ __forceinline__ float cons_stage_raw(float* row, int C, int e0, const
   return ss;
 }
 
+// The same without a norm weight (O and down inputs), for rows up to 8 * 256
+// vectors per round trip to L2: every load of a batch is issued before any
+// of its values is used (the down input of a 12288-wide FFN is staged in one
+// round trip instead of three).
+template <typename T>
+__device__ __forceinline__ float cons_stage_plain(float* row, int C, const float* src, int n) {
+  constexpr int kBatch = 8;
+  const int ct = threadIdx.x - 32;
+  const int nv = n >> 3;
+  float ss = 0.0f;
+  for (int base = ct; base < nv; base += 256 * kBatch) {
+    float x[kBatch][8];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i8 = base + u * 256;
+      if (i8 < nv) load8_row<T, float>(src + (size_t)i8 * 8, x[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i8 = base + u * 256;
+      if (i8 < nv) {
+        const int e = i8 * 8;
+        *reinterpret_cast<float4*>(row + xs_index<T>(e, C)) = make_float4(x[u][0], x[u][1], x[u][2], x[u][3]);
+        *reinterpret_cast<float4*>(row + xs_index<T>(e + 4, C)) = make_float4(x[u][4], x[u][5], x[u][6], x[u][7]);
+      }
+    }
+  }
+  return ss;
+}
+
 // Stage the normalised input row(s) of all nb requests (layout above): one
 // pass that stores x * w and sums x^2 for every vector, one block reduction
 // for all of them, then the scalar RMS factors applied in shared memory.
@@ -307,11 +337,11 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
     } else if constexpr (KIND == QKV_ROPE) {
       s0 = cons_stage_raw<T, float>(dst, C, 0, a.x + (size_t)b * a.H, a.H, a.w_norm_in);
     } else if constexpr (KIND == O_PROJ) {
-      cons_stage_raw<T, float>(dst, C, 0, a.attn + (size_t)b * a.q_dim, a.q_dim, (const T*)nullptr);
+      cons_stage_plain<T>(dst, C, a.attn + (size_t)b * a.q_dim, a.q_dim);
     } else if constexpr (KIND == GATE_UP) {
       s0 = cons_stage_raw<T, float>(dst, C, 0, a.h1 + (size_t)b * a.H, a.H, a.w_norm_post);
     } else if constexpr (KIND == DOWN) {
-      cons_stage_raw<T, float>(dst, C, 0, a.act + (size_t)b * a.F, a.F, (const T*)nullptr);
+      cons_stage_plain<T>(dst, C, a.act + (size_t)b * a.F, a.F);
     } else {
       s0 = cons_stage_raw<T, float>(dst, C, 0, a.hid + (size_t)b * a.H, a.H, a.w_norm_f);
     }
