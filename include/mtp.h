@@ -52,7 +52,9 @@ typedef enum {
   MTP_ERR_OOM = 3,          /* workspace allocation failed                    */
   MTP_ERR_CAPACITY = 4,     /* device: KV slot outside block table / pool     */
   MTP_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out                 */
-  MTP_ERR_DEVICE_ARGS = 6   /* device: inconsistent lengths/offsets/pending   */
+  MTP_ERR_DEVICE_ARGS = 6,  /* device: inconsistent lengths/offsets/pending   */
+  MTP_ERR_BOUNDS = 7        /* device, bounds-checked build only: a store fell
+                               outside its output's extent and was skipped    */
 } mtp_status;
 
 typedef enum { MTP_DTYPE_F32 = 0, MTP_DTYPE_BF16 = 1 } mtp_dtype;
@@ -439,6 +441,22 @@ const char* mtp_status_str(mtp_status s);
  * to the kernels).  dst and src must be 16-byte aligned and not overlap;
  * bytes a multiple of 16. */
 mtp_status mtp_stream_copy(void* stream, void* dst, const void* src, size_t bytes);
+
+/* Bounds-checked builds.  A library compiled with -DMTP_CHECKED (the
+ * package builds it as libmtp_checked.so; the binding loads it when the
+ * environment variable MTP_LIBRARY names it) checks every output store of
+ * the draft, verify and KV kernels against the extent of its buffer for the
+ * call (logits B*K*V, draft ids B*K, hidden_out B*H, accepted/bonus B,
+ * activations B*width, the KV pools num_blocks*n_kv*block_size*head_dim,
+ * the verify keys num_rows, the attention partials); a store outside is
+ * skipped and the error word records MTP_ERR_BOUNDS -- no trap.  It is the
+ * stand-in for a memory checker, which is not available here.
+ * mtp_selftest_bounds: checked builds run one store one element past a
+ * 4-element extent through the check (nothing is written) and return
+ * MTP_OK, leaving MTP_ERR_BOUNDS in the context's error word; other builds
+ * return MTP_ERR_INVALID and launch nothing.  Errors: MTP_ERR_INVALID for
+ * a NULL context. */
+mtp_status mtp_selftest_bounds(mtp_ctx* ctx, void* stream);
 
 /* Read-only yardstick: `bytes` bytes at src (device memory, 16-byte aligned,
  * bytes a multiple of 16) are streamed once into shared memory with bulk

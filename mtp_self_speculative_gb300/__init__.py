@@ -17,7 +17,7 @@ import torch
 
 from . import _lib as L
 from ._lib import (  # noqa: F401
-    KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
+    KERNEL_NAMES, MTP_DTYPE_BF16, MTP_DTYPE_F32, MTP_ERR_BOUNDS, MTP_ERR_CAPACITY, MTP_ERR_CUDA, MTP_ERR_DEVICE_ARGS,
     MTP_ERR_INVALID, MTP_ERR_OOM, MTP_ERR_TIMEOUT, MTP_KERNEL_ATTENTION, MTP_KERNEL_DOWN, MTP_KERNEL_EH_PROJ,
     MTP_KERNEL_GATE_UP, MTP_KERNEL_KV_EDIT, MTP_KERNEL_LM_HEAD, MTP_KERNEL_O_PROJ, MTP_KERNEL_QKV_ROPE,
     MTP_KERNEL_VERIFY, MTP_KERNEL_DRAFT_PERSISTENT, MTP_OK, MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64, MTPConfig, MTPKV,
@@ -391,6 +391,10 @@ def mtp_kv_truncate(ctx: Context, kv: KVCache, new_len: torch.Tensor, stream=Non
 
 def mtp_selftest_wait_timeout(ctx: Context, which: int, stream=None) -> None:
     _check(_clib.mtp_selftest_wait_timeout(ctx.handle, _stream(stream), int(which)), "mtp_selftest_wait_timeout")
+
+
+def mtp_selftest_bounds(ctx: Context, stream=None) -> None:
+    _check(_clib.mtp_selftest_bounds(ctx.handle, _stream(stream)), "mtp_selftest_bounds")
 
 
 def mtp_get_device_error(ctx: Context) -> int:

@@ -8,13 +8,16 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmtp.so")
+# MTP_LIBRARY may name another build of the same library (the bounds-checked
+# libmtp_checked.so); the default is the in-tree libmtp.so.
+LIB_PATH = os.environ.get("MTP_LIBRARY") or os.path.join(HERE, "libmtp.so")
 
 c_int, c_float, c_void_p, c_size_t = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 c_int64 = ctypes.c_int64
 P_i32 = ctypes.c_void_p  # device int32 pointers are passed as plain addresses
 
-MTP_OK, MTP_ERR_INVALID, MTP_ERR_CUDA, MTP_ERR_OOM, MTP_ERR_CAPACITY, MTP_ERR_TIMEOUT, MTP_ERR_DEVICE_ARGS = range(7)
+(MTP_OK, MTP_ERR_INVALID, MTP_ERR_CUDA, MTP_ERR_OOM, MTP_ERR_CAPACITY, MTP_ERR_TIMEOUT, MTP_ERR_DEVICE_ARGS,
+ MTP_ERR_BOUNDS) = range(8)
 MTP_DTYPE_F32, MTP_DTYPE_BF16 = 0, 1
 MTP_WEIGHTS_DENSE, MTP_WEIGHTS_INT4_G64 = 0, 1
 (MTP_KERNEL_EH_PROJ, MTP_KERNEL_QKV_ROPE, MTP_KERNEL_ATTENTION, MTP_KERNEL_O_PROJ, MTP_KERNEL_GATE_UP,
@@ -95,6 +98,7 @@ SIGNATURES = {
     "mtp_status_str": (ctypes.c_char_p, [c_int]),
     "mtp_stream_copy": (c_int, [c_void_p, c_void_p, c_void_p, c_size_t]),
     "mtp_stream_read": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
+    "mtp_selftest_bounds": (c_int, [c_void_p, c_void_p]),
     "mtp_profile_begin": (c_int, [c_void_p, c_int, c_int]),
     "mtp_profile_end": (c_int, [c_void_p, ctypes.POINTER(c_float), c_int, ctypes.POINTER(c_int)]),
     "mtp_launch_count": (c_int64, [c_void_p]),
@@ -108,7 +112,7 @@ def load():
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libmtp.so is not built (%s); run __graft_entry__.build() or "
+        raise ImportError("the MTP library is not built (%s); run __graft_entry__.build() or "
                           "python -m mtp_self_speculative_gb300._build" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():

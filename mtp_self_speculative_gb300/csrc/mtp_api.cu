@@ -72,6 +72,7 @@ const char* mtp_status_str(mtp_status s) {
     case MTP_ERR_CAPACITY: return "KV capacity or position range exceeded";
     case MTP_ERR_TIMEOUT: return "bounded device wait ran out";
     case MTP_ERR_DEVICE_ARGS: return "inconsistent device-side arguments";
+    case MTP_ERR_BOUNDS: return "store outside its output (bounds-checked build)";
   }
   return "unknown status";
 }
@@ -409,6 +410,25 @@ mtp_status mtp_stream_copy(void* stream, void* dst, const void* src, size_t byte
   if (cudaGetDevice(&dev) != cudaSuccess) return MTP_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MTP_ERR_CUDA;
   return after_launch(launch_stream_copy((cudaStream_t)stream, dst, src, bytes, sms));
+}
+
+namespace mtp {
+// One store one element past a 4-element extent, through the bounds check.
+// The destination has room beyond those 4 elements (workspace scratch), so
+// even a build whose check failed to skip would write inside an allocation.
+__global__ void selftest_bounds_kernel(int* err, float* scratch) { MTP_STORE(err, scratch, 4, 4, 1.0f); }
+}  // namespace mtp
+
+mtp_status mtp_selftest_bounds(mtp_ctx* ctx, void* stream) {
+  if (!ctx) return MTP_ERR_INVALID;
+#ifdef MTP_CHECKED
+  if (cudaSetDevice(ctx->device) != cudaSuccess) return MTP_ERR_CUDA;
+  selftest_bounds_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(ctx->err, ctx->hid);
+  return after_launch(cudaGetLastError());
+#else
+  (void)stream;
+  return MTP_ERR_INVALID;
+#endif
 }
 
 mtp_status mtp_stream_read(void* stream, const void* src, size_t bytes, int* err_word) {

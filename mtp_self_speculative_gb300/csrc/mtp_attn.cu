@@ -115,6 +115,7 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 template <typename T, int HD, int G>
 __device__ __forceinline__ void attn_store_out(const AttnArgs<T>& a, int b, int g, int h, int d, float v) {
   const size_t oi = (size_t)b * a.n_q * HD + (size_t)(g * G + h) * HD + d;
+  if (!MTP_IN_BOUNDS(a.err, oi, (long long)(b + 1) * a.n_q * HD)) return;
   a.out[oi] = v;
   if (a.out_bf16) a.out_bf16[oi] = f32_to_bf16_rne(v);
 }
@@ -165,8 +166,11 @@ __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, floa
       attn_store_out<T, HD, G>(a, b, g, h, d, O / L);
     } else {
       float* pp = part_base + ((size_t)h * a.max_splits + s) * RS;
-      if (d == 0) { pp[0] = M; pp[1] = L; }
-      pp[4 + d] = O;
+      // this (request, head)'s row of partials: max_splits rows of RS floats
+      if (MTP_IN_BOUNDS(a.err, (long long)s * RS + 4 + d, (long long)a.max_splits * RS)) {
+        if (d == 0) { pp[0] = M; pp[1] = L; }
+        pp[4 + d] = O;
+      }
     }
   }
   if (nsplit == 1) return;

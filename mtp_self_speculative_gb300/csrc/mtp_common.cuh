@@ -22,6 +22,27 @@ __device__ __forceinline__ void set_error(int* err, int code) {
   atomicCAS(err, 0, code);
 }
 
+// Bounds-checked builds (-DMTP_CHECKED): MTP_IN_BOUNDS(err, i, n) is false,
+// and records MTP_ERR_BOUNDS, when index i lies outside [0, n) of the
+// buffer a store is about to write; callers skip the store then.  In other
+// builds it is the constant true and costs nothing.
+#ifdef MTP_CHECKED
+__device__ __forceinline__ bool in_bounds_checked(int* err, long long i, long long n) {
+  if (i >= 0 && i < n) return true;
+  set_error(err, MTP_ERR_BOUNDS);
+  return false;
+}
+#define MTP_IN_BOUNDS(err, i, n) ::mtp::in_bounds_checked((err), (long long)(i), (long long)(n))
+#else
+#define MTP_IN_BOUNDS(err, i, n) true
+#endif
+// ptr[i] = val, unless a bounds-checked build finds i outside [0, n).
+#define MTP_STORE(err, ptr, i, n, val)                       \
+  do {                                                       \
+    const long long mtp_si_ = (long long)(i);                \
+    if (MTP_IN_BOUNDS((err), mtp_si_, (n))) (ptr)[mtp_si_] = (val); \
+  } while (0)
+
 // ------------------------------------------------------- number formats
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 2) mtp_regs_proj_kernel(const StepAr
       __threadfence();
       for (int b = threadIdx.x; b < a.B; b += kThreads) {
         const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
-        a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-        if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
+        MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
+        if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k);
       }
       if (threadIdx.x == 0) atomicExch(a.lm_cnt, 0);
     }
@@ -380,8 +380,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       __threadfence();
       for (int b = ct; b < a.B; b += 256) {
         const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
-        a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-        if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
+        MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
+        if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k);
       }
       if (ct == 0) atomicExch(a.lm_cnt, 0);
     }

@@ -124,29 +124,31 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g));
 template <typename T, int KIND>
 __device__ __forceinline__ void epilogue(const StepArgs<T>& a, int b, int r0, int r1, float v0, float v1,
                                          unsigned long long& best) {
+  const long long nBH = (long long)a.B * a.H;
   if constexpr (KIND == EH_PROJ) {
-    a.x[(size_t)b * a.H + r0] = v0;
-    if (r1 >= 0) a.x[(size_t)b * a.H + r1] = v1;
+    MTP_STORE(a.err, a.x, (size_t)b * a.H + r0, nBH, v0);
+    if (r1 >= 0) MTP_STORE(a.err, a.x, (size_t)b * a.H + r1, nBH, v1);
   } else if constexpr (KIND == O_PROJ) {
-    a.h1[(size_t)b * a.H + r0] = a.x[(size_t)b * a.H + r0] + v0;
-    if (r1 >= 0) a.h1[(size_t)b * a.H + r1] = a.x[(size_t)b * a.H + r1] + v1;
+    MTP_STORE(a.err, a.h1, (size_t)b * a.H + r0, nBH, a.x[(size_t)b * a.H + r0] + v0);
+    if (r1 >= 0) MTP_STORE(a.err, a.h1, (size_t)b * a.H + r1, nBH, a.x[(size_t)b * a.H + r1] + v1);
   } else if constexpr (KIND == DOWN) {
     const float o0 = a.h1[(size_t)b * a.H + r0] + v0;
-    a.hid[(size_t)b * a.H + r0] = o0;
-    if (a.hidden_out && a.k == a.K) a.hidden_out[(size_t)b * a.H + r0] = o0;
+    MTP_STORE(a.err, a.hid, (size_t)b * a.H + r0, nBH, o0);
+    if (a.hidden_out && a.k == a.K) MTP_STORE(a.err, a.hidden_out, (size_t)b * a.H + r0, nBH, o0);
     if (r1 >= 0) {
       const float o1 = a.h1[(size_t)b * a.H + r1] + v1;
-      a.hid[(size_t)b * a.H + r1] = o1;
-      if (a.hidden_out && a.k == a.K) a.hidden_out[(size_t)b * a.H + r1] = o1;
+      MTP_STORE(a.err, a.hid, (size_t)b * a.H + r1, nBH, o1);
+      if (a.hidden_out && a.k == a.K) MTP_STORE(a.err, a.hidden_out, (size_t)b * a.H + r1, nBH, o1);
     }
   } else if constexpr (KIND == GATE_UP) {
-    a.act[(size_t)b * a.F + r0] = silu(v0) * v1;
+    MTP_STORE(a.err, a.act, (size_t)b * a.F + r0, (long long)a.B * a.F, silu(v0) * v1);
   } else if constexpr (KIND == LM_HEAD) {
-    float* lg = a.logits ? a.logits + ((size_t)b * a.K + (a.k - 1)) * a.V : nullptr;
-    if (lg) lg[r0] = v0;
+    const long long row = ((long long)b * a.K + (a.k - 1)) * a.V;
+    const long long nL = (long long)a.B * a.K * a.V;
+    if (a.logits) MTP_STORE(a.err, a.logits, row + r0, nL, v0);
     best = umax64(best, argmax_key(v0, (uint32_t)r0));
     if (r1 >= 0) {
-      if (lg) lg[r1] = v1;
+      if (a.logits) MTP_STORE(a.err, a.logits, row + r1, nL, v1);
       best = umax64(best, argmax_key(v1, (uint32_t)r1));
     }
   } else {  // QKV_ROPE
@@ -159,9 +161,9 @@ __device__ __forceinline__ void epilogue(const StepArgs<T>& a, int b, int r0, in
     }
     if (grp < a.n_q) {
       const float2 cs = a.rope[(size_t)pos * hp + i];
-      float* qb = a.q + (size_t)b * a.q_dim;
-      qb[r0] = v0 * cs.x - v1 * cs.y;
-      qb[r1] = v1 * cs.x + v0 * cs.y;
+      const long long nQ = (long long)a.B * a.q_dim;
+      MTP_STORE(a.err, a.q, (size_t)b * a.q_dim + r0, nQ, v0 * cs.x - v1 * cs.y);
+      MTP_STORE(a.err, a.q, (size_t)b * a.q_dim + r1, nQ, v1 * cs.x + v0 * cs.y);
       return;
     }
     if (__ldcg(a.req_bad + b) || a.pending[b] != a.k - 1) {
@@ -188,9 +190,10 @@ __device__ __forceinline__ void epilogue(const StepArgs<T>& a, int b, int r0, in
       pool = a.v_pool;
       g = grp - a.n_q - a.n_kv;
     }
-    T* dst = pool + (((size_t)blk * a.n_kv + g) * a.bs + off) * a.hd;
-    Elem<T>::store1(dst + i, o0);
-    Elem<T>::store1(dst + i + hp, o1);
+    const long long e = (((long long)blk * a.n_kv + g) * a.bs + off) * a.hd + i;
+    const long long nP = (long long)a.num_blocks * a.n_kv * a.bs * a.hd;
+    if (MTP_IN_BOUNDS(a.err, e, nP)) Elem<T>::store1(pool + e, o0);
+    if (MTP_IN_BOUNDS(a.err, e + hp, nP)) Elem<T>::store1(pool + e + hp, o1);
   }
 }
 

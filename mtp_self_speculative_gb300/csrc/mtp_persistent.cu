@@ -300,35 +300,36 @@ __device__ __forceinline__ PVec p_vec(const PArgs& a, int ph, int vec, int k, in
 __device__ __forceinline__ unsigned long long p_epilogue(const PArgs& a, int ph, int k, int b, int p, float v0,
                                                          float v1, unsigned bad_mask) {
   const size_t bh = (size_t)b * a.H;
+  const long long nBH = (long long)a.B * a.H;
   switch (ph) {
     case P_EH:
-      a.x[bh + 2 * p] = v0;
-      a.x[bh + 2 * p + 1] = v1;
+      MTP_STORE(a.err, a.x, bh + 2 * p, nBH, v0);
+      MTP_STORE(a.err, a.x, bh + 2 * p + 1, nBH, v1);
       return 0ull;
     case P_O:
-      a.h1[bh + 2 * p] = __ldcg(a.x + bh + 2 * p) + v0;
-      a.h1[bh + 2 * p + 1] = __ldcg(a.x + bh + 2 * p + 1) + v1;
+      MTP_STORE(a.err, a.h1, bh + 2 * p, nBH, __ldcg(a.x + bh + 2 * p) + v0);
+      MTP_STORE(a.err, a.h1, bh + 2 * p + 1, nBH, __ldcg(a.x + bh + 2 * p + 1) + v1);
       return 0ull;
     case P_GU:
-      a.act[(size_t)b * a.F + p] = p_silu(v0) * v1;
+      MTP_STORE(a.err, a.act, (size_t)b * a.F + p, (long long)a.B * a.F, p_silu(v0) * v1);
       return 0ull;
     case P_DOWN: {
       const float o0 = __ldcg(a.h1 + bh + 2 * p) + v0, o1 = __ldcg(a.h1 + bh + 2 * p + 1) + v1;
-      a.hid[bh + 2 * p] = o0;
-      a.hid[bh + 2 * p + 1] = o1;
+      MTP_STORE(a.err, a.hid, bh + 2 * p, nBH, o0);
+      MTP_STORE(a.err, a.hid, bh + 2 * p + 1, nBH, o1);
       if (a.hidden_out && k == a.K) {
-        a.hidden_out[bh + 2 * p] = o0;
-        a.hidden_out[bh + 2 * p + 1] = o1;
+        MTP_STORE(a.err, a.hidden_out, bh + 2 * p, nBH, o0);
+        MTP_STORE(a.err, a.hidden_out, bh + 2 * p + 1, nBH, o1);
       }
       return 0ull;
     }
     case P_LM: {
       const int r0 = 2 * p, r1 = 2 * p + 1;
-      float* lg = a.logits ? a.logits + ((size_t)b * a.K + (k - 1)) * a.V : nullptr;
-      if (lg) lg[r0] = v0;
+      const long long row = ((long long)b * a.K + (k - 1)) * a.V, nL = (long long)a.B * a.K * a.V;
+      if (a.logits) MTP_STORE(a.err, a.logits, row + r0, nL, v0);
       unsigned long long key = argmax_key(v0, (uint32_t)r0);
       if (r1 < a.V) {
-        if (lg) lg[r1] = v1;
+        if (a.logits) MTP_STORE(a.err, a.logits, row + r1, nL, v1);
         key = umax64(key, argmax_key(v1, (uint32_t)r1));
       }
       return key;
@@ -343,9 +344,9 @@ __device__ __forceinline__ unsigned long long p_epilogue(const PArgs& a, int ph,
       }
       const float2 cs = a.rope[(size_t)pos * 64 + i];
       if (grp < a.n_q) {
-        float* qb = a.q + (size_t)b * a.q_dim;
-        qb[r0] = v0 * cs.x - v1 * cs.y;
-        qb[r0 + 64] = v1 * cs.x + v0 * cs.y;
+        const long long nQ = (long long)a.B * a.q_dim;
+        MTP_STORE(a.err, a.q, (size_t)b * a.q_dim + r0, nQ, v0 * cs.x - v1 * cs.y);
+        MTP_STORE(a.err, a.q, (size_t)b * a.q_dim + r0 + 64, nQ, v1 * cs.x + v0 * cs.y);
         return 0ull;
       }
       if ((bad_mask >> b) & 1u) {
@@ -371,9 +372,10 @@ __device__ __forceinline__ unsigned long long p_epilogue(const PArgs& a, int ph,
         pool = a.v_pool;
         g = grp - a.n_q - a.n_kv;
       }
-      uint16_t* dst = pool + (((size_t)blk * a.n_kv + g) * 16 + off) * 128;
-      dst[i] = f32_to_bf16_rne(o0);
-      dst[i + 64] = f32_to_bf16_rne(o1);
+      const long long e = (((long long)blk * a.n_kv + g) * 16 + off) * 128 + i;
+      const long long nP = (long long)a.num_blocks * a.n_kv * 16 * 128;
+      MTP_STORE(a.err, pool, e, nP, f32_to_bf16_rne(o0));
+      MTP_STORE(a.err, pool, e + 64, nP, f32_to_bf16_rne(o1));
       return 0ull;
     }
   }
@@ -962,8 +964,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (!grid_sync(false)) return;
     if (cta == 0 && ct < a.B) {
       const unsigned long long key = __ldcg(a.keys + (size_t)(k - 1) * a.B + ct);
-      a.draft_ids[(size_t)ct * a.K + (k - 1)] = (int32_t)key_index(key);
-      if (!((s_bad >> ct) & 1u)) a.pending[ct] = k;
+      MTP_STORE(a.err, a.draft_ids, (size_t)ct * a.K + (k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
+      if (!((s_bad >> ct) & 1u)) MTP_STORE(a.err, a.pending, ct, a.B, k);
     }
   }
 }

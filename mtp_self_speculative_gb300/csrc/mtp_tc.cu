@@ -225,7 +225,8 @@ __device__ __forceinline__ void tc_pair_store_cs(const TcArgs& a, const QkvMeta*
                                                  float v0, float v1, float2 cs) {
   if (a.kind == TC_GU) {
     const int f = tile * 64 + i;
-    if (f < a.F) a.act_bf16[(size_t)b * a.F + f] = f32_to_bf16_rne(v0 / (1.0f + __expf(-v0)) * v1);
+    if (f < a.F)
+      MTP_STORE(a.err, a.act_bf16, (size_t)b * a.F + f, (long long)a.B * a.F, f32_to_bf16_rne(v0 / (1.0f + __expf(-v0)) * v1));
     return;
   }
   // TC_QKV: tile = head
@@ -233,9 +234,10 @@ __device__ __forceinline__ void tc_pair_store_cs(const TcArgs& a, const QkvMeta*
   const int pos = meta->pos[b];
   if (pos < 0) return;
   if (grp < a.n_q) {
-    float* qb = a.q + (size_t)b * a.q_dim + grp * 128;
-    qb[i] = v0 * cs.x - v1 * cs.y;
-    qb[i + 64] = v1 * cs.x + v0 * cs.y;
+    const size_t qo = (size_t)b * a.q_dim + grp * 128;
+    const long long nQ = (long long)a.B * a.q_dim;
+    MTP_STORE(a.err, a.q, qo + i, nQ, v0 * cs.x - v1 * cs.y);
+    MTP_STORE(a.err, a.q, qo + i + 64, nQ, v1 * cs.x + v0 * cs.y);
     return;
   }
   const long long kvoff = meta->kv[b];
@@ -252,9 +254,10 @@ __device__ __forceinline__ void tc_pair_store_cs(const TcArgs& a, const QkvMeta*
     pool = a.v_pool;
     g = grp - a.n_q - a.n_kv;
   }
-  uint16_t* dst = pool + kvoff + (size_t)g * a.bs * 128;
-  dst[i] = f32_to_bf16_rne(o0);
-  dst[i + 64] = f32_to_bf16_rne(o1);
+  const long long e = kvoff + (long long)g * a.bs * 128 + i;
+  const long long nP = (long long)a.num_blocks * a.n_kv * a.bs * 128;
+  MTP_STORE(a.err, pool, e, nP, f32_to_bf16_rne(o0));
+  MTP_STORE(a.err, pool, e + 64, nP, f32_to_bf16_rne(o1));
 }
 
 // Residual input of plain output row r for batch row b (x for O, h1 for
@@ -270,14 +273,15 @@ __device__ __forceinline__ float tc_plain_residual(const TcArgs& a, int r, int b
 __device__ __forceinline__ void tc_plain_store_res(const TcArgs& a, int r, int b, float v, float res) {
   if (r >= a.H) return;
   const size_t o = (size_t)b * a.H + r;
+  const long long nBH = (long long)a.B * a.H;
   if (a.kind == TC_EH) {
-    a.x[o] = v;
+    MTP_STORE(a.err, a.x, o, nBH, v);
   } else if (a.kind == TC_O) {
-    a.h1[o] = res + v;
+    MTP_STORE(a.err, a.h1, o, nBH, res + v);
   } else {
     const float hv = res + v;
-    a.hid[o] = hv;
-    if (a.hidden_out && a.k == a.K) a.hidden_out[o] = hv;
+    MTP_STORE(a.err, a.hid, o, nBH, hv);
+    if (a.hidden_out && a.k == a.K) MTP_STORE(a.err, a.hidden_out, o, nBH, hv);
   }
 }
 
@@ -299,7 +303,7 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
       const float y = (kind == TC_EH) ? v[j] : res[j] + v[j];
       if (c0 + j < a.B) {
         tc_plain_store_res(a, r, c0 + j, v[j], res[j]);
-        a.xn_out[(size_t)(c0 + j) * a.H + r] = f32_to_bf16_rne(y * wn);
+        MTP_STORE(a.err, a.xn_out, (size_t)(c0 + j) * a.H + r, (long long)a.B * a.H, f32_to_bf16_rne(y * wn));
       }
       const float q = warp_sum((c0 + j < a.B) ? y * y : 0.0f);
       if (e.lane == 0) e.xbuf[e.quarter * 16 + j] = q;
@@ -307,8 +311,8 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
     epi_bar();
     const int t = threadIdx.x - 64;
     if (t < 16 && c0 + t < a.B)
-      a.ssq[(size_t)e.tile * a.B + c0 + t] =
-          e.xbuf[t] + e.xbuf[16 + t] + e.xbuf[32 + t] + e.xbuf[48 + t];
+      MTP_STORE(a.err, a.ssq, (size_t)e.tile * a.B + c0 + t, (long long)(a.H / 128) * a.B,
+                e.xbuf[t] + e.xbuf[16 + t] + e.xbuf[32 + t] + e.xbuf[48 + t]);
     epi_bar();
     return;
   }
@@ -320,7 +324,8 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
       const int b = c0 + j;
       if (b >= a.B) continue;  // uniform across the warp
       const float z = v[j] * e.rms[b];
-      if (a.logits && row_ok) a.logits[((size_t)b * a.K + (a.k - 1)) * a.V + r] = z;
+      if (a.logits && row_ok)
+        MTP_STORE(a.err, a.logits, ((size_t)b * a.K + (a.k - 1)) * a.V + r, (long long)a.B * a.K * a.V, z);
       const uint32_t ord = row_ok ? ordered_bits(z) : 0u;
       const uint32_t mx = __reduce_max_sync(0xffffffffu, ord);
       const uint32_t bal = __ballot_sync(0xffffffffu, ord == mx);
@@ -382,6 +387,7 @@ __device__ __forceinline__ float4 tc_plain_residual4(const TcArgs& a, int r, int
 __device__ __forceinline__ float tc_plain_store4(const TcArgs& a, int r, int b, float4 v, float4 res) {
   const size_t o = (size_t)b * a.H + r;
   const float4 t = (a.kind == TC_EH) ? v : make_float4(res.x + v.x, res.y + v.y, res.z + v.z, res.w + v.w);
+  if (!MTP_IN_BOUNDS(a.err, (long long)o + 3, (long long)a.B * a.H)) return 0.0f;
   if (a.kind == TC_EH) {
     *reinterpret_cast<float4*>(a.x + o) = t;
   } else if (a.kind == TC_O) {
@@ -627,8 +633,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
         __threadfence();
         for (int b = epi_tid; b < a.B; b += kTcEpiThreads) {
           const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
-          a.draft_ids[(size_t)b * a.K + (a.k - 1)] = (int32_t)key_index(key);
-          if (!__ldcg(a.req_bad + b)) a.pending[b] = a.k;
+          MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
+          if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k);
         }
         if (epi_tid == 0) atomicExch(a.lm_cnt, 0);
       }
@@ -688,7 +694,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
           // tile's partial for the next RMSNorm
           const int r = tile * 128 + mq;
           const float q = warp_sum(tc_plain_store4(a, r, c, v0, tc_plain_residual4(a, r, c)));
-          if (lane == 0) a.ssq[(size_t)tile * a.B + c] = q;
+          if (lane == 0) MTP_STORE(a.err, a.ssq, (size_t)tile * a.B + c, (long long)(a.H / 128) * a.B, q);
         }
       }
     }

@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const VerifyA
       const long long e = i < head_elems ? i : tail_elem0 + (i - head_elems);
       const float x = Elem<T>::load1(a.logits + e);
       const int r = (int)(e / a.V);
-      if (x == x) atomicMax(a.keys + r, argmax_key(x, (uint32_t)(e - (long long)r * a.V)));
+      if (x == x && MTP_IN_BOUNDS(a.err, r, a.num_rows))
+        atomicMax(a.keys + r, argmax_key(x, (uint32_t)(e - (long long)r * a.V)));
     }
   }
   const int cw = warp - 1;
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const VerifyA
       const long long r_end = min(e0 + cnt, (long long)(r + 1) * a.V);
       const unsigned long long key =
           segment_key<T>(sp + (e - e0), (int)(r_end - e), (int)(e - (long long)r * a.V), lane);
-      if (lane == 0 && key) atomicMax(a.keys + r, key);
+      if (lane == 0 && key && MTP_IN_BOUNDS(a.err, r, a.num_rows)) atomicMax(a.keys + r, key);
       e = r_end;
     }
     __syncwarp();
@@ -262,8 +263,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const VerifyA
     const bool bad = K_b < 0 || K_b > a.max_k || K_b > a.drafts_stride || r1 - r0 != K_b + 1 || r0 < 0 ||
                      r0 + K_b + 1 > a.num_rows;
     if (bad) {
-      a.accepted[b] = -1;
-      a.bonus[b] = -1;
+      MTP_STORE(a.err, a.accepted, b, a.B, -1);
+      MTP_STORE(a.err, a.bonus, b, a.B, -1);
       set_error(a.err, MTP_ERR_DEVICE_ARGS);
       continue;
     }
@@ -292,8 +293,8 @@ __global__ void __launch_bounds__(kVerifyThreads, 1) verify_kernel(const VerifyA
         }
       }
     }
-    a.accepted[b] = acc;
-    a.bonus[b] = bonus;
+    MTP_STORE(a.err, a.accepted, b, a.B, acc);
+    MTP_STORE(a.err, a.bonus, b, a.B, bonus);
   }
   verify_cons_bar();
   for (int r = ct; r < a.num_rows; r += kWalkThreads) a.keys[r] = 0ull;
@@ -390,8 +391,9 @@ __global__ void __launch_bounds__(256) kv_edit_kernel(const KvEditArgs<T> a) {
       continue;
     }
     T* pool = which ? a.v_pool : a.k_pool;
-    uint4* dst = reinterpret_cast<uint4*>(pool + (((size_t)blk * a.n_kv + g) * a.bs + off) * a.hd) + v;
-    *dst = make_uint4(0, 0, 0, 0);
+    const long long e = (((long long)blk * a.n_kv + g) * a.bs + off) * a.hd + (long long)v * (16 / sizeof(T));
+    if (!MTP_IN_BOUNDS(a.err, e + (16 / sizeof(T)) - 1, (long long)a.num_blocks * a.n_kv * a.bs * a.hd)) continue;
+    *reinterpret_cast<uint4*>(pool + e) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
   if (threadIdx.x == 0) {

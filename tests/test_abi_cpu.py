@@ -135,3 +135,8 @@ def test_stream_read_rejects_bad_arguments(lib):
     assert lib.mtp_stream_read(None, 16, 0, None) == _lib.MTP_ERR_INVALID
     assert lib.mtp_stream_read(None, 16, 4008, None) == _lib.MTP_ERR_INVALID
     assert lib.mtp_stream_read(None, 24, 4096, None) == _lib.MTP_ERR_INVALID
+
+
+def test_bounds_selftest_needs_a_context(lib):
+    from mtp_self_speculative_gb300 import _lib
+    assert lib.mtp_selftest_bounds(None, None) == _lib.MTP_ERR_INVALID
