@@ -48,7 +48,7 @@ LM_TRAFFIC = {
 }
 # The same for one verify launch (profiles/verify_rollback_b64.md).
 VERIFY_TRAFFIC = {
-    "verify_rollback_b64": 111302144 + 3310848,
+    "verify_rollback_b64": 111259136 + 3191296,
 }
 # The same for one launch of the persistent draft kernel (all K steps); null until captured.
 PERSISTENT_TRAFFIC = {}
