@@ -370,8 +370,8 @@ def run_ours(args, rank, world, local_rank):
     copy_gbs = 2 * nbytes / (min(copies) * 1e-3) / 1e9
     del src, dst
     kb0 = kernel_bytes(cfg, wl.lens, K, fmt=args.weights)
-    read_floor = read_floor_us({"attention": kb0["attention"], "verify": kb0["verify"],
-                                "lm_head": kb0["lm_head"]}, stream)
+    read_floor = read_floor_us({n: kb0[n] for n in ("eh_proj", "qkv_rope", "attention", "o_proj", "gate_up", "down",
+                                                    "lm_head", "verify")}, stream)
 
     for _ in range(args.warmup):
         wl.step()
@@ -665,7 +665,9 @@ def measure_verify_workload(cfg: synth.MTPShape, local_rank: int, calls: int, pe
     ver_bytes = int(vi.row_offsets[-1]) * cfg.vocab * cfg.elem_bytes
     gbs = ver_bytes / (t_ver * 1e-3) / 1e9
     M.mtp_destroy(ctx)
-    return {"batch": B, "k_range": [int(vi.num_drafts.min()), int(vi.num_drafts.max())],
+    del logits, flush
+    floor = read_floor_us({"verify": ver_bytes}, stream)["verify"]
+    return {"batch": B, "k_range": [int(vi.num_drafts.min()), int(vi.num_drafts.max())], "read_floor": floor,
             "verify_rows": int(vi.row_offsets[-1]), "calls_s": 1e3 / (t_ver + t_com), "verify_ms": t_ver,
             "commit_ms": t_com, "verify_bytes": ver_bytes, "verify_gbs": gbs, "verify_hbm_frac_of_measured": gbs / peak,
             "l2": "flushed between calls (256 MB read outside the events)", "timed_calls": calls, "clocks": clocks}
@@ -1004,6 +1006,7 @@ def run_verify_workload(args, cfg, rank, world, local_rank):
                      "frac": ver_gbs / peak, "peak_source": peak_kind + " hbm_gbs",
                      "traffic": VERIFY_TRAFFIC.get(cfg.name), "bytes_per_launch": ver_bytes},
         "commit_bytes": com_bytes,
+        "read_floor": read_floor_us({"verify": ver_bytes}, stream)["verify"],
         "e2e": {"value": 1.0 / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": ver_bytes,
                 "d2h_bytes_per_step": 2 * B * 4},
         "gpu_launches": launches,
