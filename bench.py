@@ -673,11 +673,39 @@ def measure_verify_workload(cfg: synth.MTPShape, local_rank: int, calls: int, pe
             "l2": "flushed between calls (256 MB read outside the events)", "timed_calls": calls, "clocks": clocks}
 
 
+def measure_small_batch_lm_head(local_rank: int, steps: int = 6) -> dict:
+    """LM head + argmax of the Qwen3-8B-shaped head at 1, 2 and 4 requests
+    (tree expansions and small batches): mean live duration per launch from
+    the per-kernel events, its fraction of the measured copy bandwidth, and
+    its time relative to the 1-request launch."""
+    import dataclasses
+    import torch
+    import mtp_self_speculative_gb300 as M
+    out = {}
+    for B in (1, 2, 4):
+        cfg = dataclasses.replace(synth.QWEN3_8B_B1, name="qwen3_8b_mtp_b%d" % B, batch=B)
+        wl = Workload(cfg, cfg.K)
+        for _ in range(3):
+            wl.step()
+        torch.cuda.synchronize()
+        lm = kernel_breakdown(wl, steps)["lm_head"]
+        assert M.mtp_get_device_error(wl.ctx) == 0
+        out["b%d" % B] = {"us": lm["us"], "bytes": lm["bytes"], "frac": lm["frac"]}
+        M.mtp_destroy(wl.ctx)
+        del wl
+        torch.cuda.empty_cache()
+    for k in ("b2", "b4"):
+        out[k]["vs_b1"] = round(out[k]["us"] / out["b1"]["us"], 3)
+    out["note"] = "per-kernel CUDA events inside full steps (L2 holds no weights: 1.2 GB per launch)"
+    return out
+
+
 def measure_other_workloads(args, local_rank: int) -> dict:
     """The continuous-batching, large-batch and verify configurations, each
-    set up, measured at a few steps and freed in turn."""
+    set up, measured at a few steps and freed in turn, and the LM head at
+    1, 2 and 4 requests."""
     peak = float(measured_peaks()[0]["hbm_gbs"])
-    out = {}
+    out = {"lm_head_small_batch": measure_small_batch_lm_head(local_rank)}
     for cfg, steps in ((synth.QWEN3_8B_CB32, 20), (synth.QWEN3_32B_B128, 6)):
         out[cfg.name] = measure_draft_workload(cfg, local_rank, steps, 3, peak)
     out[synth.VERIFY_B64.name] = measure_verify_workload(synth.VERIFY_B64, local_rank, 50, peak)

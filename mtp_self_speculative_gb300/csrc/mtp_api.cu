@@ -129,6 +129,10 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // overrides the default for tuning.
   ctx->gemv_stream_mask = 0x3F;
   if (const char* env = getenv("MTP_GEMV_STREAM")) ctx->gemv_stream_mask = (int)strtol(env, nullptr, 0);
+  // LM head of 2..4 requests on the tensor cores; MTP_LM_ROWS=0 keeps the
+  // streamed GEMV for it (comparison).
+  ctx->lm_rows = 1;
+  if (const char* env = getenv("MTP_LM_ROWS")) ctx->lm_rows = (int)strtol(env, nullptr, 0) != 0;
   // Shared-memory budget of the streamed kernel per kind, in KB;
   // MTP_GEMV_BUDGET ("eh,qkv,o,gu,down,lm") overrides it for tuning.
   for (int i = 0; i < 6; ++i) ctx->gemv_budget_kb[i] = 220;

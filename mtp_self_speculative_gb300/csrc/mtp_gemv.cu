@@ -407,6 +407,14 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
                   : (KIND == DOWN) ? MTP_KERNEL_DOWN : MTP_KERNEL_LM_HEAD;
   cudaError_t e;
   prof_before(ctx, kid, s);
+  if constexpr (KIND == LM_HEAD && sizeof(T) == 2) {
+    if (lm_rows_supported(ctx, a.B)) {
+      e = launch_lm_rows(ctx, s, reinterpret_cast<const StepArgs<uint16_t>&>(a));
+      prof_after(ctx, kid, s);
+      ctx->launches++;
+      return e;
+    }
+  }
   // TMA-streamed variant for B <= 4
   {
     const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;

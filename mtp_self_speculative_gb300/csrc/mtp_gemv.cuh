@@ -47,6 +47,11 @@ struct StepArgs {
   float lm_sigma;
 };
 
+// LM head of 2..4 requests through mma.sync on whole staged rows
+// (csrc/mtp_lm_rows.cu).
+bool lm_rows_supported(const mtp_ctx* ctx, int B);
+cudaError_t launch_lm_rows(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uint16_t>& a);
+
 // Source matrices of the quantized projections (canonical quantized copies).
 enum QMat { QM_EH = 0, QM_Q = 1, QM_K = 2, QM_V = 3, QM_O = 4, QM_GATE = 5, QM_UP = 6, QM_DOWN = 7 };
 
