@@ -328,3 +328,4 @@ def test_long_context_small_batch_split_combine_bf16(n_q):
     case = Case(cfg, norm="random", lens=[3001, 2500], persistent_max_batch=-1)
     _, _, ids, logits = check_forced(case, [0, 1], LOGIT_TOL)
     check_free(case, [0, 1], ids, logits, LOGIT_TOL)
+
