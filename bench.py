@@ -673,14 +673,15 @@ def measure_verify_workload(cfg: synth.MTPShape, local_rank: int, calls: int, pe
             "l2": "flushed between calls (256 MB read outside the events)", "timed_calls": calls, "clocks": clocks}
 
 
-def measure_small_batch_lm_head(local_rank: int, steps: int = 6) -> dict:
-    """LM head + argmax of the Qwen3-8B-shaped head at 1, 2 and 4 requests
-    (tree expansions and small batches): mean live duration per launch from
-    the per-kernel events, its fraction of the measured copy bandwidth, and
-    its time relative to the 1-request launch."""
+def measure_small_batch(local_rank: int, steps: int = 6) -> dict:
+    """The Qwen3-8B-shaped head at 1, 2 and 4 requests (tree expansions and
+    small batches): draft-step time and HBM fraction, and every kernel's mean
+    live duration per launch from the per-kernel events, with its time
+    relative to the 1-request launch."""
     import dataclasses
     import torch
     import mtp_self_speculative_gb300 as M
+    peak = float(measured_peaks()[0]["hbm_gbs"])
     out = {}
     for B in (1, 2, 4):
         cfg = dataclasses.replace(synth.QWEN3_8B_B1, name="qwen3_8b_mtp_b%d" % B, batch=B)
@@ -688,24 +689,36 @@ def measure_small_batch_lm_head(local_rank: int, steps: int = 6) -> dict:
         for _ in range(3):
             wl.step()
         torch.cuda.synchronize()
-        lm = kernel_breakdown(wl, steps)["lm_head"]
+        stream = torch.cuda.current_stream()
+
+        def draft_only():
+            wl.draft()
+            M.mtp_kv_rollback(wl.ctx, wl.kv)
+        ms_draft = timed_steps(draft_only, steps * 4, stream)
+        kernels = kernel_breakdown(wl, steps)
         assert M.mtp_get_device_error(wl.ctx) == 0
-        out["b%d" % B] = {"us": lm["us"], "bytes": lm["bytes"], "frac": lm["frac"]}
+        sb = step_bytes(cfg, wl.lens, cfg.K)
+        out["b%d" % B] = {
+            "ms_per_draft_step": round(ms_draft / cfg.K, 4),
+            "draft_hbm_frac_of_measured": round(sb["draft"] / (ms_draft * 1e-3) / 1e9 / peak, 4),
+            "kernels_us": {k: v["us"] for k, v in kernels.items() if k not in ("verify", "kv_edit")},
+            "lm_head_frac": kernels["lm_head"]["frac"]}
         M.mtp_destroy(wl.ctx)
         del wl
         torch.cuda.empty_cache()
     for k in ("b2", "b4"):
-        out[k]["vs_b1"] = round(out[k]["us"] / out["b1"]["us"], 3)
-    out["note"] = "per-kernel CUDA events inside full steps (L2 holds no weights: 1.2 GB per launch)"
+        out[k]["vs_b1"] = {n: round(us / out["b1"]["kernels_us"][n], 3)
+                           for n, us in out[k]["kernels_us"].items() if out["b1"]["kernels_us"].get(n)}
+    out["note"] = "per-kernel CUDA events inside full steps (L2 holds no weights: 1.7 GB per draft step)"
     return out
 
 
 def measure_other_workloads(args, local_rank: int) -> dict:
     """The continuous-batching, large-batch and verify configurations, each
-    set up, measured at a few steps and freed in turn, and the LM head at
-    1, 2 and 4 requests."""
+    set up, measured at a few steps and freed in turn, and the Qwen3-8B
+    shape at 1, 2 and 4 requests."""
     peak = float(measured_peaks()[0]["hbm_gbs"])
-    out = {"lm_head_small_batch": measure_small_batch_lm_head(local_rank)}
+    out = {"small_batch": measure_small_batch(local_rank)}
     for cfg, steps in ((synth.QWEN3_8B_CB32, 20), (synth.QWEN3_32B_B128, 6)):
         out[cfg.name] = measure_draft_workload(cfg, local_rank, steps, 3, peak)
     out[synth.VERIFY_B64.name] = measure_verify_workload(synth.VERIFY_B64, local_rank, 50, peak)

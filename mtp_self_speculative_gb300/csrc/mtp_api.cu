@@ -133,6 +133,10 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // streamed GEMV for it (comparison).
   ctx->lm_rows = 1;
   if (const char* env = getenv("MTP_LM_ROWS")) ctx->lm_rows = (int)strtol(env, nullptr, 0) != 0;
+  // the short projections of 2..4 requests likewise; MTP_ROWS_PROJ=0 keeps
+  // the streamed GEMV for them (comparison)
+  ctx->rows_proj = 1;
+  if (const char* env = getenv("MTP_ROWS_PROJ")) ctx->rows_proj = (int)strtol(env, nullptr, 0) != 0;
   // Shared-memory budget of the streamed kernel per kind, in KB;
   // MTP_GEMV_BUDGET ("eh,qkv,o,gu,down,lm") overrides it for tuning.
   for (int i = 0; i < 6; ++i) ctx->gemv_budget_kb[i] = 220;

@@ -415,6 +415,14 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
       return e;
     }
   }
+  if constexpr (KIND != LM_HEAD && sizeof(T) == 2) {
+    if (rows_proj_supported(ctx, KIND, a.B)) {
+      e = launch_rows_proj(ctx, s, KIND, reinterpret_cast<const StepArgs<uint16_t>&>(a));
+      prof_after(ctx, kid, s);
+      ctx->launches++;
+      return e;
+    }
+  }
   // TMA-streamed variant for B <= 4
   {
     const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;

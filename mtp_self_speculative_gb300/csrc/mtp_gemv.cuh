@@ -52,6 +52,11 @@ struct StepArgs {
 bool lm_rows_supported(const mtp_ctx* ctx, int B);
 cudaError_t launch_lm_rows(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uint16_t>& a);
 
+// The short projections of 2..4 requests through mma.sync on staged row
+// chunks (csrc/mtp_rows_proj.cu).
+bool rows_proj_supported(const mtp_ctx* ctx, int kind, int B);
+cudaError_t launch_rows_proj(mtp_ctx* ctx, cudaStream_t s, int kind, const StepArgs<uint16_t>& a);
+
 // Source matrices of the quantized projections (canonical quantized copies).
 enum QMat { QM_EH = 0, QM_Q = 1, QM_K = 2, QM_V = 3, QM_O = 4, QM_GATE = 5, QM_UP = 6, QM_DOWN = 7 };
 

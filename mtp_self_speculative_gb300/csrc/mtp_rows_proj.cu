@@ -1,0 +1,376 @@
+// The short projections of the draft step (eh_proj, QKV + rotary, O-proj,
+// gate/up, down) for 2 to 4 requests per call on the tensor cores
+// ("MTP (Multi-Token Prediction)", "Architecture": the MTP module is one
+// decoder layer -- RMSNorm, attention, SwiGLU MLP -- behind the projection of
+// the concatenated, normalised hidden state and token embedding).
+//
+// At 2-4 requests the streamed GEMV reads every staged activation once per
+// request for each weight vector and is bound by shared memory.  This kernel
+// keeps the GEMV's data movement -- whole weight rows by bulk copies -- and
+// runs the arithmetic on mma.sync m16n8k16 with the weights as the B operand:
+// a unit is 8 weight rows (N = 8), the requests are rows of the A operand
+// (M = 16, rows NB..15 zero).
+//
+// One CTA per SM owns a balanced range of the kind's row pairs (the pairs of
+// the epilogues: rotary halves, gate and up rows, neighbouring rows; single
+// rows for eh_proj and down) and takes them 8 rows at a time; the last unit
+// of a range may hold fewer rows, so every CTA streams about the same bytes.
+// Rows are wide (2H for eh_proj, F for down), so a unit streams in chunks of
+// kc columns: a stage holds the chunk of all 8 rows, one bulk copy per row,
+// rows padded by 16 bytes so that the 8 rows' B-fragment words fall in
+// distinct banks.  Warp 0 fills a ring of such stages; every consumer warp
+// takes its eighth of each chunk's columns, reads the A fragments of those
+// columns from the staged input and the B fragments from the stage, and
+// releases the stage (the empty barrier counts the 8 warps).  A unit's
+// partial sums (per request and row) stay in registers over its chunks and
+// meet in a double-buffered shared area after one consumer barrier; 8 x NB
+// threads add them in warp order (deterministic) and run the kind's
+// epilogue.
+//
+// The input is staged once per CTA as bf16 x * w (the RMSNorm weight; no
+// weight for O-proj and down) with each request's sum of squares; the RMS
+// factor 1 / sqrt(mean(x^2) + eps) multiplies the finished sums in the
+// epilogue (eh_proj: one factor per half, the hidden and the embedding
+// halves accumulated apart), so the main loop starts after a single pass
+// over the input.  The rounding of the activations to bf16 is the operand
+// rounding the batched tensor-core path makes.
+#include "mtp_common.cuh"
+#include "mtp_attn_mma.cuh"
+#include "mtp_gemv.cuh"
+
+namespace mtp {
+
+constexpr int kRpCons = 8;
+constexpr int kRpThreads = 32 * (kRpCons + 1);
+constexpr int kRpMaxStages = 16;
+constexpr uint32_t kRpWaitLimit = 1u << 24;
+
+__device__ __forceinline__ void rp_cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Pairs (epilogue units) per 8-row unit.
+__host__ __device__ constexpr int rp_pairs_per_unit(int kind) { return gemv_unit_rows(kind) == 2 ? 4 : 8; }
+
+// Stage rows [i8 * 8, i8 * 8 + 8) of one input vector of request b: y = x * w
+// (w = nullptr: y = x) rounded to bf16 into dst; returns the sum of x^2.
+template <typename S>
+__device__ __forceinline__ float rp_stage8(unsigned char* dst, const S* src, const uint16_t* w) {
+  float x[8], wv[8];
+  load8_row<uint16_t, S>(src, x);
+  if (w) load8_row<uint16_t, uint16_t>(w, wv);
+  float ss = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ss = fmaf(x[e], x[e], ss);
+    if (w) x[e] *= wv[e];
+  }
+  *reinterpret_cast<uint4*>(dst) =
+      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+  return ss;
+}
+
+template <int KIND, int NB>
+__global__ void __launch_bounds__(kRpThreads, 1)
+    mtp_rows_proj_kernel(const StepArgs<uint16_t> a, int stages, int kc) {
+  constexpr int UPP = rp_pairs_per_unit(KIND);
+  constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
+  constexpr int NH = (KIND == EH_PROJ) ? 2 : 1;  // accumulated halves (RMS factors per request)
+  extern __shared__ __align__(128) unsigned char rps[];
+  __shared__ __align__(8) uint64_t full_bar[kRpMaxStages], empty_bar[kRpMaxStages];
+  __shared__ float red[2][NH][kRpCons][NB][8];
+  __shared__ float ssq[kRpCons][2 * NB];
+  __shared__ float srs[2 * NB];
+  __shared__ int s_abort[2];
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = gemv_cols(a, KIND);
+  const int P = gemv_pairs(a, KIND);
+  const int p0 = (int)(((long long)blockIdx.x * P) / gridDim.x);
+  const int p1 = (int)(((long long)(blockIdx.x + 1) * P) / gridDim.x);
+  const int nunits = (p1 - p0 + UPP - 1) / UPP;
+  const int nch = C / kc;
+  const uint32_t chunk_bytes = (uint32_t)kc * 2;
+  const uint32_t rp = chunk_bytes + 16;        // row pitch in a stage
+  const uint32_t stage_bytes = 8 * rp;
+  const uint32_t ap = (uint32_t)C * 2 + 16;    // row pitch of the staged input
+  unsigned char* xa = rps + (size_t)stages * stage_bytes;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kRpCons);
+    }
+    s_abort[0] = s_abort[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // weights are read once per step
+      int it = 0;
+      for (int u = 0; u < nunits; ++u) {
+        // rows of the unit: slot 2j / 2j + 1 = pair j's rows (pair kinds), slot j = pair j's row
+        const uint16_t* src[8];
+        int nrows = 0;
+        for (int j = 0; j < UPP; ++j) {
+          const int p = p0 + u * UPP + j;
+          int r0, r1;
+          const uint16_t *w0, *w1;
+          if (p < p1) pair_rows<uint16_t, KIND>(a, p, C, r0, r1, w0, w1);
+          else { w0 = w1 = nullptr; }
+          if (UPP == 4) {
+            src[2 * j] = w0;
+            src[2 * j + 1] = w1;
+          } else {
+            src[j] = w0;
+          }
+        }
+        for (int r = 0; r < 8; ++r) nrows += (src[r] != nullptr);
+        for (int c = 0; c < nch; ++c, ++it) {
+          const int s = it % stages;
+          if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)(((it / stages) & 1) ^ 1), kRpWaitLimit)) {
+            set_error(a.err, MTP_ERR_TIMEOUT);
+            return;
+          }
+          unsigned char* dst = rps + (size_t)s * stage_bytes;
+          mbar_expect_tx(&full_bar[s], (uint32_t)nrows * chunk_bytes);
+          for (int r = 0; r < 8; ++r)
+            if (src[r]) bulk_g2s_hint(dst + (size_t)r * rp, src[r] + (size_t)c * kc, chunk_bytes, &full_bar[s], pol);
+        }
+      }
+    }
+    return;
+  }
+
+  // consumers: stage x * w (bf16) of every request, sums of squares per
+  // (request, half)
+  pdl_wait();
+  const int ct = threadIdx.x - 32, cw = warp - 1;
+  const int nb = a.B;
+  if (KIND == EH_PROJ && a.k == 1 && blockIdx.x == 0)
+    for (int b = ct; b < a.B; b += 32 * kRpCons) a.req_bad[b] = (a.pending[b] != 0);
+  {
+    float ss[2 * NB];
+#pragma unroll
+    for (int i = 0; i < 2 * NB; ++i) ss[i] = 0.0f;
+    const int nv = a.H >> 3;  // 8-value vectors per H-wide input
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      if (b < nb) {
+        unsigned char* row = xa + (size_t)b * ap;
+        if constexpr (KIND == EH_PROJ) {
+          int id = 0;
+          if (a.k > 1) {
+            id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+            if (id < 0 || id >= a.V) {
+              if (ct == 0) set_error(a.err, MTP_ERR_DEVICE_ARGS);
+              id = 0;
+            }
+          }
+          for (int i = ct; i < nv; i += 32 * kRpCons) {
+            if (a.k == 1) {
+              ss[2 * b] += rp_stage8<uint16_t>(row + (size_t)i * 16, a.hidden_in + (size_t)b * a.H + 8 * i,
+                                               a.w_norm_h + 8 * i);
+              ss[2 * b + 1] += rp_stage8<uint16_t>(row + (size_t)(a.H + 8 * i) * 2,
+                                                   a.embeds_in + (size_t)b * a.H + 8 * i, a.w_norm_e + 8 * i);
+            } else {
+              ss[2 * b] += rp_stage8<float>(row + (size_t)i * 16, a.hid + (size_t)b * a.H + 8 * i, a.w_norm_h + 8 * i);
+              ss[2 * b + 1] += rp_stage8<uint16_t>(row + (size_t)(a.H + 8 * i) * 2, a.embed + (size_t)id * a.H + 8 * i,
+                                                   a.w_norm_e + 8 * i);
+            }
+          }
+        } else {
+          const float* src = (KIND == QKV_ROPE) ? a.x : (KIND == O_PROJ) ? a.attn : (KIND == GATE_UP) ? a.h1 : a.act;
+          const uint16_t* w = (KIND == QKV_ROPE) ? a.w_norm_in : (KIND == GATE_UP) ? a.w_norm_post : nullptr;
+          for (int i = ct; i < (C >> 3); i += 32 * kRpCons)
+            ss[2 * b] += rp_stage8<float>(row + (size_t)i * 16, src + (size_t)b * C + 8 * i, w ? w + 8 * i : nullptr);
+        }
+      }
+    }
+    if constexpr (kNorm) {
+#pragma unroll
+      for (int i = 0; i < 2 * NB; ++i) {
+        const float t = warp_sum(ss[i]);
+        if (lane == 0) ssq[cw][i] = t;
+      }
+    }
+    rp_cons_bar();
+    if (kNorm && ct < 2 * nb) {
+      float t = 0.0f;
+      for (int w = 0; w < kRpCons; ++w) t += ssq[w][ct];
+      srs[ct] = rsqrtf(t / (float)a.H + a.eps);
+    }
+    // srs is read in the epilogues, after the first unit's barrier
+  }
+
+  const int gi = lane >> 2, ti = lane & 3;
+  const int kw = kc / kRpCons;                 // this warp's columns of a chunk
+  const int nks = kw / 16;
+  const bool real = gi < nb;
+  const unsigned char* xrow = xa + (size_t)(real ? gi : 0) * ap;
+  // thread ct < 8 NB sums request ct / 8, row slot ct % 8 of every unit
+  const int my_b = ct >> 3, my_r = ct & 7;
+  unsigned long long best_unused = 0ull;
+  int it = 0;
+  bool failed = false;
+  int u = 0;
+  for (; u < nunits; ++u) {
+    const int buf = u & 1;
+    float acc[NH][4];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
+    for (int c = 0; c < nch; ++c, ++it) {
+      const int s = it % stages;
+      if (!failed &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], (uint32_t)((it / stages) & 1), kRpWaitLimit))) {
+        failed = true;
+        if (lane == 0) s_abort[buf] = 1;
+      }
+      if (failed) continue;
+      const int col0 = c * kc + cw * kw;       // first column of this warp's slice
+      const unsigned char* bp = rps + (size_t)s * stage_bytes + (size_t)gi * rp + (size_t)(cw * kw + 2 * ti) * 2;
+      const unsigned char* apn = xrow + (size_t)(col0 + 2 * ti) * 2;
+      const int h = (KIND == EH_PROJ && col0 >= a.H) ? 1 : 0;
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+      for (int j = 0; j < nks; ++j) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp + 32 * j);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 16);
+        uint32_t af[4] = {0u, 0u, 0u, 0u};
+        if (real) {
+          af[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * j);
+          af[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 16);
+        }
+        mma_bf16(d, af, b0, b1);
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[s])) : "memory");
+      if (NH == 2 && h) {
+        acc[NH - 1][0] += d[0];
+        acc[NH - 1][1] += d[1];
+      } else {
+        acc[0][0] += d[0];
+        acc[0][1] += d[1];
+      }
+    }
+    // d[0], d[1]: request gi, row slots 2 ti and 2 ti + 1 of the unit
+    if (!failed && real) {
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) {
+        red[buf][hh][cw][gi][2 * ti] = acc[hh][0];
+        red[buf][hh][cw][gi][2 * ti + 1] = acc[hh][1];
+      }
+    }
+    rp_cons_bar();
+    if (s_abort[buf]) break;
+    if (ct < 32) {
+      const bool mine = my_b < nb;  // nb <= NB, so red is indexed within bounds
+      float v = 0.0f;
+      if (mine) {
+        float z[NH];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          z[hh] = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kRpCons; ++w) z[hh] += red[buf][hh][w][my_b][my_r];
+        }
+        if constexpr (KIND == EH_PROJ) v = z[0] * srs[2 * my_b] + z[NH - 1] * srs[2 * my_b + 1];
+        else if constexpr (kNorm) v = z[0] * srs[2 * my_b];
+        else v = z[0];
+      }
+      // pair kinds: the even slot's thread runs the pair's epilogue with its
+      // odd neighbour's value; single-row kinds: every slot is one row
+      const float vn = __shfl_down_sync(0xffffffffu, v, 1);
+      const int j = (UPP == 4) ? (my_r >> 1) : my_r;
+      const int p = p0 + u * UPP + j;
+      if (mine && p < p1 && (UPP == 8 || (my_r & 1) == 0)) {
+        int r0, r1;
+        const uint16_t *w0, *w1;
+        pair_rows<uint16_t, KIND>(a, p, C, r0, r1, w0, w1);
+        epilogue<uint16_t, KIND>(a, my_b, r0, r1, v, (UPP == 4) ? vn : 0.0f, best_unused);
+      }
+    }
+  }
+  if (u < nunits) {
+    if (ct == 0) set_error(a.err, MTP_ERR_TIMEOUT);
+    // copies still in flight into the ring get a bounded chance to land
+    if (ct == 0)
+      for (int j = 0; j < stages; ++j)
+        mbar_wait_bounded(&full_bar[(it + j) % stages], (uint32_t)(((it + j) / stages) & 1), kRpWaitLimit);
+  }
+}
+
+// Columns per chunk: the largest divisor of C (a multiple of 128 columns, at
+// most 4096; for eh_proj a divisor of H, so that a chunk lies in one half)
+// whose stages leave room for at least four in the shared memory left by the
+// staged input.
+static bool rows_plan(const mtp_ctx* ctx, int kind, int C, int H, int nb, int* stages, int* kc) {
+  const size_t budget = 220 * 1024;
+  const size_t xa = (size_t)nb * ((size_t)C * 2 + 16);
+  if (xa >= budget) return false;
+  const size_t avail = budget - xa;
+  for (int k = 4096; k >= 128; k >>= 1) {
+    if (C % k || (kind == EH_PROJ && H % k)) continue;
+    const size_t st = (size_t)8 * ((size_t)k * 2 + 16);
+    int n = (int)(avail / st);
+    if (n > kRpMaxStages) n = kRpMaxStages;
+    if (n >= 4) {
+      *stages = n;
+      *kc = k;
+      return true;
+    }
+  }
+  (void)ctx;
+  return false;
+}
+
+static int rows_cols(const mtp_ctx* ctx, int kind) {
+  const mtp_config& c = ctx->cfg;
+  return kind == EH_PROJ ? 2 * c.hidden : kind == O_PROJ ? ctx->q_dim : kind == DOWN ? c.ffn : c.hidden;
+}
+
+bool rows_proj_supported(const mtp_ctx* ctx, int kind, int B) {
+  const mtp_config& c = ctx->cfg;
+  if (!(B >= 2 && B <= 4 && c.dtype == MTP_DTYPE_BF16 && ctx->has_weights && ctx->rows_proj)) return false;
+  if (kind == LM_HEAD) return false;
+  const int C = rows_cols(ctx, kind);
+  if (C % 128 || c.hidden % 8) return false;
+  int st, kc;
+  return rows_plan(ctx, kind, C, c.hidden, B <= 2 ? 2 : 4, &st, &kc);
+}
+
+template <int KIND, int NB>
+static cudaError_t rows_launch(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uint16_t>& a, int C) {
+  int stages = 0, kc = 0;
+  if (!rows_plan(ctx, KIND, C, a.H, NB, &stages, &kc)) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)stages * 8 * ((size_t)kc * 2 + 16) + (size_t)NB * ((size_t)C * 2 + 16);
+  const int P = (KIND == EH_PROJ || KIND == DOWN) ? a.H
+                : (KIND == O_PROJ) ? a.H / 2
+                : (KIND == QKV_ROPE) ? (a.q_dim + 2 * a.kv_dim) / 2
+                                     : a.F;
+  const int grid = P < ctx->num_sms ? P : ctx->num_sms;
+  auto kern = mtp_rows_proj_kernel<KIND, NB>;
+  cudaError_t e = ensure_smem((const void*)kern, smem);
+  if (e == cudaSuccess) e = launch_pdl(kern, dim3(grid), dim3(kRpThreads), smem, s, a, stages, kc);
+  return e;
+}
+
+template <int KIND>
+static cudaError_t rows_launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uint16_t>& a) {
+  const int C = rows_cols(ctx, KIND);
+  return a.B <= 2 ? rows_launch<KIND, 2>(ctx, s, a, C) : rows_launch<KIND, 4>(ctx, s, a, C);
+}
+
+cudaError_t launch_rows_proj(mtp_ctx* ctx, cudaStream_t s, int kind, const StepArgs<uint16_t>& a) {
+  switch (kind) {
+    case EH_PROJ: return rows_launch_kind<EH_PROJ>(ctx, s, a);
+    case QKV_ROPE: return rows_launch_kind<QKV_ROPE>(ctx, s, a);
+    case O_PROJ: return rows_launch_kind<O_PROJ>(ctx, s, a);
+    case GATE_UP: return rows_launch_kind<GATE_UP>(ctx, s, a);
+    case DOWN: return rows_launch_kind<DOWN>(ctx, s, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mtp
