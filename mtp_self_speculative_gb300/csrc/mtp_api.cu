@@ -137,6 +137,13 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // the streamed GEMV for them (comparison)
   ctx->rows_proj = 1;
   if (const char* env = getenv("MTP_ROWS_PROJ")) ctx->rows_proj = (int)strtol(env, nullptr, 0) != 0;
+  ctx->rows_max_kc = 4096;
+  ctx->rows_min_stages = 3;
+  if (const char* env = getenv("MTP_ROWS_KC")) ctx->rows_max_kc = (int)strtol(env, nullptr, 0);
+  if (const char* env = getenv("MTP_ROWS_MIN_STAGES")) ctx->rows_min_stages = (int)strtol(env, nullptr, 0);
+  if (ctx->rows_max_kc < 256 || ctx->rows_max_kc > 4096 || (ctx->rows_max_kc & (ctx->rows_max_kc - 1)))
+    ctx->rows_max_kc = 4096;
+  if (ctx->rows_min_stages < 2 || ctx->rows_min_stages > 8) ctx->rows_min_stages = 3;
   // Shared-memory budget of the streamed kernel per kind, in KB;
   // MTP_GEMV_BUDGET ("eh,qkv,o,gu,down,lm") overrides it for tuning.
   for (int i = 0; i < 6; ++i) ctx->gemv_budget_kb[i] = 220;

@@ -273,6 +273,7 @@ struct mtp_ctx {
   int gemv_budget_kb[6];         // shared memory per streamed-kernel CTA, per kind
   int lm_rows;                   // LM head of 2..4 requests on the tensor cores (0: streamed GEMV)
   int rows_proj;                 // short projections of 2..4 requests on the tensor cores (0: streamed GEMV)
+  int rows_max_kc, rows_min_stages;  // their chunk plan: widest chunk (columns), fewest ring stages
   // persistent draft kernel (batches 1..p_max_batch; 0 = off)
   int p_max_batch;
   void* p_ws;

@@ -42,7 +42,7 @@ namespace mtp {
 
 constexpr int kRpCons = 8;
 constexpr int kRpThreads = 32 * (kRpCons + 1);
-constexpr int kRpMaxStages = 16;
+constexpr int kRpMaxStages = 8;
 constexpr uint32_t kRpWaitLimit = 1u << 24;
 
 __device__ __forceinline__ void rp_cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
@@ -232,18 +232,27 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       const unsigned char* bp = rps + (size_t)s * stage_bytes + (size_t)gi * rp + (size_t)(cw * kw + 2 * ti) * 2;
       const unsigned char* apn = xrow + (size_t)(col0 + 2 * ti) * 2;
       const int h = (KIND == EH_PROJ && col0 >= a.H) ? 1 : 0;
-      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-      for (int j = 0; j < nks; ++j) {
+      // two accumulator chains (even and odd k-steps), so that consecutive
+      // MMAs of a warp do not wait on each other's results; nks is even
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
+      for (int j = 0; j < nks; j += 2) {
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp + 32 * j);
         const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 16);
-        uint32_t af[4] = {0u, 0u, 0u, 0u};
+        const uint32_t b2 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 32);
+        const uint32_t b3 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 48);
+        uint32_t af[4] = {0u, 0u, 0u, 0u}, ag[4] = {0u, 0u, 0u, 0u};
         if (real) {
           af[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * j);
           af[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 16);
+          ag[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 32);
+          ag[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 48);
         }
         mma_bf16(d, af, b0, b1);
+        mma_bf16(e, ag, b2, b3);
       }
+      d[0] += e[0];
+      d[1] += e[1];
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&empty_bar[s])) : "memory");
       if (NH == 2 && h) {
@@ -301,27 +310,64 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   }
 }
 
-// Columns per chunk: the largest divisor of C (a multiple of 128 columns, at
-// most 4096; for eh_proj a divisor of H, so that a chunk lies in one half)
-// whose stages leave room for at least four in the shared memory left by the
-// staged input.
+// Dynamic shared memory a CTA of the kernel takes at most: 220 KB (filling
+// the last few KB that the device's opt-in limit leaves -- three 64 KB
+// stages beside a 4-request input -- measured about 1% slower on the tree
+// loops than 5 stages of 32 KB), within that limit less the kernel's static
+// shared memory and 64 bytes of slack.
+static size_t rows_smem_budget(int kind, int nb) {
+  static size_t budget[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  if (kind < EH_PROJ || kind > DOWN) return 0;
+  const int slot = kind * 2 + (nb > 2 ? 1 : 0);
+  if (budget[slot]) return budget[slot];
+  int dev = 0, optin = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaFuncAttributes fa{};
+  const void* f = nullptr;
+  switch (kind) {
+    case EH_PROJ: f = nb > 2 ? (const void*)mtp_rows_proj_kernel<EH_PROJ, 4> : (const void*)mtp_rows_proj_kernel<EH_PROJ, 2>; break;
+    case QKV_ROPE: f = nb > 2 ? (const void*)mtp_rows_proj_kernel<QKV_ROPE, 4> : (const void*)mtp_rows_proj_kernel<QKV_ROPE, 2>; break;
+    case O_PROJ: f = nb > 2 ? (const void*)mtp_rows_proj_kernel<O_PROJ, 4> : (const void*)mtp_rows_proj_kernel<O_PROJ, 2>; break;
+    case GATE_UP: f = nb > 2 ? (const void*)mtp_rows_proj_kernel<GATE_UP, 4> : (const void*)mtp_rows_proj_kernel<GATE_UP, 2>; break;
+    case DOWN: f = nb > 2 ? (const void*)mtp_rows_proj_kernel<DOWN, 4> : (const void*)mtp_rows_proj_kernel<DOWN, 2>; break;
+    default: return 0;
+  }
+  if (cudaFuncGetAttributes(&fa, f) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  size_t lim = (size_t)optin > fa.sharedSizeBytes + 64 ? (size_t)optin - fa.sharedSizeBytes - 64 : 0;
+  if (lim > 220 * 1024) lim = 220 * 1024;
+  budget[slot] = lim;
+  return lim;
+}
+
+// Columns per chunk: the largest power of two from 256 to 4096 (MTP_ROWS_KC
+// lowers the top) dividing C -- and H for eh_proj, so that a chunk lies in
+// one half -- whose stages fit at least rows_min_stages times (3;
+// MTP_ROWS_MIN_STAGES) into the shared memory the staged input leaves.
+// Wider chunks (8 KB row copies) streamed better on the tree loops than
+// more stages of narrower ones: 2 KB copies cost 9%, 1 KB copies 20%.
 static bool rows_plan(const mtp_ctx* ctx, int kind, int C, int H, int nb, int* stages, int* kc) {
-  const size_t budget = 220 * 1024;
+  const size_t budget = rows_smem_budget(kind, nb);
   const size_t xa = (size_t)nb * ((size_t)C * 2 + 16);
-  if (xa >= budget) return false;
+  if (budget == 0 || xa >= budget) return false;
   const size_t avail = budget - xa;
-  for (int k = 4096; k >= 128; k >>= 1) {
+  for (int k = ctx->rows_max_kc; k >= 256; k >>= 1) {
     if (C % k || (kind == EH_PROJ && H % k)) continue;
     const size_t st = (size_t)8 * ((size_t)k * 2 + 16);
     int n = (int)(avail / st);
     if (n > kRpMaxStages) n = kRpMaxStages;
-    if (n >= 4) {
+    if (n >= ctx->rows_min_stages) {
       *stages = n;
       *kc = k;
       return true;
     }
   }
-  (void)ctx;
   return false;
 }
 
