@@ -50,24 +50,6 @@ __device__ __forceinline__ void rp_cons_bar() { asm volatile("bar.sync 1, 256;" 
 // Pairs (epilogue units) per 8-row unit.
 __host__ __device__ constexpr int rp_pairs_per_unit(int kind) { return gemv_unit_rows(kind) == 2 ? 4 : 8; }
 
-// Stage rows [i8 * 8, i8 * 8 + 8) of one input vector of request b: y = x * w
-// (w = nullptr: y = x) rounded to bf16 into dst; returns the sum of x^2.
-template <typename S>
-__device__ __forceinline__ float rp_stage8(unsigned char* dst, const S* src, const uint16_t* w) {
-  float x[8], wv[8];
-  load8_row<uint16_t, S>(src, x);
-  if (w) load8_row<uint16_t, uint16_t>(w, wv);
-  float ss = 0.0f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    ss = fmaf(x[e], x[e], ss);
-    if (w) x[e] *= wv[e];
-  }
-  *reinterpret_cast<uint4*>(dst) =
-      make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-  return ss;
-}
-
 template <int KIND, int NB>
 __global__ void __launch_bounds__(kRpThreads, 1)
     mtp_rows_proj_kernel(const StepArgs<uint16_t> a, int stages, int kc) {
@@ -144,47 +126,96 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   }
 
   // consumers: stage x * w (bf16) of every request, sums of squares per
-  // (request, half)
-  pdl_wait();
+  // (request, half).  A thread takes 8-value vectors i = ct, ct + 256, ...
+  // of each input half; the norm weights of its first two vectors are
+  // constant and load before the dependency wait, and the inputs of all
+  // requests for a vector load together (one round trip per vector pair).
   const int ct = threadIdx.x - 32, cw = warp - 1;
   const int nb = a.B;
+  const int nvv = (KIND == EH_PROJ) ? (a.H >> 3) : (C >> 3);  // vectors per input half
+  const uint16_t* wn[NH];
+  if constexpr (KIND == EH_PROJ) {
+    wn[0] = a.w_norm_h;
+    wn[NH - 1] = a.w_norm_e;
+  } else {
+    wn[0] = (KIND == QKV_ROPE) ? a.w_norm_in : (KIND == GATE_UP) ? a.w_norm_post : nullptr;
+  }
+  float wpre[2][NH][8];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+      if (kNorm && ct + 256 * t < nvv) load8_row<uint16_t, uint16_t>(wn[h] + 8 * (ct + 256 * t), wpre[t][h]);
+  pdl_wait();
   if (KIND == EH_PROJ && a.k == 1 && blockIdx.x == 0)
     for (int b = ct; b < a.B; b += 32 * kRpCons) a.req_bad[b] = (a.pending[b] != 0);
   {
     float ss[2 * NB];
 #pragma unroll
-    for (int i = 0; i < 2 * NB; ++i) ss[i] = 0.0f;
-    const int nv = a.H >> 3;  // 8-value vectors per H-wide input
+    for (int q = 0; q < 2 * NB; ++q) ss[q] = 0.0f;
+    int id[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      if (b < nb) {
-        unsigned char* row = xa + (size_t)b * ap;
-        if constexpr (KIND == EH_PROJ) {
-          int id = 0;
-          if (a.k > 1) {
-            id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
-            if (id < 0 || id >= a.V) {
+    for (int b = 0; b < NB; ++b) id[b] = 0;
+    if constexpr (KIND == EH_PROJ) {
+      if (a.k > 1) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (b < nb) {
+            id[b] = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+            if (id[b] < 0 || id[b] >= a.V) {
               if (ct == 0) set_error(a.err, MTP_ERR_DEVICE_ARGS);
-              id = 0;
+              id[b] = 0;
             }
           }
-          for (int i = ct; i < nv; i += 32 * kRpCons) {
-            if (a.k == 1) {
-              ss[2 * b] += rp_stage8<uint16_t>(row + (size_t)i * 16, a.hidden_in + (size_t)b * a.H + 8 * i,
-                                               a.w_norm_h + 8 * i);
-              ss[2 * b + 1] += rp_stage8<uint16_t>(row + (size_t)(a.H + 8 * i) * 2,
-                                                   a.embeds_in + (size_t)b * a.H + 8 * i, a.w_norm_e + 8 * i);
-            } else {
-              ss[2 * b] += rp_stage8<float>(row + (size_t)i * 16, a.hid + (size_t)b * a.H + 8 * i, a.w_norm_h + 8 * i);
-              ss[2 * b + 1] += rp_stage8<uint16_t>(row + (size_t)(a.H + 8 * i) * 2, a.embed + (size_t)id * a.H + 8 * i,
-                                                   a.w_norm_e + 8 * i);
-            }
-          }
+        }
+      }
+    }
+    for (int i = ct, t = 0; i < nvv; i += 32 * kRpCons, ++t) {
+      float w[NH][8];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        if (!kNorm) break;
+        if (t < 2) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) w[h][e] = (t == 0) ? wpre[0][h][e] : wpre[1][h][e];
         } else {
-          const float* src = (KIND == QKV_ROPE) ? a.x : (KIND == O_PROJ) ? a.attn : (KIND == GATE_UP) ? a.h1 : a.act;
-          const uint16_t* w = (KIND == QKV_ROPE) ? a.w_norm_in : (KIND == GATE_UP) ? a.w_norm_post : nullptr;
-          for (int i = ct; i < (C >> 3); i += 32 * kRpCons)
-            ss[2 * b] += rp_stage8<float>(row + (size_t)i * 16, src + (size_t)b * C + 8 * i, w ? w + 8 * i : nullptr);
+          load8_row<uint16_t, uint16_t>(wn[h] + 8 * i, w[h]);
+        }
+      }
+      float x[NB][NH][8];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < nb) {
+          if constexpr (KIND == EH_PROJ) {
+            if (a.k == 1) {
+              load8_row<uint16_t, uint16_t>(a.hidden_in + (size_t)b * a.H + 8 * i, x[b][0]);
+              load8_row<uint16_t, uint16_t>(a.embeds_in + (size_t)b * a.H + 8 * i, x[b][NH - 1]);
+            } else {
+              load8_row<uint16_t, float>(a.hid + (size_t)b * a.H + 8 * i, x[b][0]);
+              load8_row<uint16_t, uint16_t>(a.embed + (size_t)id[b] * a.H + 8 * i, x[b][NH - 1]);
+            }
+          } else {
+            const float* src = (KIND == QKV_ROPE) ? a.x : (KIND == O_PROJ) ? a.attn : (KIND == GATE_UP) ? a.h1 : a.act;
+            load8_row<uint16_t, float>(src + (size_t)b * C + 8 * i, x[b][0]);
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        if (b < nb) {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            float q = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              q = fmaf(x[b][h][e], x[b][h][e], q);
+              if (kNorm) x[b][h][e] *= w[h][e];
+            }
+            ss[2 * b + h] += q;
+            unsigned char* dst = xa + (size_t)b * ap + (size_t)(h * a.H + 8 * i) * 2;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16(x[b][h][0], x[b][h][1]), pack_bf16(x[b][h][2], x[b][h][3]),
+                                                        pack_bf16(x[b][h][4], x[b][h][5]), pack_bf16(x[b][h][6], x[b][h][7]));
+          }
         }
       }
     }
