@@ -279,6 +279,22 @@ def test_qwen3_8b_b1_full_size(path):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_qwen3_8b_small_batch_full_size(B):
+    """Qwen3-8B-shaped head at 2, 3 and 4 requests (tree expansions, small
+    batches), bf16, ragged paged contexts, K=3: the tensor-core short
+    projections at their real chunking (4096- and 2048-column chunks, eh_proj
+    accumulating its two halves apart, a 4-request tile with one empty row at
+    B=3) and the tensor-core LM head; every request checked."""
+    import dataclasses
+    cfg = dataclasses.replace(synth.QWEN3_8B_B1, name="qwen3_8b_mtp_b%d" % B, batch=B, K=3, ctx_lo=1, ctx_hi=4096,
+                              paged_shuffle=True, seed_index=57)
+    case = Case(cfg, lens=[4096, 1, 2500, 17][:B], persistent_max_batch=-1)
+    worst, exact, ids, logits = check_forced(case, list(range(B)), LOGIT_TOL)
+    check_free(case, list(range(B)), ids, logits, LOGIT_TOL)
+
+
+@pytest.mark.slow
 def test_qwen3_8b_cb32_ragged_paged():
     """Continuous batching: B=32, contexts uniform in 512..8192 in shuffled
     16-token blocks, K=5; every request checked."""
