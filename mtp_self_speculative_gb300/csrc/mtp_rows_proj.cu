@@ -23,9 +23,11 @@
 // columns from the staged input and the B fragments from the stage, and
 // releases the stage (the empty barrier counts the 8 warps).  A unit's
 // partial sums (per request and row) stay in registers over its chunks and
-// meet in a double-buffered shared area after one consumer barrier; 8 x NB
-// threads add them in warp order (deterministic) and run the kind's
-// epilogue.
+// are parked in a double-buffered shared area (sum_full counts the 8 warps);
+// a tenth warp adds them in warp order (deterministic), runs the kind's
+// epilogue -- whose loads of residuals, rotary table and cache metadata
+// would otherwise hold up a consumer warp and with it every stage -- and
+// hands the buffer back (sum_empty).
 //
 // The input is staged once per CTA as bf16 x * w (the RMSNorm weight; no
 // weight for O-proj and down) with each request's sum of squares; the RMS
@@ -41,11 +43,21 @@
 namespace mtp {
 
 constexpr int kRpCons = 8;
-constexpr int kRpThreads = 32 * (kRpCons + 1);
+constexpr int kRpEpiWarp = kRpCons + 1;           // warp 0 copies, 1..8 multiply, 9 runs the epilogues
+constexpr int kRpThreads = 32 * (kRpCons + 2);
 constexpr int kRpMaxStages = 8;
 constexpr uint32_t kRpWaitLimit = 1u << 24;
 
 __device__ __forceinline__ void rp_cons_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Bounded wait that gives up early once another warp has given up.
+__device__ __forceinline__ bool rp_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  for (uint32_t i = 0; i < kRpWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && *abort) return false;
+  }
+  return false;
+}
 
 // Pairs (epilogue units) per 8-row unit.
 __host__ __device__ constexpr int rp_pairs_per_unit(int kind) { return gemv_unit_rows(kind) == 2 ? 4 : 8; }
@@ -60,8 +72,8 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   __shared__ __align__(8) uint64_t full_bar[kRpMaxStages], empty_bar[kRpMaxStages];
   __shared__ float red[2][NH][kRpCons][NB][8];
   __shared__ float ssq[kRpCons][2 * NB];
-  __shared__ float srs[2 * NB];
-  __shared__ int s_abort[2];
+  __shared__ __align__(8) uint64_t sum_full[2], sum_empty[2];
+  __shared__ volatile int s_abort;
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,7 +94,11 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kRpCons);
     }
-    s_abort[0] = s_abort[1] = 0;
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&sum_full[q], kRpCons);
+      mbar_init(&sum_empty[q], 1);
+    }
+    s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -111,8 +127,9 @@ __global__ void __launch_bounds__(kRpThreads, 1)
         for (int r = 0; r < 8; ++r) nrows += (src[r] != nullptr);
         for (int c = 0; c < nch; ++c, ++it) {
           const int s = it % stages;
-          if (!mbar_wait_bounded(&empty_bar[s], (uint32_t)(((it / stages) & 1) ^ 1), kRpWaitLimit)) {
+          if (!rp_wait(&empty_bar[s], (uint32_t)(((it / stages) & 1) ^ 1), &s_abort)) {
             set_error(a.err, MTP_ERR_TIMEOUT);
+            s_abort = 1;
             return;
           }
           unsigned char* dst = rps + (size_t)s * stage_bytes;
@@ -121,6 +138,64 @@ __global__ void __launch_bounds__(kRpThreads, 1)
             if (src[r]) bulk_g2s_hint(dst + (size_t)r * rp, src[r] + (size_t)c * kc, chunk_bytes, &full_bar[s], pol);
         }
       }
+    }
+    return;
+  }
+
+  if (warp == kRpEpiWarp) {
+    // Epilogue warp: for each unit, once the 8 consumer warps have parked
+    // their sums (sum_full), add them in warp order, scale by the RMS
+    // factors and run the kind's epilogue; then hand the buffer back
+    // (sum_empty).  Its loads (residuals, rotary table, cache metadata) and
+    // stores stay off the consumers' path.
+    pdl_wait();
+    const int my_b = lane >> 3, my_r = lane & 7;
+    const bool mine = my_b < a.B;  // B <= NB, so red and ssq are indexed within bounds
+    float sr[2] = {1.0f, 1.0f};
+    unsigned long long best_unused = 0ull;
+    for (int u = 0; u < nunits; ++u) {
+      const int buf = u & 1;
+      if (!__all_sync(0xffffffffu, rp_wait(&sum_full[buf], (uint32_t)((u >> 1) & 1), &s_abort))) {
+        if (lane == 0) {
+          set_error(a.err, MTP_ERR_TIMEOUT);
+          s_abort = 1;
+        }
+        break;
+      }
+      if (u == 0 && kNorm && mine) {
+        // the consumer warps wrote their sums of squares before their first arrival
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          float t = 0.0f;
+          for (int w = 0; w < kRpCons; ++w) t += ssq[w][2 * my_b + h];
+          sr[h] = rsqrtf(t / (float)a.H + a.eps);
+        }
+      }
+      float v = 0.0f;
+      if (mine) {
+        float z[NH];
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          z[hh] = 0.0f;
+#pragma unroll
+          for (int w = 0; w < kRpCons; ++w) z[hh] += red[buf][hh][w][my_b][my_r];
+        }
+        v = z[0] * sr[0];
+        if constexpr (NH == 2) v += z[NH - 1] * sr[1];
+      }
+      // pair kinds: the even slot's lane runs the pair's epilogue with its
+      // odd neighbour's value; single-row kinds: every slot is one row
+      const float vn = __shfl_down_sync(0xffffffffu, v, 1);
+      const int j = (UPP == 4) ? (my_r >> 1) : my_r;
+      const int p = p0 + u * UPP + j;
+      if (mine && p < p1 && (UPP == 8 || (my_r & 1) == 0)) {
+        int r0, r1;
+        const uint16_t *w0, *w1;
+        pair_rows<uint16_t, KIND>(a, p, C, r0, r1, w0, w1);
+        epilogue<uint16_t, KIND>(a, my_b, r0, r1, v, (UPP == 4) ? vn : 0.0f, best_unused);
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sum_empty[buf])) : "memory");
     }
     return;
   }
@@ -227,12 +302,6 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       }
     }
     rp_cons_bar();
-    if (kNorm && ct < 2 * nb) {
-      float t = 0.0f;
-      for (int w = 0; w < kRpCons; ++w) t += ssq[w][ct];
-      srs[ct] = rsqrtf(t / (float)a.H + a.eps);
-    }
-    // srs is read in the epilogues, after the first unit's barrier
   }
 
   const int gi = lane >> 2, ti = lane & 3;
@@ -240,25 +309,19 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   const int nks = kw / 16;
   const bool real = gi < nb;
   const unsigned char* xrow = xa + (size_t)(real ? gi : 0) * ap;
-  // thread ct < 8 NB sums request ct / 8, row slot ct % 8 of every unit
-  const int my_b = ct >> 3, my_r = ct & 7;
-  unsigned long long best_unused = 0ull;
   int it = 0;
   bool failed = false;
-  int u = 0;
-  for (; u < nunits; ++u) {
+  for (int u = 0; u < nunits && !failed; ++u) {
     const int buf = u & 1;
     float acc[NH][4];
 #pragma unroll
     for (int h = 0; h < NH; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.0f;
     for (int c = 0; c < nch; ++c, ++it) {
       const int s = it % stages;
-      if (!failed &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[s], (uint32_t)((it / stages) & 1), kRpWaitLimit))) {
+      if (!__all_sync(0xffffffffu, rp_wait(&full_bar[s], (uint32_t)((it / stages) & 1), &s_abort))) {
         failed = true;
-        if (lane == 0) s_abort[buf] = 1;
+        break;
       }
-      if (failed) continue;
       const int col0 = c * kc + cw * kw;       // first column of this warp's slice
       const unsigned char* bp = rps + (size_t)s * stage_bytes + (size_t)gi * rp + (size_t)(cw * kw + 2 * ti) * 2;
       const unsigned char* apn = xrow + (size_t)(col0 + 2 * ti) * 2;
@@ -267,17 +330,17 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       // MMAs of a warp do not wait on each other's results; nks is even
       float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 2
-      for (int j = 0; j < nks; j += 2) {
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp + 32 * j);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 16);
-        const uint32_t b2 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 32);
-        const uint32_t b3 = *reinterpret_cast<const uint32_t*>(bp + 32 * j + 48);
+      for (int jj = 0; jj < nks; jj += 2) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bp + 32 * jj);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bp + 32 * jj + 16);
+        const uint32_t b2 = *reinterpret_cast<const uint32_t*>(bp + 32 * jj + 32);
+        const uint32_t b3 = *reinterpret_cast<const uint32_t*>(bp + 32 * jj + 48);
         uint32_t af[4] = {0u, 0u, 0u, 0u}, ag[4] = {0u, 0u, 0u, 0u};
         if (real) {
-          af[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * j);
-          af[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 16);
-          ag[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 32);
-          ag[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * j + 48);
+          af[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * jj);
+          af[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * jj + 16);
+          ag[0] = *reinterpret_cast<const uint32_t*>(apn + 32 * jj + 32);
+          ag[2] = *reinterpret_cast<const uint32_t*>(apn + 32 * jj + 48);
         }
         mma_bf16(d, af, b0, b1);
         mma_bf16(e, ag, b2, b3);
@@ -294,50 +357,32 @@ __global__ void __launch_bounds__(kRpThreads, 1)
         acc[0][1] += d[1];
       }
     }
-    // d[0], d[1]: request gi, row slots 2 ti and 2 ti + 1 of the unit
-    if (!failed && real) {
+    if (failed) break;
+    // the epilogue warp has finished with this buffer's previous unit (u - 2)
+    if (u >= 2 &&
+        !__all_sync(0xffffffffu, rp_wait(&sum_empty[buf], (uint32_t)(((u >> 1) - 1) & 1), &s_abort))) {
+      failed = true;
+      break;
+    }
+    // acc[h][0], acc[h][1]: request gi, row slots 2 ti and 2 ti + 1 of the unit
+    if (real) {
 #pragma unroll
       for (int hh = 0; hh < NH; ++hh) {
         red[buf][hh][cw][gi][2 * ti] = acc[hh][0];
         red[buf][hh][cw][gi][2 * ti + 1] = acc[hh][1];
       }
     }
-    rp_cons_bar();
-    if (s_abort[buf]) break;
-    if (ct < 32) {
-      const bool mine = my_b < nb;  // nb <= NB, so red is indexed within bounds
-      float v = 0.0f;
-      if (mine) {
-        float z[NH];
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-          z[hh] = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kRpCons; ++w) z[hh] += red[buf][hh][w][my_b][my_r];
-        }
-        if constexpr (KIND == EH_PROJ) v = z[0] * srs[2 * my_b] + z[NH - 1] * srs[2 * my_b + 1];
-        else if constexpr (kNorm) v = z[0] * srs[2 * my_b];
-        else v = z[0];
-      }
-      // pair kinds: the even slot's thread runs the pair's epilogue with its
-      // odd neighbour's value; single-row kinds: every slot is one row
-      const float vn = __shfl_down_sync(0xffffffffu, v, 1);
-      const int j = (UPP == 4) ? (my_r >> 1) : my_r;
-      const int p = p0 + u * UPP + j;
-      if (mine && p < p1 && (UPP == 8 || (my_r & 1) == 0)) {
-        int r0, r1;
-        const uint16_t *w0, *w1;
-        pair_rows<uint16_t, KIND>(a, p, C, r0, r1, w0, w1);
-        epilogue<uint16_t, KIND>(a, my_b, r0, r1, v, (UPP == 4) ? vn : 0.0f, best_unused);
-      }
-    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sum_full[buf])) : "memory");
   }
-  if (u < nunits) {
-    if (ct == 0) set_error(a.err, MTP_ERR_TIMEOUT);
-    // copies still in flight into the ring get a bounded chance to land
-    if (ct == 0)
-      for (int j = 0; j < stages; ++j)
-        mbar_wait_bounded(&full_bar[(it + j) % stages], (uint32_t)(((it + j) / stages) & 1), kRpWaitLimit);
+  if (failed) {
+    if (lane == 0) {
+      set_error(a.err, MTP_ERR_TIMEOUT);
+      s_abort = 1;
+      // copies still in flight into the ring get a bounded chance to land
+      for (int q = 0; q < stages; ++q)
+        mbar_wait_bounded(&full_bar[(it + q) % stages], (uint32_t)(((it + q) / stages) & 1), kRpWaitLimit >> 4);
+    }
   }
 }
 
