@@ -133,6 +133,11 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   // streamed GEMV for it (comparison).
   ctx->lm_rows = 1;
   if (const char* env = getenv("MTP_LM_ROWS")) ctx->lm_rows = (int)strtol(env, nullptr, 0) != 0;
+  // streamed LM head: ranges weighted by each SM's measured streaming rate;
+  // MTP_LM_BALANCE=0 keeps equal ranges (comparison)
+  ctx->lm_balance = 1;
+  ctx->lm_seq = 0;
+  if (const char* env = getenv("MTP_LM_BALANCE")) ctx->lm_balance = (int)strtol(env, nullptr, 0) != 0;
   // the short projections of 2..4 requests likewise; MTP_ROWS_PROJ=0 keeps
   // the streamed GEMV for them (comparison)
   ctx->rows_proj = 1;
@@ -185,6 +190,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   const size_t o_part = take(part_rows * (c.head_dim + 4) * 4);
   const size_t o_acnt = take(maxB * c.n_kv_heads * 4);
   const size_t o_lmk = take(maxB * 8), o_lmc = take(4);
+  const size_t o_lmt = take(64 * 8), o_lmr = take((size_t)ctx->num_sms * 4);
   const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(256);
   const size_t o_err = take(4);
   const size_t o_bad = take(maxB * 4);
@@ -206,6 +212,8 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->attn_cnt = (int*)(base + o_acnt);
   ctx->lm_keys = (unsigned long long*)(base + o_lmk);
   ctx->lm_cnt = (int*)(base + o_lmc);
+  ctx->lm_tick = (unsigned long long*)(base + o_lmt);
+  ctx->lm_rate = (float*)(base + o_lmr);
   ctx->ver_keys = (unsigned long long*)(base + o_vk);
   ctx->ver_cnt = (int*)(base + o_vc);
   ctx->err = (int*)(base + o_err);
@@ -412,6 +420,12 @@ mtp_status mtp_get_device_error(mtp_ctx* ctx) {
   // a persistent draft call that gave up leaves its grid-barrier words
   // (arrivals, abort flag) inconsistent: start them afresh
   if (word == MTP_ERR_TIMEOUT && ctx->p_gbar && cudaMemset(ctx->p_gbar, 0, 384) != cudaSuccess) return MTP_ERR_CUDA;
+  // an LM head that gave up may leave its arrival and claim counters and
+  // argmax keys part-way: start them afresh as well
+  if (word == MTP_ERR_TIMEOUT && ctx->lm_cnt &&
+      (cudaMemset(ctx->lm_cnt, 0, 4) != cudaSuccess || cudaMemset(ctx->lm_tick, 0, 64 * 8) != cudaSuccess ||
+       cudaMemset(ctx->lm_keys, 0, (size_t)ctx->cfg.max_batch * 8) != cudaSuccess))
+    return MTP_ERR_CUDA;
   return (mtp_status)word;
 }
 

@@ -110,6 +110,13 @@ __device__ __forceinline__ float dot_vec<float>(const uint4& w, const float* x) 
   return s;
 }
 
+// The GPU's global nanosecond timer.
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -272,6 +279,10 @@ struct mtp_ctx {
   int gemv_stream_mask;
   int gemv_budget_kb[6];         // shared memory per streamed-kernel CTA, per kind
   int lm_rows;                   // LM head of 2..4 requests on the tensor cores (0: streamed GEMV)
+  int lm_balance;                // streamed LM head sizes each CTA's range by its SM's measured rate
+  unsigned lm_seq;               // streamed LM head launches (picks the launch's claim counter)
+  unsigned long long* lm_tick;   // [64] claim counters, one per launch in a ring
+  float* lm_rate;                // [num_sms] per-SM streaming rates of the LM head
   int rows_proj;                 // short projections of 2..4 requests on the tensor cores (0: streamed GEMV)
   int rows_max_kc, rows_min_stages;  // their chunk plan: widest chunk (columns), fewest ring stages
   // persistent draft kernel (batches 1..p_max_batch; 0 = off)

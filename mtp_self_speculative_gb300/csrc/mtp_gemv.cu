@@ -241,14 +241,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
   __shared__ float red[kTmaConsumers * 8];
   __shared__ unsigned long long cta_best[kTmaConsumers][NB];
   __shared__ int am_last;
+  __shared__ int s_range[2];
+  __shared__ unsigned long long s_t0;
 
   pdl_trigger();
   const int C = gemv_cols(a, KIND);
   const int P = gemv_pairs(a, KIND);
   const int G = gridDim.x;
-  const int p_begin = (int)(((long long)blockIdx.x * P) / G);
-  const int p_end = (int)(((long long)(blockIdx.x + 1) * P) / G);
-  const int n = p_end - p_begin;
+  int p_begin = (int)(((long long)blockIdx.x * P) / G);
+  int p_end = (int)(((long long)(blockIdx.x + 1) * P) / G);
   const uint32_t row_bytes = (uint32_t)C * sizeof(T);
   const uint32_t stage_stride = (gemv_unit_rows(KIND) * row_bytes + 127) & ~127u;
   float* xs = reinterpret_cast<float*>(gsm + (size_t)stages * stage_stride);
@@ -263,7 +264,51 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     }
     fence_mbar_init();
   }
+  // LM head with weighted ranges: the SMs of this GPU stream at rates that
+  // differ by up to about 10% and stay the same from launch to launch (the
+  // rate follows the SM, not the data), so equal ranges leave the fastest
+  // SMs idle at the end.  Each CTA sizes its range by its SM's measured
+  // rate and takes it with one atomic on a packed (ticket, next pair)
+  // counter: ranges are contiguous in ticket order and the last ticket takes
+  // whatever remains, so the pairs are covered exactly once wherever the
+  // CTAs land.  Every logit is computed the same way whichever CTA owns its
+  // row, so the results do not depend on the split.
+  if constexpr (KIND == LM_HEAD) {
+    if (a.lm_tick && warp == 0) {
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      float sum = 0.0f, known = 0.0f;
+      for (int i = lane; i < a.lm_nsm; i += 32) {
+        const float r = __ldcg(a.lm_rate + i);
+        sum += r;
+        known += (r > 0.0f) ? 1.0f : 0.0f;
+      }
+      sum = warp_sum(sum);
+      known = warp_sum(known);
+      if (lane == 0) {
+        const float mean = known > 0.0f ? sum / known : 1.0f;
+        const float total = known > 0.0f ? sum + ((float)a.lm_nsm - known) * mean : (float)a.lm_nsm;
+        float mine = (smid < (unsigned)a.lm_nsm) ? __ldcg(a.lm_rate + smid) : 0.0f;
+        if (!(mine > 0.0f)) mine = mean;
+        int units = (int)((double)P * (double)mine / (double)total + 0.5);
+        if (units < 1) units = 1;
+        const unsigned long long old = atomicAdd(a.lm_tick, (1ull << 32) | (unsigned long long)units);
+        const int t = (int)(old >> 32);
+        const long long st = (long long)(old & 0xffffffffull);
+        const long long en = (t >= G - 1) ? (long long)P : st + units;
+        s_range[0] = (int)(st < P ? st : P);
+        s_range[1] = (int)(en < P ? en : P);
+      }
+    }
+  }
   __syncthreads();
+  if constexpr (KIND == LM_HEAD) {
+    if (a.lm_tick) {
+      p_begin = s_range[0];
+      p_end = s_range[1];
+    }
+  }
+  const int n = p_end - p_begin;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -300,6 +345,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     for (int b = threadIdx.x - 32; b < a.B; b += 32 * kTmaConsumers) a.req_bad[b] = (a.pending[b] != 0);
   const int nb = a.B;  // launched only for B <= NB
   cons_stage_inputs<T, KIND>(a, xs, C, nb, red);
+  if (KIND == LM_HEAD && threadIdx.x == 32) s_t0 = globaltimer_ns();
   const int cw = warp - 1;
   // Full-barrier waits are by phase parity, so a warp may wait on a stage
   // only after the stage's previous fill has landed.  `stages` is a multiple
@@ -364,6 +410,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       for (int j = 0; j < NB; ++j) cta_best[cw][j] = best[j];
     cons_bar();
     const int ct = threadIdx.x - 32;
+    // this SM's streaming rate (pairs per ns from the staged input to the
+    // last pair), folded into its running estimate
+    if (a.lm_tick && ct == 0 && n > 0) {
+      const unsigned long long dt = globaltimer_ns() - s_t0;
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      if (dt > 0 && smid < (unsigned)a.lm_nsm) {
+        const float r = (float)n / (float)dt;
+        const float old = __ldcg(a.lm_rate + smid);
+        a.lm_rate[smid] = old > 0.0f ? 0.75f * old + 0.25f * r : r;
+      }
+    }
     if (ct < nb) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][ct]);
@@ -383,7 +441,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
         MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
         if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k);
       }
-      if (ct == 0) atomicExch(a.lm_cnt, 0);
+      if (ct == 0) {
+        atomicExch(a.lm_cnt, 0);
+        if (a.lm_tick) atomicExch(a.lm_tick, 0ull);
+      }
     }
   }
 }
@@ -494,7 +555,7 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
                                 const void* embeds, const int32_t* positions, const mtp_kv* kv,
                                 const int32_t* chain_ids, int32_t* draft_ids, float* logits, float* hidden_out) {
   const mtp_config& c = ctx->cfg;
-  StepArgs<T> a;
+  StepArgs<T> a{};
   memset(&a, 0, sizeof(a));
   a.B = B; a.H = c.hidden; a.q_dim = ctx->q_dim; a.kv_dim = ctx->kv_dim; a.F = c.ffn; a.V = c.vocab;
   a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.hd = c.head_dim; a.bs = c.block_size; a.eps = c.eps;
@@ -512,6 +573,12 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
   a.hid = ctx->hid; a.x = ctx->x; a.q = ctx->q; a.attn = ctx->attn; a.h1 = ctx->h1; a.act = ctx->act;
   a.lm_keys = ctx->lm_keys; a.lm_cnt = ctx->lm_cnt; a.err = ctx->err; a.rope = ctx->rope;
   a.req_bad = ctx->req_bad;
+  // each launch claims from its own counter of a ring of 64 (reset by the
+  // launch's last CTA), so a launch that starts while an earlier LM head is
+  // still finishing never sees that launch's counter
+  a.lm_tick = ctx->lm_balance ? ctx->lm_tick + (ctx->lm_seq++ & 63) : nullptr;
+  a.lm_rate = ctx->lm_rate;
+  a.lm_nsm = ctx->num_sms;
 
   cudaError_t e;
   if ((e = launch_kind<T, EH_PROJ>(ctx, s, a)) != cudaSuccess) return e;

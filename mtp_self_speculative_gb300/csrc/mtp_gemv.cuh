@@ -33,6 +33,12 @@ struct StepArgs {
   float *hid, *x, *q, *attn, *h1, *act;
   unsigned long long* lm_keys;
   int* lm_cnt;
+  // Streamed LM head, weighted ranges (null: equal ranges): packed (ticket,
+  // first pair) claim counter of this launch, per-SM streaming rates
+  // (pairs per ns, 0 = not yet measured) over lm_nsm SM ids.
+  unsigned long long* lm_tick;
+  float* lm_rate;
+  int lm_nsm;
   int* err;
   int* req_bad;
   const float2* rope;

@@ -1007,7 +1007,7 @@ static cudaError_t launch_q8_lm(mtp_ctx* ctx, cudaStream_t s, const StepArgs<uin
 
 static StepArgs<uint16_t> q_dims(const mtp_ctx* ctx) {
   const mtp_config& c = ctx->cfg;
-  StepArgs<uint16_t> a;
+  StepArgs<uint16_t> a{};
   memset(&a, 0, sizeof(a));
   a.H = c.hidden; a.q_dim = ctx->q_dim; a.kv_dim = ctx->kv_dim; a.F = c.ffn; a.V = c.vocab;
   a.n_q = c.n_q_heads; a.n_kv = c.n_kv_heads; a.hd = c.head_dim; a.bs = c.block_size; a.eps = c.eps;
