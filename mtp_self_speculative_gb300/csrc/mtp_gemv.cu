@@ -264,42 +264,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     }
     fence_mbar_init();
   }
-  // LM head with weighted ranges: the SMs of this GPU stream at rates that
-  // differ by up to about 10% and stay the same from launch to launch (the
-  // rate follows the SM, not the data), so equal ranges leave the fastest
-  // SMs idle at the end.  Each CTA sizes its range by its SM's measured
-  // rate and takes it with one atomic on a packed (ticket, next pair)
-  // counter: ranges are contiguous in ticket order and the last ticket takes
-  // whatever remains, so the pairs are covered exactly once wherever the
-  // CTAs land.  Every logit is computed the same way whichever CTA owns its
-  // row, so the results do not depend on the split.
+  // LM head: ranges weighted by each SM's measured streaming rate (see
+  // lm_weighted_range).  Every logit is computed the same way whichever CTA
+  // owns its row, so the results do not depend on the split.
   if constexpr (KIND == LM_HEAD) {
-    if (a.lm_tick && warp == 0) {
-      unsigned smid;
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      float sum = 0.0f, known = 0.0f;
-      for (int i = lane; i < a.lm_nsm; i += 32) {
-        const float r = __ldcg(a.lm_rate + i);
-        sum += r;
-        known += (r > 0.0f) ? 1.0f : 0.0f;
-      }
-      sum = warp_sum(sum);
-      known = warp_sum(known);
-      if (lane == 0) {
-        const float mean = known > 0.0f ? sum / known : 1.0f;
-        const float total = known > 0.0f ? sum + ((float)a.lm_nsm - known) * mean : (float)a.lm_nsm;
-        float mine = (smid < (unsigned)a.lm_nsm) ? __ldcg(a.lm_rate + smid) : 0.0f;
-        if (!(mine > 0.0f)) mine = mean;
-        int units = (int)((double)P * (double)mine / (double)total + 0.5);
-        if (units < 1) units = 1;
-        const unsigned long long old = atomicAdd(a.lm_tick, (1ull << 32) | (unsigned long long)units);
-        const int t = (int)(old >> 32);
-        const long long st = (long long)(old & 0xffffffffull);
-        const long long en = (t >= G - 1) ? (long long)P : st + units;
-        s_range[0] = (int)(st < P ? st : P);
-        s_range[1] = (int)(en < P ? en : P);
-      }
-    }
+    if (a.lm_tick && warp == 0) lm_weighted_range(a.lm_rate, a.lm_nsm, a.lm_tick, P, G, lane, s_range);
   }
   __syncthreads();
   if constexpr (KIND == LM_HEAD) {
@@ -410,18 +379,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       for (int j = 0; j < NB; ++j) cta_best[cw][j] = best[j];
     cons_bar();
     const int ct = threadIdx.x - 32;
-    // this SM's streaming rate (pairs per ns from the staged input to the
-    // last pair), folded into its running estimate
-    if (a.lm_tick && ct == 0 && n > 0) {
-      const unsigned long long dt = globaltimer_ns() - s_t0;
-      unsigned smid;
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      if (dt > 0 && smid < (unsigned)a.lm_nsm) {
-        const float r = (float)n / (float)dt;
-        const float old = __ldcg(a.lm_rate + smid);
-        a.lm_rate[smid] = old > 0.0f ? 0.75f * old + 0.25f * r : r;
-      }
-    }
+    // this SM's streaming rate (rows from the staged input to the last pair)
+    if (a.lm_tick && ct == 0) lm_rate_update(a.lm_rate, a.lm_nsm, 2 * n, s_t0);
     if (ct < nb) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][ct]);

@@ -53,6 +53,56 @@ struct StepArgs {
   float lm_sigma;
 };
 
+// Weighted ranges of the LM heads.  The SMs of a GPU stream at rates that
+// differ by up to about 10% and stay the same from launch to launch (the
+// rate follows the SM, not the data), so equal ranges leave the fastest SMs
+// idle at the end.  Each CTA sizes its range of `total` units by its SM's
+// measured rate (weight rows per ns, a running average shared by the LM-head
+// kernels; SMs not yet measured count as the mean) and takes it with one atomic on a packed (ticket, next unit)
+// counter: ranges are contiguous in ticket order and the last of the G
+// tickets takes whatever remains, so the units are covered exactly once
+// wherever the CTAs land.  Called by one whole warp; lane 0 writes
+// range[0..1].
+__device__ __forceinline__ void lm_weighted_range(const float* rate, int nsm, unsigned long long* tick, int total,
+                                                  int G, int lane, int* range) {
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  float sum = 0.0f, known = 0.0f;
+  for (int i = lane; i < nsm; i += 32) {
+    const float r = __ldcg(rate + i);
+    sum += r;
+    known += (r > 0.0f) ? 1.0f : 0.0f;
+  }
+  sum = warp_sum(sum);
+  known = warp_sum(known);
+  if (lane == 0) {
+    const float mean = known > 0.0f ? sum / known : 1.0f;
+    const float all = known > 0.0f ? sum + ((float)nsm - known) * mean : (float)nsm;
+    float mine = (smid < (unsigned)nsm) ? __ldcg(rate + smid) : 0.0f;
+    if (!(mine > 0.0f)) mine = mean;
+    int units = (int)((double)total * (double)mine / (double)all + 0.5);
+    if (units < 1) units = 1;
+    const unsigned long long old = atomicAdd(tick, (1ull << 32) | (unsigned long long)units);
+    const int t = (int)(old >> 32);
+    const long long st = (long long)(old & 0xffffffffull);
+    const long long en = (t >= G - 1) ? (long long)total : st + units;
+    range[0] = (int)(st < total ? st : total);
+    range[1] = (int)(en < total ? en : total);
+  }
+}
+
+// Fold this CTA's rate (`rows` weight rows since t0) into its SM's running estimate.
+__device__ __forceinline__ void lm_rate_update(float* rate, int nsm, int rows, unsigned long long t0) {
+  const unsigned long long dt = globaltimer_ns() - t0;
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  if (rows > 0 && dt > 0 && smid < (unsigned)nsm) {
+    const float r = (float)rows / (float)dt;
+    const float old = __ldcg(rate + smid);
+    rate[smid] = old > 0.0f ? 0.75f * old + 0.25f * r : r;
+  }
+}
+
 // LM head of 2..4 requests through mma.sync on whole staged rows
 // (csrc/mtp_lm_rows.cu).
 bool lm_rows_supported(const mtp_ctx* ctx, int B);

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
   __shared__ float rss[kLrCons][NB];
   __shared__ float srs[NB];
   __shared__ int am_last, s_abort[2];
+  __shared__ int s_range[2];
+  __shared__ unsigned long long s_t0;
 
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -57,9 +59,8 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
   const uint32_t pitch = row_bytes + 16;
   const uint32_t stage_bytes = 8 * pitch;
   const int nunits = (a.V + 7) >> 3;
-  const int u0 = (int)(((long long)blockIdx.x * nunits) / gridDim.x);
-  const int u1 = (int)(((long long)(blockIdx.x + 1) * nunits) / gridDim.x);
-  const int n = u1 - u0;
+  int u0 = (int)(((long long)blockIdx.x * nunits) / gridDim.x);
+  int u1 = (int)(((long long)(blockIdx.x + 1) * nunits) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -69,7 +70,15 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
     s_abort[0] = s_abort[1] = 0;
     fence_mbar_init();
   }
+  // ranges of 8-row units weighted by each SM's measured streaming rate
+  // (lm_weighted_range); the logits do not depend on the split
+  if (a.lm_tick && warp == 0) lm_weighted_range(a.lm_rate, a.lm_nsm, a.lm_tick, nunits, gridDim.x, lane, s_range);
   __syncthreads();
+  if (a.lm_tick) {
+    u0 = s_range[0];
+    u1 = s_range[1];
+  }
+  const int n = u1 - u0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -147,6 +156,7 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
     }
   }
 
+  if (ct == 0) s_t0 = globaltimer_ns();
   const long long nL = (long long)a.B * a.K * a.V;
   // thread ct < NB * 8 sums request ct / 8, row ct % 8 of every unit
   const int my_b = ct >> 3, my_r = ct & 7;
@@ -219,6 +229,8 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
   }
   lr_cons_bar();
   if (ct == 0) {
+    // this SM's streaming rate (units from the staged input to the last unit)
+    if (a.lm_tick) lm_rate_update(a.lm_rate, a.lm_nsm, 8 * n, s_t0);
     __threadfence();
     am_last = (atomicAdd(a.lm_cnt, 1) == (int)gridDim.x - 1);
   }
@@ -230,7 +242,10 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
       MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
       if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k);
     }
-    if (ct == 0) atomicExch(a.lm_cnt, 0);
+    if (ct == 0) {
+      atomicExch(a.lm_cnt, 0);
+      if (a.lm_tick) atomicExch(a.lm_tick, 0ull);
+    }
   }
 }
 
