@@ -43,6 +43,7 @@ METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM ro
 # dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch from an ncu capture of the
 # current kernel (profiles/lm_head_argmax_qwen3_8b_mtp_b1.md); other workloads report null.
 LM_TRAFFIC = {
+    "qwen3_8b_mtp_b1": 1244833536 + 3388160,
     "qwen3_8b_mtp_b1:int4_g64": 622737408 + 3309056,
 }
 # The same for one verify launch (profiles/verify_rollback_b64.md).
@@ -522,8 +523,10 @@ def l2_flush(buf) -> None:
     """Evicts L2 by reading a buffer larger than it.  A read leaves clean
     lines behind: a write would leave the next kernel to write back up to
     the whole L2 of dirty lines as it misses, which is not that kernel's
-    traffic."""
-    buf.sum()
+    traffic.  The bytes are summed as int64 words, so that no widened copy
+    of the buffer is written first."""
+    import torch
+    buf.view(torch.int64).sum()
 
 
 def read_floor_us(sizes: dict, stream, reps: int = 10) -> dict:
