@@ -315,6 +315,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
   const int nb = a.B;  // launched only for B <= NB
   cons_stage_inputs<T, KIND>(a, xs, C, nb, red);
   if (KIND == LM_HEAD && threadIdx.x == 32) s_t0 = globaltimer_ns();
+  float rs[NB][2];
+  cons_rms_factors<T, KIND, NB>(a, red, nb, rs);
   const int cw = warp - 1;
   // Full-barrier waits are by phase parity, so a warp may wait on a stage
   // only after the stage's previous fill has landed.  `stages` is a multiple
@@ -340,8 +342,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     float acc0[NB], acc1[NB];
 #pragma unroll
     for (int j = 0; j < NB; ++j) acc0[j] = acc1[j] = 0.0f;
+    if constexpr (KIND == EH_PROJ) {
+      // the hidden half into acc0, the embedding half into acc1: each has
+      // its own RMS factor
+      const int nh = nvec >> 1;
 #pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) {
+      for (int v = lane; v < nh; v += 32) {
+        const uint4 wa = *reinterpret_cast<const uint4*>(s0 + (size_t)v * VPE);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (j < nb) acc0[j] += dot_vec_xs<T>(wa, xs + (size_t)j * C, v, C);
+      }
+#pragma unroll 4
+      for (int v = nh + lane; v < nvec; v += 32) {
+        const uint4 wa = *reinterpret_cast<const uint4*>(s0 + (size_t)v * VPE);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          if (j < nb) acc1[j] += dot_vec_xs<T>(wa, xs + (size_t)j * C, v, C);
+      }
+    }
+#pragma unroll 4
+    for (int v = lane; KIND != EH_PROJ && v < nvec; v += 32) {
       const uint4 wa = *reinterpret_cast<const uint4*>(s0 + (size_t)v * VPE);
       if constexpr (gemv_unit_rows(KIND) == 1) {
 #pragma unroll
@@ -364,12 +385,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
       acc0[j] = warp_sum(acc0[j]);
-      if constexpr (gemv_unit_rows(KIND) == 2) acc1[j] = warp_sum(acc1[j]);
+      if constexpr (gemv_unit_rows(KIND) == 2 || KIND == EH_PROJ) acc1[j] = warp_sum(acc1[j]);
     }
     if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < NB; ++j)
-        if (j < nb) epilogue<T, KIND>(a, j, r0, r1, acc0[j], acc1[j], best[j]);
+      for (int j = 0; j < NB; ++j) {
+        if (j < nb) {
+          if constexpr (KIND == EH_PROJ)
+            epilogue<T, KIND>(a, j, r0, r1, acc0[j] * rs[j][0] + acc1[j] * rs[j][1], 0.0f, best[j]);
+          else
+            epilogue<T, KIND>(a, j, r0, r1, acc0[j] * rs[j][0], acc1[j] * rs[j][0], best[j]);
+        }
+      }
     }
   }
 

@@ -377,9 +377,9 @@ __device__ __forceinline__ float cons_stage_plain(float* row, int C, const float
   return ss;
 }
 
-// Stage the normalised input row(s) of all nb requests (layout above): one
-// pass that stores x * w and sums x^2 for every vector, one block reduction
-// for all of them, then the scalar RMS factors applied in shared memory.
+// Stage the input row(s) of all nb requests times their norm weights (layout
+// above): one pass that stores x * w and sums x^2 for every vector, and the
+// warps' sums in red for cons_rms_factors.
 template <typename T, int KIND>
 __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb, float* red) {
   constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
@@ -428,19 +428,32 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
       const float t = warp_sum(ss[i]);
       if (l == 0 && i < 2 * nb) red[cw * 8 + i] = t;
     }
-    cons_bar();
-    const int ct = threadIdx.x - 32;
-    const int nvec = (KIND == EH_PROJ) ? 2 : 1;
-    for (int b = 0; b < nb; ++b)
-      for (int v = 0; v < nvec; ++v) {
-        float t = 0.0f;
-        for (int w = 0; w < kTmaConsumers; ++w) t += red[w * 8 + 2 * b + v];
-        const float sc = rsqrtf(t / (float)a.H + a.eps);
-        float* dst = xs + (size_t)b * C;
-        for (int i = ct; i < a.H; i += 256) dst[xs_index<T>(v * a.H + i, C)] *= sc;
-      }
   }
   cons_bar();
+}
+
+// The RMS factors 1 / sqrt(mean(x^2) + eps) of the staged inputs (request
+// b, input vector v: eh_proj's hidden and embedding halves), from the warps'
+// sums of squares; 1 for the kinds without a norm.  The staged rows hold
+// x * w unscaled: the factor multiplies the finished dot products, which
+// takes a pass over the staged rows and a barrier off the critical path.
+template <typename T, int KIND, int NB>
+__device__ __forceinline__ void cons_rms_factors(const StepArgs<T>& a, const float* red, int nb, float (&rs)[NB][2]) {
+  constexpr bool kNorm = (KIND != O_PROJ && KIND != DOWN);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    rs[b][0] = rs[b][1] = 1.0f;
+    if (kNorm && b < nb) {
+#pragma unroll
+      for (int v = 0; v < 2; ++v) {
+        if (v == 0 || KIND == EH_PROJ) {
+          float t = 0.0f;
+          for (int w = 0; w < kTmaConsumers; ++w) t += red[w * 8 + 2 * b + v];
+          rs[b][v] = rsqrtf(t / (float)a.H + a.eps);
+        }
+      }
+    }
+  }
 }
 
 }  // namespace mtp
