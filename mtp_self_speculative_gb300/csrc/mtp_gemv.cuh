@@ -393,6 +393,50 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
       if (a.k == 1) {
         s0 = cons_stage_raw<T, T>(dst, C, 0, a.hidden_in + (size_t)b * a.H, a.H, a.w_norm_h);
         s1 = cons_stage_raw<T, T>(dst, C, a.H, a.embeds_in + (size_t)b * a.H, a.H, a.w_norm_e);
+      } else if (a.H <= 8 * 2 * 256) {
+        // the previous step's draft id, the hidden row and the norm weights
+        // load together, the embedding row as soon as the id is in: the two
+        // halves' round trips overlap (at most two 8-value vectors per thread)
+        const int ct = threadIdx.x - 32;
+        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
+                             : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
+        float xh[2][8], wh[2][8], xe[2][8], we[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i8 = ct + 256 * u;
+          if (8 * i8 < a.H) {
+            load8_row<T, float>(a.hid + (size_t)b * a.H + 8 * i8, xh[u]);
+            load8_row<T, T>(a.w_norm_h + 8 * i8, wh[u]);
+            load8_row<T, T>(a.w_norm_e + 8 * i8, we[u]);
+          }
+        }
+        if (id < 0 || id >= a.V) {
+          if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
+          id = 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i8 = ct + 256 * u;
+          if (8 * i8 < a.H) load8_row<T, T>(a.embed + (size_t)id * a.H + 8 * i8, xe[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i8 = ct + 256 * u;
+          if (8 * i8 < a.H) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              s0 = fmaf(xh[u][e], xh[u][e], s0);
+              s1 = fmaf(xe[u][e], xe[u][e], s1);
+              xh[u][e] *= wh[u][e];
+              xe[u][e] *= we[u][e];
+            }
+            const int eh = i8 * 8, ee = a.H + i8 * 8;
+            *reinterpret_cast<float4*>(dst + xs_index<T>(eh, C)) = make_float4(xh[u][0], xh[u][1], xh[u][2], xh[u][3]);
+            *reinterpret_cast<float4*>(dst + xs_index<T>(eh + 4, C)) = make_float4(xh[u][4], xh[u][5], xh[u][6], xh[u][7]);
+            *reinterpret_cast<float4*>(dst + xs_index<T>(ee, C)) = make_float4(xe[u][0], xe[u][1], xe[u][2], xe[u][3]);
+            *reinterpret_cast<float4*>(dst + xs_index<T>(ee + 4, C)) = make_float4(xe[u][4], xe[u][5], xe[u][6], xe[u][7]);
+          }
+        }
       } else {
         int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
                              : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
