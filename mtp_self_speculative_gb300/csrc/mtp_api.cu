@@ -173,6 +173,10 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->q_dim = c.n_q_heads * c.head_dim;
   ctx->kv_dim = c.n_kv_heads * c.head_dim;
   ctx->attn_target_ctas = 16 * sms;  // about eight waves of two CTAs per SM: ragged batches stay balanced
+  if (const char* env = getenv("MTP_ATTN_WAVES")) {
+    const long v = strtol(env, nullptr, 0);
+    if (v >= 1 && v <= 256) ctx->attn_target_ctas = (int)v * sms;
+  }
   ctx->attn_max_splits = 64;
   const size_t H = with_w ? c.hidden : 0, F = with_w ? c.ffn : 0;
   const size_t qd = with_w ? ctx->q_dim : 0;
