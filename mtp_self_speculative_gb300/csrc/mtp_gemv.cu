@@ -314,7 +314,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     for (int b = threadIdx.x - 32; b < a.B; b += 32 * kTmaConsumers) a.req_bad[b] = (a.pending[b] != 0);
   const int nb = a.B;  // launched only for B <= NB
   cons_stage_inputs<T, KIND>(a, xs, C, nb, red);
-  if (KIND == LM_HEAD && threadIdx.x == 32) s_t0 = globaltimer_ns();
+  float rate_old = 0.0f;
+  if (threadIdx.x == 32) {
+    s_t0 = globaltimer_ns();
+    if (KIND == LM_HEAD && a.lm_tick) rate_old = lm_rate_peek(a.lm_rate, a.lm_nsm);
+  }
   float rs[NB][2];
   cons_rms_factors<T, KIND, NB>(a, red, nb, rs);
   const int cw = warp - 1;
@@ -406,8 +410,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       for (int j = 0; j < NB; ++j) cta_best[cw][j] = best[j];
     cons_bar();
     const int ct = threadIdx.x - 32;
-    // this SM's streaming rate (rows from the staged input to the last pair)
-    if (a.lm_tick && ct == 0) lm_rate_update(a.lm_rate, a.lm_nsm, 2 * n, s_t0);
     if (ct < nb) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][ct]);
@@ -416,12 +418,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
     }
     cons_bar();
     if (ct == 0) {
-      __threadfence();
-      am_last = (atomicAdd(a.lm_cnt, 1) == (int)gridDim.x - 1);
+      // this SM's streaming rate (rows from the staged input to the last pair)
+      if (a.lm_tick) lm_rate_store(a.lm_rate, a.lm_nsm, 2 * n, s_t0, rate_old);
+      am_last = (lm_arrive(a.lm_cnt) == (int)gridDim.x - 1);
     }
     cons_bar();
     if (am_last) {
-      __threadfence();
       for (int b = ct; b < a.B; b += 256) {
         const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
         MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));

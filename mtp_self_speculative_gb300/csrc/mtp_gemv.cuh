@@ -91,16 +91,33 @@ __device__ __forceinline__ void lm_weighted_range(const float* rate, int nsm, un
   }
 }
 
-// Fold this CTA's rate (`rows` weight rows since t0) into its SM's running estimate.
-__device__ __forceinline__ void lm_rate_update(float* rate, int nsm, int rows, unsigned long long t0) {
+// This SM's running rate estimate (0 if none), read early so that folding
+// the CTA's own rate in at the end (lm_rate_store) is a plain store.
+__device__ __forceinline__ float lm_rate_peek(const float* rate, int nsm) {
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  return smid < (unsigned)nsm ? __ldcg(rate + smid) : 0.0f;
+}
+
+// Fold this CTA's rate (`rows` weight rows since t0) into its SM's running
+// estimate `old` (from lm_rate_peek).
+__device__ __forceinline__ void lm_rate_store(float* rate, int nsm, int rows, unsigned long long t0, float old) {
   const unsigned long long dt = globaltimer_ns() - t0;
   unsigned smid;
   asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
   if (rows > 0 && dt > 0 && smid < (unsigned)nsm) {
     const float r = (float)rows / (float)dt;
-    const float old = __ldcg(rate + smid);
     rate[smid] = old > 0.0f ? 0.75f * old + 0.25f * r : r;
   }
+}
+
+// CTA arrival with release (orders this CTA's earlier argmax updates) and
+// acquire (the last CTA's later reads see every CTA's updates); returns the
+// count before this arrival.
+__device__ __forceinline__ int lm_arrive(int* cnt) {
+  int prev;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
+  return prev;
 }
 
 // LM head of 2..4 requests through mma.sync on whole staged rows

@@ -156,7 +156,11 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
     }
   }
 
-  if (ct == 0) s_t0 = globaltimer_ns();
+  float rate_old = 0.0f;
+  if (ct == 0) {
+    s_t0 = globaltimer_ns();
+    if (a.lm_tick) rate_old = lm_rate_peek(a.lm_rate, a.lm_nsm);
+  }
   const long long nL = (long long)a.B * a.K * a.V;
   // thread ct < NB * 8 sums request ct / 8, row ct % 8 of every unit
   const int my_b = ct >> 3, my_r = ct & 7;
@@ -230,13 +234,11 @@ __global__ void __launch_bounds__(kLrThreads, 1) mtp_lm_rows_kernel(const StepAr
   lr_cons_bar();
   if (ct == 0) {
     // this SM's streaming rate (units from the staged input to the last unit)
-    if (a.lm_tick) lm_rate_update(a.lm_rate, a.lm_nsm, 8 * n, s_t0);
-    __threadfence();
-    am_last = (atomicAdd(a.lm_cnt, 1) == (int)gridDim.x - 1);
+    if (a.lm_tick) lm_rate_store(a.lm_rate, a.lm_nsm, 8 * n, s_t0, rate_old);
+    am_last = (lm_arrive(a.lm_cnt) == (int)gridDim.x - 1);
   }
   lr_cons_bar();
   if (am_last) {
-    __threadfence();
     for (int b = ct; b < a.B; b += 32 * kLrCons) {
       const unsigned long long key = atomicExch(a.lm_keys + b, 0ull);
       MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 1), (long long)a.B * a.K, (int32_t)key_index(key));
