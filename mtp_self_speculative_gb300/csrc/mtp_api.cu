@@ -178,6 +178,11 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
     if (v >= 1 && v <= 256) ctx->attn_target_ctas = (int)v * sms;
   }
   ctx->attn_max_splits = 64;
+  ctx->attn_force_bps = 0;
+  if (const char* env = getenv("MTP_ATTN_BPS")) {
+    const long v = strtol(env, nullptr, 0);
+    if (v >= 1 && v <= 4096) ctx->attn_force_bps = (int)v;
+  }
   const size_t H = with_w ? c.hidden : 0, F = with_w ? c.ffn : 0;
   const size_t qd = with_w ? ctx->q_dim : 0;
   const size_t part_rows = with_w ? (size_t)(ctx->attn_target_ctas / c.n_kv_heads + maxB + 1) * c.n_q_heads : 0;

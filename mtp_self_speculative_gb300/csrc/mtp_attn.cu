@@ -602,9 +602,20 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
   const int HD = c.head_dim;
   const bool use_mma = sizeof(T) == 2 && HD == 128;
   // the tensor-core kernel keeps at least 16 blocks per split to amortise
-  // its set-up and the split combine; when its grid is short of two CTAs per
-  // SM it runs eight warps per CTA (two blocks each at 16 blocks per split)
-  a.bps = attn_bps(ctx, B, kv->max_blocks, use_mma ? 16 : 2);
+  // its set-up and the split combine (32 at 2-4 requests, where the planned
+  // 16 gave up to 2 waves of narrow CTAs: per launch at B=2 16.3 against
+  // 22.3 us, the bf=4 tree loop 1.4% faster); when its grid is short of two
+  // CTAs per SM it runs eight warps per CTA (two blocks each at 16 blocks per
+  // split)
+  a.bps = attn_bps(ctx, B, kv->max_blocks, use_mma ? (B >= 2 && B <= 4 ? 32 : 16) : 2);
+  if (ctx->attn_force_bps > 0) {
+    // a forced split size (tuning) is taken only while the partials of all
+    // splits fit the buffer sized for the planned ones
+    int bps = ctx->attn_force_bps;
+    while ((kv->max_blocks + bps - 1) / bps > ctx->attn_max_splits) ++bps;
+    const long long rows = (long long)B * ((kv->max_blocks + bps - 1) / bps);
+    if (rows <= (long long)ctx->attn_target_ctas / c.n_kv_heads + ctx->cfg.max_batch + 1) a.bps = bps;
+  }
   const long long mma_ctas = (long long)((kv->max_blocks + a.bps - 1) / a.bps) * c.n_kv_heads * B;
   const bool wide = use_mma && mma_ctas <= 2LL * ctx->num_sms;
   const int splits = (kv->max_blocks + a.bps - 1) / a.bps;

@@ -279,6 +279,7 @@ struct mtp_ctx {
   int gemv_stream_mask;
   int gemv_budget_kb[6];         // shared memory per streamed-kernel CTA, per kind
   int lm_rows;                   // LM head of 2..4 requests on the tensor cores (0: streamed GEMV)
+  int attn_force_bps;            // attention blocks per split (0: planned; tuning)
   int lm_balance;                // streamed LM head sizes each CTA's range by its SM's measured rate
   unsigned lm_seq;               // streamed LM head launches (picks the launch's claim counter)
   unsigned long long* lm_tick;   // [64] claim counters, one per launch in a ring
