@@ -176,9 +176,14 @@ __device__ void attn_finish_merged(const AttnArgs<T>& a, const float* wacc, floa
   if (nsplit == 1) return;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    am_last = (atomicAdd(a.cnt + (size_t)b * a.n_kv + g, 1) == nsplit - 1);
-    if (am_last) __threadfence();
+    // arrival with release (orders the CTA's partials, written before the
+    // barrier) and acquire (the last CTA's reads below see every split's)
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(a.cnt + (size_t)b * a.n_kv + g)
+                 : "memory");
+    am_last = (prev == nsplit - 1);
   }
   __syncthreads();
   if (!am_last) return;
