@@ -138,6 +138,13 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->lm_balance = 1;
   ctx->lm_seq = 0;
   if (const char* env = getenv("MTP_LM_BALANCE")) ctx->lm_balance = (int)strtol(env, nullptr, 0) != 0;
+  // one request: every draft step but the last leaves its argmax to the next
+  // eh_proj; MTP_LM_DEFER=0 keeps the LM head's last-CTA argmax (comparison)
+  ctx->lm_defer = 1;
+  ctx->lm_defer_pending = 0;
+  ctx->lm_defer_grid = 0;
+  ctx->lm_defer_tick = nullptr;
+  if (const char* env = getenv("MTP_LM_DEFER")) ctx->lm_defer = (int)strtol(env, nullptr, 0) != 0;
   // the short projections of 2..4 requests likewise; MTP_ROWS_PROJ=0 keeps
   // the streamed GEMV for them (comparison)
   ctx->rows_proj = 1;
@@ -200,6 +207,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   const size_t o_acnt = take(maxB * c.n_kv_heads * 4);
   const size_t o_lmk = take(maxB * 8), o_lmc = take(4);
   const size_t o_lmt = take(64 * 8), o_lmr = take((size_t)ctx->num_sms * 4);
+  const size_t o_ctk = take((size_t)ctx->num_sms * 8);
   const size_t o_vk = take(maxB * (c.max_k + 1) * 8), o_vc = take(256);
   const size_t o_err = take(4);
   const size_t o_bad = take(maxB * 4);
@@ -223,6 +231,7 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   ctx->lm_cnt = (int*)(base + o_lmc);
   ctx->lm_tick = (unsigned long long*)(base + o_lmt);
   ctx->lm_rate = (float*)(base + o_lmr);
+  ctx->cta_keys = (unsigned long long*)(base + o_ctk);
   ctx->ver_keys = (unsigned long long*)(base + o_vk);
   ctx->ver_cnt = (int*)(base + o_vc);
   ctx->err = (int*)(base + o_err);

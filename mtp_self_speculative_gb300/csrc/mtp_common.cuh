@@ -281,6 +281,10 @@ struct mtp_ctx {
   int lm_rows;                   // LM head of 2..4 requests on the tensor cores (0: streamed GEMV)
   int attn_force_bps;            // attention blocks per split (0: planned; tuning)
   int lm_balance;                // streamed LM head sizes each CTA's range by its SM's measured rate
+  int lm_defer;                  // one request: the next eh_proj reduces the LM head's per-CTA keys
+  int lm_defer_pending, lm_defer_grid;  // the last LM head launch deferred its argmax, over this many CTAs
+  unsigned long long* lm_defer_tick;    // ... and left this claim counter to be zeroed
+  unsigned long long* cta_keys;  // [num_sms] per-CTA argmax keys of a deferred LM head
   unsigned lm_seq;               // streamed LM head launches (picks the launch's claim counter)
   unsigned long long* lm_tick;   // [64] claim counters, one per launch in a ring
   float* lm_rate;                // [num_sms] per-SM streaming rates of the LM head

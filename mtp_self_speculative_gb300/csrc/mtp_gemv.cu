@@ -410,6 +410,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       for (int j = 0; j < NB; ++j) cta_best[cw][j] = best[j];
     cons_bar();
     const int ct = threadIdx.x - 32;
+    if (a.defer_out) {
+      // deferred argmax (one request): the CTA's best key goes to its own
+      // slot; the next step's eh_proj reduces the slots, writes the draft id
+      // and pending, and zeroes the claim counter
+      if (ct == 0) {
+        unsigned long long m = 0ull;
+        for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][0]);
+        a.cta_keys[blockIdx.x] = m;
+        if (a.lm_tick) lm_rate_store(a.lm_rate, a.lm_nsm, 2 * n, s_t0, rate_old);
+      }
+      return;
+    }
     if (ct < nb) {
       unsigned long long m = 0ull;
       for (int w = 0; w < kTmaConsumers; ++w) m = umax64(m, cta_best[w][ct]);
@@ -435,6 +447,56 @@ __global__ void __launch_bounds__(kTmaThreads, 1) mtp_stream_proj_kernel(const S
       }
     }
   }
+}
+
+// The streamed variant's ring for this kind and batch: stages (a multiple
+// of the consumer warps), consumer warps and dynamic shared memory.  False
+// when the streamed variant is switched off for the kind or does not fit.
+template <typename T, int KIND>
+static bool stream_plan(const mtp_ctx* ctx, const StepArgs<T>& a, int* stages_out, int* consumers_out,
+                        size_t* smem_out) {
+  const int C = (KIND == EH_PROJ) ? 2 * a.H : (KIND == O_PROJ) ? a.q_dim : (KIND == DOWN) ? a.F : a.H;
+  const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;
+  const size_t stage_stride = ((size_t)gemv_unit_rows(KIND) * C * sizeof(T) + 127) & ~(size_t)127;
+  const size_t xs_bytes = (size_t)nbt * C * sizeof(float);
+  const size_t budget = (size_t)ctx->gemv_budget_kb[KIND] * 1024;
+  int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;
+  if (max_stages > kMaxTmaStages) max_stages = kMaxTmaStages;
+  // stages = consumers * k.  One row: pick the consumer count (4..8) that
+  // keeps the most stages.  Two or four rows: the consumers' arithmetic
+  // grows with the rows while the bytes do not, so keep all eight consumer
+  // warps whenever eight stages fit.
+  int consumers = 0, stages = 0;
+  if (nbt >= 2 && max_stages >= kTmaConsumers) {
+    consumers = kTmaConsumers;
+    stages = kTmaConsumers * (max_stages / kTmaConsumers);
+  }
+  if (stages == 0) {
+    for (int cw = kTmaConsumers; cw >= 1; --cw) {
+      const int st = cw * (max_stages / cw);
+      if (st > stages || (st == stages && st > 0 && cw > consumers && cw <= max_stages)) {
+        stages = st;
+        consumers = cw;
+      }
+      if (cw <= 4 && stages > 0) break;
+    }
+  }
+  *stages_out = stages;
+  *consumers_out = consumers;
+  *smem_out = stages * stage_stride + xs_bytes;
+  return ((ctx->gemv_stream_mask >> KIND) & 1) && a.B <= 4 && stages >= 2 && consumers >= 2;
+}
+
+// True when launch_kind runs the streamed variant for this kind and batch.
+template <typename T, int KIND>
+static bool runs_streamed(const mtp_ctx* ctx, const StepArgs<T>& a) {
+  if (sizeof(T) == 2) {
+    if (KIND == LM_HEAD && lm_rows_supported(ctx, a.B)) return false;
+    if (KIND != LM_HEAD && rows_proj_supported(ctx, KIND, a.B)) return false;
+  }
+  int st, cw;
+  size_t sm;
+  return stream_plan<T, KIND>(ctx, a, &st, &cw, &sm);
 }
 
 template <typename T, int KIND>
@@ -475,32 +537,9 @@ static cudaError_t launch_kind(mtp_ctx* ctx, cudaStream_t s, const StepArgs<T>& 
   // TMA-streamed variant for B <= 4
   {
     const int nbt = a.B <= 1 ? 1 : a.B <= 2 ? 2 : 4;
-    const size_t stage_stride = ((size_t)gemv_unit_rows(KIND) * C * sizeof(T) + 127) & ~(size_t)127;
-    const size_t xs_bytes = (size_t)nbt * C * sizeof(float);
-    const size_t budget = (size_t)ctx->gemv_budget_kb[KIND] * 1024;
-    int max_stages = xs_bytes < budget ? (int)((budget - xs_bytes) / stage_stride) : 0;
-    if (max_stages > kMaxTmaStages) max_stages = kMaxTmaStages;
-    // stages = consumers * k.  One row: pick the consumer count (4..8) that
-    // keeps the most stages.  Two or four rows: the consumers' arithmetic
-    // grows with the rows while the bytes do not, so keep all eight consumer
-    // warps whenever eight stages fit.
-    int consumers = 0, stages = 0;
-    if (nbt >= 2 && max_stages >= kTmaConsumers) {
-      consumers = kTmaConsumers;
-      stages = kTmaConsumers * (max_stages / kTmaConsumers);
-    }
-    if (stages == 0) {
-      for (int cw = kTmaConsumers; cw >= 1; --cw) {
-        const int st = cw * (max_stages / cw);
-        if (st > stages || (st == stages && st > 0 && cw > consumers && cw <= max_stages)) {
-          stages = st;
-          consumers = cw;
-        }
-        if (cw <= 4 && stages > 0) break;
-      }
-    }
-    if (((ctx->gemv_stream_mask >> KIND) & 1) && a.B <= 4 && stages >= 2 && consumers >= 2) {
-      const size_t smem_t = stages * stage_stride + xs_bytes;
+    int stages = 0, consumers = 0;
+    size_t smem_t = 0;
+    if (stream_plan<T, KIND>(ctx, a, &stages, &consumers, &smem_t)) {
       const int gridt = min(ctx->num_sms, P);
       if (nbt == 1) {
         auto kern = mtp_stream_proj_kernel<T, KIND, 1>;
@@ -567,6 +606,23 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
   a.lm_tick = ctx->lm_balance ? ctx->lm_tick + (ctx->lm_seq++ & 63) : nullptr;
   a.lm_rate = ctx->lm_rate;
   a.lm_nsm = ctx->num_sms;
+  // Deferred argmax (one request, steps before the last, both kernels the
+  // streamed variant): the LM head leaves one key per CTA and the next
+  // step's eh_proj, which needs the id first thing, reduces them -- the LM
+  // head's arrival counter and last-CTA tail drop out of every step but the
+  // last.
+  a.cta_keys = ctx->cta_keys;
+  if (ctx->lm_defer_pending && k == 1 && ctx->lm_defer_tick) {
+    // a deferred step whose successor never ran: zero its claim counter
+    cudaError_t e0 = cudaMemsetAsync(ctx->lm_defer_tick, 0, sizeof(unsigned long long), s);
+    if (e0 != cudaSuccess) return e0;
+  }
+  a.keys_in = ctx->lm_defer_pending && k > 1;
+  a.keys_n = ctx->lm_defer_grid;
+  a.keys_tick = ctx->lm_defer_tick;
+  ctx->lm_defer_pending = 0;
+  a.defer_out = ctx->lm_defer && B == 1 && k < K && runs_streamed<T, LM_HEAD>(ctx, a) &&
+                runs_streamed<T, EH_PROJ>(ctx, a);
 
   cudaError_t e;
   if ((e = launch_kind<T, EH_PROJ>(ctx, s, a)) != cudaSuccess) return e;
@@ -575,7 +631,13 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
   if ((e = launch_kind<T, O_PROJ>(ctx, s, a)) != cudaSuccess) return e;
   if ((e = launch_kind<T, GATE_UP>(ctx, s, a)) != cudaSuccess) return e;
   if ((e = launch_kind<T, DOWN>(ctx, s, a)) != cudaSuccess) return e;
-  return launch_kind<T, LM_HEAD>(ctx, s, a);
+  if ((e = launch_kind<T, LM_HEAD>(ctx, s, a)) != cudaSuccess) return e;
+  if (a.defer_out) {
+    ctx->lm_defer_pending = 1;
+    ctx->lm_defer_grid = min(ctx->num_sms, (a.V + 1) / 2);
+    ctx->lm_defer_tick = a.lm_tick;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_draft_step(mtp_ctx* ctx, cudaStream_t s, int B, int k, int K, const void* hidden,

@@ -39,6 +39,14 @@ struct StepArgs {
   unsigned long long* lm_tick;
   float* lm_rate;
   int lm_nsm;
+  // Deferred argmax (one request, every step but the last): the streamed LM
+  // head stores each CTA's best (value, id) key in cta_keys[CTA] and stops
+  // there (defer_out); the next step's eh_proj reduces the keys_n keys
+  // itself (keys_in), writes the draft id, advances pending and zeroes the
+  // LM launch's claim counter keys_tick.
+  unsigned long long* cta_keys;
+  unsigned long long* keys_tick;
+  int defer_out, keys_in, keys_n;
   int* err;
   int* req_bad;
   const float2* rope;
@@ -415,8 +423,6 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
         // load together, the embedding row as soon as the id is in: the two
         // halves' round trips overlap (at most two 8-value vectors per thread)
         const int ct = threadIdx.x - 32;
-        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
-                             : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
         float xh[2][8], wh[2][8], xe[2][8], we[2][8];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -427,6 +433,8 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
             load8_row<T, T>(a.w_norm_e + 8 * i8, we[u]);
           }
         }
+        const int prev = (a.keys_in || !a.chain_ids) ? eh_prev_draft(a, b) : 0;
+        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : prev;
         if (id < 0 || id >= a.V) {
           if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
           id = 0;
@@ -455,9 +463,9 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
           }
         }
       } else {
-        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)]
-                             : a.draft_ids[(size_t)b * a.K + (a.k - 2)];
         s0 = cons_stage_raw<T, float>(dst, C, 0, a.hid + (size_t)b * a.H, a.H, a.w_norm_h);
+        const int prev = (a.keys_in || !a.chain_ids) ? eh_prev_draft(a, b) : 0;
+        int id = a.chain_ids ? a.chain_ids[(size_t)b * (a.K - 1) + (a.k - 2)] : prev;
         if (id < 0 || id >= a.V) {
           if (threadIdx.x == 32) set_error(a.err, MTP_ERR_DEVICE_ARGS);
           id = 0;
@@ -491,6 +499,30 @@ __device__ void cons_stage_inputs(const StepArgs<T>& a, float* xs, int C, int nb
     }
   }
   cons_bar();
+}
+
+// The previous step's draft id of request b, for eh_proj at k > 1 (called
+// by whole warps): reduced from the deferred LM head's per-CTA keys -- every
+// warp reduces them itself, so no barrier is needed -- or read from
+// draft_ids.  With deferred keys, thread 32 of CTA 0 also writes the draft id,
+// advances pending as the LM head's last CTA would have, and zeroes the LM
+// launch's claim counter.
+template <typename T>
+__device__ __forceinline__ int eh_prev_draft(const StepArgs<T>& a, int b) {
+  if (a.keys_in) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long kk = 0ull;
+    for (int i = lane; i < a.keys_n; i += 32) kk = umax64(kk, __ldcg(a.cta_keys + i));
+    kk = warp_max_u64(kk);
+    const int id = (int)key_index(kk);
+    if (blockIdx.x == 0 && threadIdx.x == 32) {
+      MTP_STORE(a.err, a.draft_ids, (size_t)b * a.K + (a.k - 2), (long long)a.B * a.K, id);
+      if (!__ldcg(a.req_bad + b)) MTP_STORE(a.err, a.pending, b, a.B, a.k - 1);
+      if (a.keys_tick) *a.keys_tick = 0ull;
+    }
+    return id;
+  }
+  return a.draft_ids[(size_t)b * a.K + (a.k - 2)];
 }
 
 // The RMS factors 1 / sqrt(mean(x^2) + eps) of the staged inputs (request

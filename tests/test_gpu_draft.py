@@ -370,3 +370,29 @@ def test_lm_head_weighted_ranges_are_bit_identical(B, monkeypatch):
         got[bal] = (ids, logits)
     np.testing.assert_array_equal(got["1"][0], got["0"][0])
     np.testing.assert_array_equal(got["1"][1], got["0"][1])
+
+
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 60001), ("bf16", 201), ("f32", 4099)])
+def test_deferred_argmax_matches_last_cta_argmax(dtype, vocab, monkeypatch):
+    """One request: in every step but the last the LM head leaves one argmax
+    key per CTA and the next step's eh_proj reduces them (writing the draft
+    id and the pending count itself).  Forced and free-running drafts give
+    the same ids, logits, hidden rows and cache as the LM head's own last-CTA
+    argmax, bit for bit, and match the oracle.  201 rows launch fewer CTAs
+    than there are SMs."""
+    cfg = synth.MTPShape("defer_" + dtype, H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=vocab, batch=1, K=5,
+                         dtype=dtype, ctx_lo=40, ctx_hi=90, seed_index=61)
+    tol = F32_LOGIT_TOL if dtype == "f32" else LOGIT_TOL
+    got = {}
+    for defer in ("1", "0"):
+        monkeypatch.setenv("MTP_LM_DEFER", defer)
+        case = Case(cfg, norm="random", persistent_max_batch=-1)
+        _, _, ids, logits = check_forced(case, [0], tol)
+        check_free(case, [0], ids, logits, tol)
+        free = case.gpu_draft(forced=False)
+        got[defer] = (ids, logits, free[0], free[1], free[2], download_kv(free[3]))
+    a, b = got["1"], got["0"]
+    for x, y in zip(a[:5], b[:5]):
+        np.testing.assert_array_equal(x, y)
+    for f in ("k_pool", "v_pool", "seq_len", "pending"):
+        np.testing.assert_array_equal(getattr(a[5], f), getattr(b[5], f), err_msg=f)
