@@ -43,7 +43,7 @@ METRIC = "MTP draft+verify steps/s and accepted tok/s (Qwen3-8B shape); % HBM ro
 # dram__bytes_read.sum + dram__bytes_write.sum of one LM-head launch from an ncu capture of the
 # current kernel (profiles/lm_head_argmax_qwen3_8b_mtp_b1.md); other workloads report null.
 LM_TRAFFIC = {
-    "qwen3_8b_mtp_b1": 1244798464 + 3557376,
+    "qwen3_8b_mtp_b1": 1244766976 + 3336448,
     "qwen3_8b_mtp_b1:int4_g64": 622737408 + 3309056,
 }
 # The same for one verify launch (profiles/verify_rollback_b64.md).
