@@ -186,6 +186,12 @@ mtp_status mtp_init(const mtp_config* cfg, const mtp_weights* weights, int devic
   }
   ctx->attn_max_splits = 64;
   ctx->attn_force_bps = 0;
+  // MTP_ATTN_CLUSTER=0 keeps the split combine through HBM partials (comparison)
+  ctx->attn_cluster = 1;
+  ctx->attn_cl_key = -1;
+  ctx->attn_cl_fit = 0;
+  ctx->attn_cl_bps = 0;
+  if (const char* env = getenv("MTP_ATTN_CLUSTER")) ctx->attn_cluster = (int)strtol(env, nullptr, 0) != 0;
   if (const char* env = getenv("MTP_ATTN_BPS")) {
     const long v = strtol(env, nullptr, 0);
     if (v >= 1 && v <= 4096) ctx->attn_force_bps = (int)v;

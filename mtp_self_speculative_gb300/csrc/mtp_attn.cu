@@ -19,6 +19,7 @@
 // sum per head, base-2 exponentials with the scale folded into q).  Warps
 // merge in shared memory; splits merge in the last CTA to finish (arrival
 // counter), which writes o and resets the counter.
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -424,6 +425,100 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
   attn_finish<T, HD, G, DPL>(a, smem_raw, wm, wl, m, l, acc, warp, lane, s, g, b, nsplit);
 }
 
+// ------------------------------------------------ split combine in a cluster
+//
+// All splits of one (request, kv head) form one thread-block cluster (at most
+// 16 CTAs).  Each CTA merges its warps' online-softmax states into one
+// partial (M, L, O) per query head in its own shared memory; after a cluster
+// barrier, CTA r combines output columns r, r + S, ... (S = cluster size, one
+// column = 4 values of one head), 16 lanes per column, lane j reading split
+// j's partial through distributed shared memory; a second barrier keeps every
+// CTA's partial alive until all reads are done.  Splits with no blocks hold
+// an empty state (M = -inf), so the combine is the same as the global one:
+// no partials in HBM, no arrival counter, no last-CTA pass.
+
+__device__ __forceinline__ uint32_t attn_mapa(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void attn_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int HD, int G, int W>
+__device__ void attn_finish_cluster(const AttnArgs<uint16_t>& a, const float* wacc, float (*wm)[G], float (*wl)[G],
+                                    float* cpart, int g, int b) {
+  constexpr int RS = HD + 4;  // partial row: M, L, -, -, O[HD] (16-byte aligned)
+  constexpr int NT = W * 32;
+  constexpr int ITEMS = G * (HD / 4);
+  for (int idx = threadIdx.x; idx < G * HD; idx += NT) {
+    const int h = idx / HD, d = idx - h * HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w][h]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float f = (wm[w][h] == -INFINITY) ? 0.0f : exp2f(wm[w][h] - M);
+      L += wl[w][h] * f;
+      O += wacc[((size_t)w * G + h) * HD + d] * f;
+    }
+    if (d == 0) {
+      cpart[h * RS] = M;
+      cpart[h * RS + 1] = L;
+    }
+    cpart[h * RS + 4 + d] = O;
+  }
+  attn_cluster_sync();
+  const int S = (int)gridDim.x;  // the cluster spans the grid's x
+  const int r = (int)blockIdx.x;
+  const int per = (ITEMS + S - 1) / S;
+  const uint32_t base = smem_addr(cpart);
+  for (int t0 = 0; t0 < per * 16; t0 += NT) {
+    const int t = t0 + (int)threadIdx.x;
+    const int j = t & 15;
+    const int item = r + (t >> 4) * S;
+    const bool have = (t < per * 16) && item < ITEMS;
+    const int h = have ? item / (HD / 4) : 0, d4 = have ? item - h * (HD / 4) : 0;
+    float Mr = -INFINITY, Lr = 0.0f;
+    float4 Or = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (have && j < S) {
+      const uint32_t row = attn_mapa(base + (uint32_t)(h * RS) * 4u, (uint32_t)j);
+      float2 ml;
+      asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(ml.x), "=f"(ml.y) : "r"(row));
+      asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(Or.x), "=f"(Or.y), "=f"(Or.z), "=f"(Or.w)
+                   : "r"(row + 16u + 16u * (uint32_t)d4));
+      Mr = ml.x;
+      Lr = ml.y;
+      if (Mr == -INFINITY) {
+        Lr = 0.0f;
+        Or = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+    // merge the 16 lanes of the column (xor offsets below 16 stay in the group)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, Mr, o), l2 = __shfl_xor_sync(0xffffffffu, Lr, o);
+      float4 o2;
+      o2.x = __shfl_xor_sync(0xffffffffu, Or.x, o);
+      o2.y = __shfl_xor_sync(0xffffffffu, Or.y, o);
+      o2.z = __shfl_xor_sync(0xffffffffu, Or.z, o);
+      o2.w = __shfl_xor_sync(0xffffffffu, Or.w, o);
+      merge_state(Mr, Lr, Or, m2, l2, o2);
+    }
+    if (have && j == 0) {
+      const float inv = 1.0f / Lr;
+      attn_store_out<uint16_t, HD, G>(a, b, g, h, 4 * d4 + 0, Or.x * inv);
+      attn_store_out<uint16_t, HD, G>(a, b, g, h, 4 * d4 + 1, Or.y * inv);
+      attn_store_out<uint16_t, HD, G>(a, b, g, h, 4 * d4 + 2, Or.z * inv);
+      attn_store_out<uint16_t, HD, G>(a, b, g, h, 4 * d4 + 3, Or.w * inv);
+    }
+  }
+  attn_cluster_sync();
+}
+
 // ------------------------------------------------ tensor-core attention
 //
 // bf16 cache, head_dim 128.  Same split-KV grid and per-warp block ownership
@@ -431,7 +526,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs<T>
 // the group's query heads on M, P kept in registers) on K/V tiles staged by
 // swizzled 2-D tensor-map loads.
 
-template <int G, int W, int NSTG>
+template <int G, int W, int NSTG, bool CL>
 __global__ void __launch_bounds__(W * 32, (W <= 4) ? 2 : 1)
     attn_mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const AttnArgs<uint16_t> a) {
@@ -457,7 +552,9 @@ __global__ void __launch_bounds__(W * 32, (W <= 4) ? 2 : 1)
   const int T_len = a.seq_len[b] + a.k;
   const int nblk = (T_len + 15) >> 4;
   const int blk0 = s * a.bps;
-  if (blk0 >= nblk || T_len <= 0) return;
+  // in a cluster every split stays to the combine (T_len is the cluster's
+  // own, so that return is cluster-uniform)
+  if (T_len <= 0 || (!CL && blk0 >= nblk)) return;
   const int blk1 = min(nblk, blk0 + a.bps);
   const int nsplit = (nblk + a.bps - 1) / a.bps;
 
@@ -528,16 +625,54 @@ __global__ void __launch_bounds__(W * 32, (W <= 4) ? 2 : 1)
     }
   }
   __syncthreads();
-  attn_finish_merged<uint16_t, HD, G, W>(a, wacc, wm, wl, s, g, b, nsplit);
+  if constexpr (CL)
+    attn_finish_cluster<HD, G, W>(a, wacc, wm, wl, wacc + (size_t)W * G * HD, g, b);
+  else
+    attn_finish_merged<uint16_t, HD, G, W>(a, wacc, wm, wl, s, g, b, nsplit);
 }
 
 template <int G, int W, int NSTG>
 static cudaError_t attn_mma_launch(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap& km,
                                    const CUtensorMap& vm, const AttnArgs<uint16_t>& ab) {
-  auto kern = attn_mma_kernel<G, W, NSTG>;
+  auto kern = attn_mma_kernel<G, W, NSTG, false>;
   const cudaError_t e = ensure_smem((const void*)kern, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, grid, dim3(W * 32), smem, s, km, vm, ab);
+}
+
+// The cluster form: grid.x splits (2..16) of one (request, kv head) per
+// cluster.  `query` only asks how many such clusters fit on the GPU at once.
+template <int G>
+static cudaError_t attn_cluster_launch(dim3 grid, size_t smem, cudaStream_t s, const CUtensorMap* km,
+                                       const CUtensorMap* vm, const AttnArgs<uint16_t>* ab, int* query) {
+  auto kern = attn_mma_kernel<G, 8, 2, true>;
+  cudaError_t e = ensure_smem((const void*)kern, smem);
+  if (e != cudaSuccess) return e;
+  static bool nonportable = false;
+  if (!nonportable) {
+    e = cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    nonportable = true;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3(8 * 32);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = grid.x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  if (query) {
+    lc.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(query, (const void*)kern, &lc);
+  }
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, kern, *km, *vm, *ab);
 }
 
 template <typename T, int HD, int G>
@@ -633,6 +768,62 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
     const CUtensorMap& vm = *vmp;
     const AttnArgs<uint16_t>& ab = reinterpret_cast<const AttnArgs<uint16_t>&>(a);
     dim3 grid(splits, c.n_kv_heads, B);
+    if (ctx->attn_cluster && (G == 1 || G == 2 || G == 4 || G == 8)) {
+      // every split of a (request, kv head) in one cluster of at most 16
+      // CTAs: the largest cluster size (from the planned split) whose
+      // B * n_kv clusters all fit on the GPU at once, planned once per
+      // (capacity, G, clusters, forced split) and cached
+      const long long key = ((long long)kv->max_blocks << 40) | ((long long)G << 32) |
+                            ((long long)(c.n_kv_heads * B) << 12) | (long long)(a.bps & 0xfff);
+      if (ctx->attn_cl_key != key) {
+        ctx->attn_cl_key = key;
+        ctx->attn_cl_fit = 0;
+        ctx->attn_cl_bps = 0;
+        int cs0 = (kv->max_blocks + a.bps - 1) / a.bps;
+        if (cs0 > 16) cs0 = (ctx->attn_force_bps == 0) ? 16 : 0;
+        // fewer splits lengthen every CTA's serial part: at most a quarter fewer
+        const int want_min = (3 * cs0 + 3) / 4 > 2 ? (3 * cs0 + 3) / 4 : 2;
+        for (int want = cs0; want >= want_min; --want) {
+          const int bps = (kv->max_blocks + want - 1) / want;
+          const int cs = (kv->max_blocks + bps - 1) / bps;
+          if ((long long)cs * c.n_kv_heads * B > 2LL * ctx->num_sms) continue;
+          const size_t smem = 1024 + (size_t)8 * 2 * 2 * 4096 + block_slice_bytes(bps);
+          const dim3 gc(cs, c.n_kv_heads, B);
+          int fit = 0;
+          cudaError_t eq = (G == 1)   ? attn_cluster_launch<1>(gc, smem, s, nullptr, nullptr, nullptr, &fit)
+                           : (G == 2) ? attn_cluster_launch<2>(gc, smem, s, nullptr, nullptr, nullptr, &fit)
+                           : (G == 4) ? attn_cluster_launch<4>(gc, smem, s, nullptr, nullptr, nullptr, &fit)
+                                      : attn_cluster_launch<8>(gc, smem, s, nullptr, nullptr, nullptr, &fit);
+          if (eq != cudaSuccess) {
+            cudaGetLastError();
+            fit = 0;
+          }
+          if (getenv("MTP_ATTN_TRACE"))
+            fprintf(stderr, "attention cluster: %d splits of %d blocks, G %d, %zu B smem: %d clusters fit, %d needed\n",
+                    cs, bps, G, smem, fit, c.n_kv_heads * B);
+          if (fit >= c.n_kv_heads * B) {
+            ctx->attn_cl_fit = cs;
+            ctx->attn_cl_bps = bps;
+            break;
+          }
+          if (ctx->attn_force_bps) break;  // a forced split size is taken as it is or not at all
+        }
+      }
+      if (ctx->attn_cl_fit >= 2) {
+        const int cs = ctx->attn_cl_fit, bps = ctx->attn_cl_bps;
+        const size_t smem = 1024 + (size_t)8 * 2 * 2 * 4096 + block_slice_bytes(bps);
+        const dim3 gc(cs, c.n_kv_heads, B);
+        AttnArgs<uint16_t> ac = ab;
+        ac.bps = bps;
+        ac.max_splits = cs;
+        switch (G) {
+          case 1: return attn_cluster_launch<1>(gc, smem, s, &km, &vm, &ac, nullptr);
+          case 2: return attn_cluster_launch<2>(gc, smem, s, &km, &vm, &ac, nullptr);
+          case 4: return attn_cluster_launch<4>(gc, smem, s, &km, &vm, &ac, nullptr);
+          case 8: return attn_cluster_launch<8>(gc, smem, s, &km, &vm, &ac, nullptr);
+        }
+      }
+    }
     if (wide) {
       // few CTAs: 8 warps of 2 stages each, every tile of a 16-block split
       // requested at once

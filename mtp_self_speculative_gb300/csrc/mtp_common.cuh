@@ -280,6 +280,9 @@ struct mtp_ctx {
   int gemv_budget_kb[6];         // shared memory per streamed-kernel CTA, per kind
   int lm_rows;                   // LM head of 2..4 requests on the tensor cores (0: streamed GEMV)
   int attn_force_bps;            // attention blocks per split (0: planned; tuning)
+  int attn_cluster;              // tensor-core attention: splits combined in a thread-block cluster
+  long long attn_cl_key;         // (capacity, G, clusters, split) of the cached cluster plan
+  int attn_cl_fit, attn_cl_bps;  // ... its cluster size (0: none fits) and blocks per split
   int lm_balance;                // streamed LM head sizes each CTA's range by its SM's measured rate
   int lm_defer;                  // one request: the next eh_proj reduces the LM head's per-CTA keys
   int lm_defer_pending, lm_defer_grid;  // the last LM head launch deferred its argmax, over this many CTAs
