@@ -22,7 +22,8 @@
 //   * kinds with at least as many 128-row tiles as CTAs (LM head, large
 //     FFNs) take whole tiles, a balanced contiguous range per CTA, with two
 //     TMEM accumulators so the epilogue of one tile overlaps the next tile's
-//     MMAs;
+//     MMAs (the LM head's ranges are counted in 16-row units, its last tile
+//     per CTA loaded as 16-row boxes);
 //   * kinds with fewer tiles than CTAs are split along K over a thread-block
 //     cluster of S <= 8 CTAs per tile: each CTA accumulates its K-slice in
 //     TMEM, parks the partial tile in its (drained) stage memory, and after a
@@ -204,6 +205,7 @@ __device__ void qkv_meta_fill(const TcArgs& a, QkvMeta* meta, int tid, int nthre
 
 struct EpiCtx {
   int tile, m, lane, quarter;  // m = row of the tile held by this thread
+  int row0, row_end;           // LM head: first row of the tile, end of the CTA's rows
   float* xbuf;                 // [64][16] exchange buffer
   const float* rms;            // [B] RMS factor per request (1 unless folded)
   unsigned long long* cta_best;
@@ -317,8 +319,10 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
     return;
   }
   if (kind == TC_LM) {
-    const int r = e.tile * 128 + e.m;
-    const bool row_ok = r < a.V;
+    // rows at or past row_end are another CTA's (or past the vocabulary):
+    // their accumulators hold whatever the stage's unused rows held
+    const int r = e.row0 + e.m;
+    const bool row_ok = r < e.row_end;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int b = c0 + j;
@@ -330,7 +334,7 @@ __device__ void tc_epilogue(const TcArgs& a, const EpiCtx& e, int c0, const floa
       const uint32_t mx = __reduce_max_sync(0xffffffffu, ord);
       const uint32_t bal = __ballot_sync(0xffffffffu, ord == mx);
       if (e.lane == (b & 31)) {
-        const uint32_t row = (uint32_t)(e.tile * 128 + e.quarter * 32 + (__ffs(bal) - 1));
+        const uint32_t row = (uint32_t)(e.row0 + e.quarter * 32 + (__ffs(bal) - 1));
         const unsigned long long key = ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - row);
         atomicMax(e.cta_best + b, key);
       }
@@ -413,11 +417,27 @@ __device__ __forceinline__ void cluster_sync_all() {
 //   ksplit == 1: whole tiles, a balanced contiguous range per CTA.
 //   ksplit == S: CTA blockIdx.x is rank r of the cluster for tile
 //                blockIdx.x / S and owns k-blocks [r*nkb/S, (r+1)*nkb/S).
+//   LM head: a balanced contiguous range of rows [r0, r1) in 16-row units,
+//                as tiles of 128 rows from r0 (the last one may be shorter):
+//                every CTA streams within 16 rows of the same bytes.
 struct SegList {
   int t0, count, k0, k1;  // ksplit == 1: tiles t0..t0+count-1 with [0, nkb)
+  int r0, r1;             // LM head: the CTA's rows
 };
 __device__ __forceinline__ SegList seg_list(const TcArgs& a) {
   SegList L;
+  L.r0 = L.r1 = 0;
+  if (a.kind == TC_LM) {
+    const long long G = gridDim.x, U = (a.V + 15) / 16;
+    const int u0 = (int)(((long long)blockIdx.x * U) / G), u1 = (int)(((long long)(blockIdx.x + 1) * U) / G);
+    L.r0 = min(16 * u0, a.V);
+    L.r1 = min(16 * u1, a.V);
+    L.t0 = 0;
+    L.count = (L.r1 - L.r0 + 127) / 128;
+    L.k0 = 0;
+    L.k1 = a.nkb;
+    return L;
+  }
   if (a.ksplit == 1) {
     const long long G = gridDim.x;
     L.t0 = (int)(((long long)blockIdx.x * a.n_tiles) / G);
@@ -496,9 +516,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
           else if (tile < a.n_q + a.n_kv)
             tma_load_2d_hint(dst, &maps.a1, kb * 64, (tile - a.n_q) * 128, &full_bar[st], pol);
           else tma_load_2d_hint(dst, &maps.a2, kb * 64, (tile - a.n_q - a.n_kv) * 128, &full_bar[st], pol);
+        } else if (a.kind == TC_LM) {
+          // tile = segment: 128 rows from r0 + 128 * seg; a shorter last
+          // segment loads only its own 16-row boxes (map a1) -- each lands at
+          // a 2 KB offset, so the 128-byte swizzle pattern is the same
+          const int rb = L.r0 + 128 * tile;
+          const int nr = min(128, L.r1 - rb);
+          if (nr == 128) {
+            tma_load_2d_hint(dst, &maps.a0, kb * 64, rb, &full_bar[st], pol);
+          } else {
+            for (int i = 0; 16 * i < nr; ++i)
+              tma_load_2d_hint(dst + 2048 * i, &maps.a1, kb * 64, rb + 16 * i, &full_bar[st], pol);
+          }
         } else {
           tma_load_2d_hint(dst, &maps.a0, kb * 64, tile * 128, &full_bar[st], pol);
         }
+      };
+      // bytes of the A operand of a segment (tile index for the other kinds)
+      auto a_bytes = [&](int seg) -> uint32_t {
+        if (a.kind != TC_LM) return (uint32_t)kTcTileBytesA;
+        const int nr = min(128, L.r1 - (L.r0 + 128 * seg));
+        return nr == 128 ? (uint32_t)kTcTileBytesA : (uint32_t)(((nr + 15) / 16) * 2048);
       };
       auto issue_b = [&](int st, int kb) {
         tma_load_2d(smem + (size_t)st * stage_bytes + kTcTileBytesA, &maps.b, kb * 64, 0, &full_bar[st]);
@@ -506,7 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
       const int n_it = L.count * per_seg;
       const int pre = n_it < NS ? n_it : NS;
       for (int it = 0; it < pre; ++it) {
-        mbar_expect_tx(&full_bar[it], stage_bytes);
+        mbar_expect_tx(&full_bar[it], a_bytes(it / per_seg) + bytes_b);
         issue_a(it, L.t0 + it / per_seg, L.k0 + it % per_seg);
       }
       pdl_wait();
@@ -518,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
           set_error(a.err, MTP_ERR_TIMEOUT);
           break;
         }
-        mbar_expect_tx(&full_bar[st], stage_bytes);
+        mbar_expect_tx(&full_bar[st], a_bytes(it / per_seg) + bytes_b);
         issue_a(st, L.t0 + it / per_seg, L.k0 + it % per_seg);
         issue_b(st, L.k0 + it % per_seg);
       }
@@ -588,6 +626,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) mtp_tc_proj_kernel(const __grid
     for (int seg = 0; seg < L.count; ++seg) {
       const int buf = seg & 1;
       e.tile = L.t0 + seg;
+      e.row0 = L.r0 + 128 * seg;
+      e.row_end = L.r1;
       bool ok = tc_wait(&accf_bar[buf], (seg >> 1) & 1, &abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok && lane == 0) {
@@ -894,7 +934,8 @@ static TcPlan* tc_plan(mtp_ctx* ctx, cudaStream_t s, int kind, int NT) {
       break;
     default:
       C = c.hidden; n_tiles = (c.vocab + 127) / 128;
-      ok = make_map(&maps.a0, w.lm_head, c.vocab, C, 128) && make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
+      ok = make_map(&maps.a0, w.lm_head, c.vocab, C, 128) && make_map(&maps.a1, w.lm_head, c.vocab, C, 16) &&
+           make_map(&maps.b, ctx->tc_xn, c.max_batch, C, NT);
       break;
   }
   if (!ok) return nullptr;

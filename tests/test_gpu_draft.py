@@ -347,21 +347,25 @@ def test_long_context_small_batch_split_combine_bf16(n_q):
 
 
 
-@pytest.mark.parametrize("B", [1, 4])
+@pytest.mark.parametrize("B", [1, 4, 24])
 def test_lm_head_weighted_ranges_are_bit_identical(B, monkeypatch):
-    """The LM heads size each CTA's range of vocabulary rows by its SM's
-    measured streaming rate, claimed through a packed (ticket, next unit)
-    counter.  Every logit is one warp's (1 request) or one tile column's
-    (2-4 requests) dot product whichever CTA owns its row, so repeated drafts
-    -- whose ranges change as the rate table settles -- and drafts over equal
-    ranges give the same logits and ids bit for bit, and both match the
-    oracle.  60001 rows give every CTA many units."""
+    """The 1-4-request LM heads size each CTA's range of vocabulary rows by
+    its SM's measured streaming rate, claimed through a packed (ticket, next
+    unit) counter.  Every logit is one warp's (1 request) or one tile
+    column's (2-4 requests) dot product whichever CTA owns its row, so
+    repeated drafts -- whose ranges change as the rate table settles -- and
+    drafts over equal ranges give the same logits and ids bit for bit, and
+    both match the oracle.  The tcgen05 LM head (24 requests) takes equal
+    ranges in 16-row units, so a CTA's last 128-row tile is often short and
+    its unused accumulator rows hold stale stage data that must not reach
+    the argmax.  60001 rows give every CTA many units and a last unit of one
+    row."""
     cfg = synth.MTPShape("balance_bf16", H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=60001, batch=B, K=3,
                          dtype="bf16", ctx_lo=40, ctx_hi=90, seed_index=58)
     got = {}
     for bal in ("1", "0"):
         monkeypatch.setenv("MTP_LM_BALANCE", bal)
-        case = Case(cfg, norm="random", persistent_max_batch=-1)
+        case = Case(cfg, norm="random", persistent_max_batch=-1, tc_min_batch=1 if B > 4 else 0)
         _, _, ids, logits = check_forced(case, list(range(B)), LOGIT_TOL)
         for _ in range(3):
             ids2, logits2, _, _ = case.gpu_draft(forced=True)
