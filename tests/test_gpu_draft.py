@@ -6,6 +6,8 @@ normwise tolerance, draft ids equal except at the oracle's near-ties, the
 appended KV entries within tolerance, every other KV slot bit-identical.  The
 free-running GPU chain is checked against the free-running oracle chain up to
 the first (legitimate) near-tie divergence."""
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -404,18 +406,29 @@ def test_deferred_argmax_matches_last_cta_argmax(dtype, vocab, monkeypatch):
 
 @pytest.mark.parametrize("cluster", ["1", "0"])
 @pytest.mark.parametrize("n_q,lens", [(8, [200]), (8, [200, 0, 37]), (16, [150, 3]), (2, [90, 180])])
-def test_attention_split_combine_in_a_cluster(cluster, n_q, lens, monkeypatch):
+def test_attention_split_combine_in_a_cluster(cluster, n_q, lens, monkeypatch, capfd):
     """One block per split (up to 14 splits) so that every request's splits
     form one thread-block cluster that combines them through distributed
     shared memory (cluster=1), or write partials to HBM for the last CTA
     (cluster=0).  Requests of 0+k and 3+k tokens leave most CTAs of their
     cluster without blocks; G = 4, 8 and 1 query heads per kv head.  Both
-    forms match the oracle."""
+    forms match the oracle.  The plan trace shows which form ran: with at
+    most four clusters needed they all fit on the GPU at once, so the cluster
+    form is the one tested."""
     monkeypatch.setenv("MTP_ATTN_CLUSTER", cluster)
     monkeypatch.setenv("MTP_ATTN_BPS", "1")
+    monkeypatch.setenv("MTP_ATTN_TRACE", "1")
     cfg = synth.MTPShape("cluster_bf16", H=512, n_q=n_q, n_kv=2, head_dim=128, ffn=1536, vocab=5003,
                          batch=len(lens), K=3, dtype="bf16", ctx_lo=0, ctx_hi=200, seed_index=62)
     case = Case(cfg, norm="random", lens=lens, persistent_max_batch=-1)
     subset = list(range(len(lens)))
     _, _, ids, logits = check_forced(case, subset, LOGIT_TOL)
     check_free(case, subset, ids, logits, LOGIT_TOL)
+    plans = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("attention cluster:")]
+    if cluster == "0":
+        assert not plans
+    else:
+        assert plans, "no attention cluster plan was made"
+        fit, needed = (int(w) for w in re.findall(r"(\d+) clusters fit, (\d+) needed", plans[-1])[0])
+        if needed <= 4:
+            assert fit >= needed, plans[-1]
