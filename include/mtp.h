@@ -497,6 +497,22 @@ mtp_status mtp_profile_end(mtp_ctx* ctx, float* ms_out, int max_out, int* n_out)
  * entry points), for launch accounting. */
 int64_t mtp_launch_count(const mtp_ctx* ctx);
 
+/* Launch-time path choices the context has taken since creation, for tests
+ * and diagnostics (which of two equivalent forms ran).  Ids for
+ * mtp_path_count: */
+typedef enum {
+  MTP_PATH_LM_DEFERRED = 0,  /* one-request draft steps before the last whose LM head left its argmax
+                                to the next step's eh_proj ("MTP (Multi-Token Prediction)",
+                                "Architecture": each step's token feeds the next step) */
+  MTP_PATH_ATTN_CLUSTER = 1, /* attention launches whose splits were combined in a thread-block
+                                cluster instead of through HBM partials */
+  MTP_PATH_COUNT = 2
+} mtp_path_id;
+
+/* Count of path `path` (an mtp_path_id); 0 for a NULL context or an unknown
+ * id.  Host-side counter, no synchronisation. */
+int64_t mtp_path_count(const mtp_ctx* ctx, int path);
+
 #ifdef __cplusplus
 }
 #endif

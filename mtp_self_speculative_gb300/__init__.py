@@ -435,3 +435,12 @@ def mtp_profile_end(ctx: Context, max_out: int = 1 << 16):
 
 def mtp_launch_count(ctx: Context) -> int:
     return int(_clib.mtp_launch_count(ctx.handle))
+
+
+MTP_PATH_LM_DEFERRED = 0
+MTP_PATH_ATTN_CLUSTER = 1
+
+
+def mtp_path_count(ctx: Context, path: int) -> int:
+    """How often the context took launch-time path `path` (include/mtp.h)."""
+    return int(_clib.mtp_path_count(ctx.handle, int(path)))

@@ -102,6 +102,7 @@ SIGNATURES = {
     "mtp_profile_begin": (c_int, [c_void_p, c_int, c_int]),
     "mtp_profile_end": (c_int, [c_void_p, ctypes.POINTER(c_float), c_int, ctypes.POINTER(c_int)]),
     "mtp_launch_count": (c_int64, [c_void_p]),
+    "mtp_path_count": (c_int64, [c_void_p, c_int]),
 }
 
 _lib = None

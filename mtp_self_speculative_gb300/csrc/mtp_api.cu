@@ -529,4 +529,9 @@ mtp_status mtp_profile_end(mtp_ctx* ctx, float* ms_out, int max_out, int* n_out)
 
 int64_t mtp_launch_count(const mtp_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
+int64_t mtp_path_count(const mtp_ctx* ctx, int path) {
+  if (!ctx || path < 0 || path >= MTP_PATH_COUNT) return 0;
+  return ctx->path_counts[path];
+}
+
 }  // extern "C"

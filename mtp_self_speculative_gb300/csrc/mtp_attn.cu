@@ -816,6 +816,7 @@ static cudaError_t attention_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, const
         AttnArgs<uint16_t> ac = ab;
         ac.bps = bps;
         ac.max_splits = cs;
+        ctx->path_counts[MTP_PATH_ATTN_CLUSTER]++;
         switch (G) {
           case 1: return attn_cluster_launch<1>(gc, smem, s, &km, &vm, &ac, nullptr);
           case 2: return attn_cluster_launch<2>(gc, smem, s, &km, &vm, &ac, nullptr);

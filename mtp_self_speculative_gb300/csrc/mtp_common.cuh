@@ -271,6 +271,7 @@ struct mtp_ctx {
   int prof_n;
   cudaEvent_t* prof_ev;  // 2 * prof_cap
   long long launches;
+  long long path_counts[MTP_PATH_COUNT];  // mtp_path_count
   // host-side caches (tensor maps need 64-byte aligned storage)
   void* tc_plan_cache;          // TcPlan[6][17], lazily allocated
   void* attn_map_cache;         // AttnMapCache, lazily allocated

@@ -633,6 +633,7 @@ static cudaError_t draft_step_t(mtp_ctx* ctx, cudaStream_t s, int B, int k, int 
   if ((e = launch_kind<T, DOWN>(ctx, s, a)) != cudaSuccess) return e;
   if ((e = launch_kind<T, LM_HEAD>(ctx, s, a)) != cudaSuccess) return e;
   if (a.defer_out) {
+    ctx->path_counts[MTP_PATH_LM_DEFERRED]++;
     ctx->lm_defer_pending = 1;
     ctx->lm_defer_grid = min(ctx->num_sms, (a.V + 1) / 2);
     ctx->lm_defer_tick = a.lm_tick;

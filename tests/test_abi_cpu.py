@@ -83,6 +83,7 @@ def test_calls_without_context_are_rejected(lib):
     assert lib.mtp_selftest_wait_timeout(None, None, 0) == _lib.MTP_ERR_INVALID
     assert lib.mtp_profile_begin(None, 0, 1) == _lib.MTP_ERR_INVALID
     assert lib.mtp_launch_count(None) == 0
+    assert lib.mtp_path_count(None, 0) == 0
     lib.mtp_destroy(None)
 
 

@@ -388,6 +388,7 @@ def test_deferred_argmax_matches_last_cta_argmax(dtype, vocab, monkeypatch):
     than there are SMs."""
     cfg = synth.MTPShape("defer_" + dtype, H=512, n_q=8, n_kv=2, head_dim=128, ffn=1536, vocab=vocab, batch=1, K=5,
                          dtype=dtype, ctx_lo=40, ctx_hi=90, seed_index=61)
+    import mtp_self_speculative_gb300 as M
     tol = F32_LOGIT_TOL if dtype == "f32" else LOGIT_TOL
     got = {}
     for defer in ("1", "0"):
@@ -397,6 +398,10 @@ def test_deferred_argmax_matches_last_cta_argmax(dtype, vocab, monkeypatch):
         check_free(case, [0], ids, logits, tol)
         free = case.gpu_draft(forced=False)
         got[defer] = (ids, logits, free[0], free[1], free[2], download_kv(free[3]))
+        # every draft call (forced, free, free again: three) defers K-1 of
+        # its K steps, or none
+        deferred = M.mtp_path_count(case.ctx, M.MTP_PATH_LM_DEFERRED)
+        assert deferred == (3 * (cfg.K - 1) if defer == "1" else 0), deferred
     a, b = got["1"], got["0"]
     for x, y in zip(a[:5], b[:5]):
         np.testing.assert_array_equal(x, y)
@@ -424,11 +429,14 @@ def test_attention_split_combine_in_a_cluster(cluster, n_q, lens, monkeypatch, c
     subset = list(range(len(lens)))
     _, _, ids, logits = check_forced(case, subset, LOGIT_TOL)
     check_free(case, subset, ids, logits, LOGIT_TOL)
+    import mtp_self_speculative_gb300 as M
+    launched = M.mtp_path_count(case.ctx, M.MTP_PATH_ATTN_CLUSTER)
     plans = [ln for ln in capfd.readouterr().err.splitlines() if ln.startswith("attention cluster:")]
     if cluster == "0":
-        assert not plans
+        assert not plans and launched == 0
     else:
         assert plans, "no attention cluster plan was made"
         fit, needed = (int(w) for w in re.findall(r"(\d+) clusters fit, (\d+) needed", plans[-1])[0])
+        assert (launched > 0) == (fit >= needed), (launched, plans[-1])
         if needed <= 4:
-            assert fit >= needed, plans[-1]
+            assert launched > 0, plans[-1]
