@@ -923,7 +923,7 @@ def loop_cpu_baseline(cfg, w, lens, h0, last0, thr, fmt) -> dict:
     OL.spec_loop(W, kv, st, cfg.K, thr, 1, cfg.dtype, embed_rows=dense)
     dt = time.perf_counter() - t
     n = sum(len(o) for o in st.out)
-    return {"value": n / dt, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+    return {"value": n / dt, "unit": "tok/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
             "sample": "1 loop step (K=%d draft steps, verifier rows, verify, commit), B=%d, float64 numpy" %
                       (cfg.K, len(lens))}
 
@@ -1053,7 +1053,7 @@ def run_verify_workload(args, cfg, rank, world, local_rank):
         "e2e": {"value": 1.0 / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": ver_bytes,
                 "d2h_bytes_per_step": 2 * B * 4},
         "gpu_launches": launches,
-        "cpu_baseline": {"value": cpu, "unit": "calls/s", "cores": blas_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": cpu, "unit": "calls/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
                          "sample": "%d full call(s): float64 numpy verify + commit of the same inputs" % reps},
         "clocks": clocks,
     }
@@ -1155,7 +1155,7 @@ def run_reference_verify(args, cfg, world):
                        "vocab": cfg.vocab, "verify_rows": int(vi.row_offsets[-1]), "context": int(lens[0]),
                        "l2": "L2 flushed between calls (256 MB read, outside the timed events); "
                              "%.1f MB of logits per call" % (ver_bytes / 1e6)},
-            "cpu_baseline": {"value": value, "unit": "calls/s", "cores": blas_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "calls/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
                              "sample": "%d full call(s): float64 numpy verify + commit of the same inputs%s" %
                                        (len(times), "; capped by the time budget" if len(times) < args.steps else "")},
             "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1218,7 +1218,7 @@ def run_reference_loop(args, cfg, world):
                                  "num_assistant_tokens": tree_shape[2]} if tree_shape else None),
                        "mean_emitted_per_step": toks / (B * len(dts)),
                        "l2": "inputs larger than L2 (weights streamed every draft step)"},
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": blas_threads(), "nproc": os.cpu_count(), "kind": "oracle",
                              "sample": "%d loop iteration(s) of the float64 numpy oracle%s" %
                                        (len(dts), "; capped by the time budget" if len(dts) < args.steps else "")},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1273,7 +1273,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "batch": len(lens), "draft_steps_K": cfg.K},
-            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "nproc": os.cpu_count(), "kind": "oracle",
                              "sample": "%d sampled draft step(s) of the float64 numpy oracle (decoder layer, "
                                        "LM head, argmax, verify), scaled by K=%d to a full step%s" %
                                        (len(times), cfg.K, "; capped by the time budget" if len(times) < args.steps
