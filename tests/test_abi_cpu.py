@@ -141,3 +141,18 @@ def test_stream_read_rejects_bad_arguments(lib):
 def test_bounds_selftest_needs_a_context(lib):
     from mtp_self_speculative_gb300 import _lib
     assert lib.mtp_selftest_bounds(None, None) == _lib.MTP_ERR_INVALID
+
+
+def test_binding_constants_equal_the_header_enums():
+    """Every enumerator of include/mtp.h (status codes, dtypes, weight formats,
+    kernel ids, path ids; the *_COUNT bounds aside) exists in the Python
+    binding with the header's value."""
+    import mtp_self_speculative_gb300 as M
+    text = open(HEADER).read()
+    enums = re.findall(r"\b(MTP_[A-Z0-9_]+)\s*=\s*(\d+)", text)
+    assert len(enums) >= 20
+    for name, value in enums:
+        if name.endswith("_COUNT"):
+            continue
+        assert hasattr(M, name), "binding lacks " + name
+        assert getattr(M, name) == int(value), name
